@@ -1,0 +1,498 @@
+"""Benchmark of the compressed-KV decode hot path (one JSON line on stdout).
+
+Metric: decode-attention layer-steps/s, with the achieved HBM bandwidth of the
+dominant kernel against the measured copy bandwidth of this GPU.
+
+A step is one decode step of one layer for the whole batch on a synthetic
+workload (see compressed_kv_sparse_append_gb300/workloads.py):
+  * CSA workloads (default: csa_128k = batch 8, 131072-token context, 32768
+    compressed entries, 128 heads, 64 indexer heads, top-512, mixed
+    FP8-nope/BF16-rope main KV, FP4 indexer keys): kv_append_quant of the
+    step's new compressed entry and indexer key, csa_index_topk,
+    csa_sparse_attn;
+  * hca_1m: kv_append_quant + hca_attn;
+  * csa2_group: one csa2_group_decode call (six layer-steps).
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream, with a 256 MB L2 flush (outside the events) before
+every step; barrier + max over ranks when launched with torchrun (each rank
+runs its own replica: batch sharding needs no collective).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn layer-steps/s at 128k/1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "layer-steps/s"
+KERNEL_SOURCES = ["append.cu", "indexer.cu", "indexer_umma.cu", "attention.cu", "api.cu",
+                  "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="csa_128k")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "compressed_kv_sparse_append_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """Per-launch DRAM bytes of `kernel_tag` from the committed ncu summary,
+    if it was captured on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash()
+    for line in open(path, encoding="utf-8"):
+        parts = line.strip().strip("|").split("|")
+        parts = [p.strip() for p in parts]
+        if len(parts) >= 4 and parts[0] == kernel_tag and parts[1] == cur:
+            try:
+                return float(parts[2])
+            except ValueError:
+                return None
+    return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            self.result = None
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        self.result = None if not sm else {
+            "sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+        return False
+
+
+# ------------------------------------------------------------------ setup --
+
+def setup_csa(wl, dev, ckv, wlmod):
+    """Cache planes of a CSA layer, filled through kv_append_quant."""
+    import torch
+    B, n = wl.B, wl.n_comp
+    cap = n + 8                     # room for the step's appended entry
+    kv = ckv.Plane(wl.main_fmt, 512, B, cap, dev)
+    win = ckv.Plane(wl.main_fmt, 512, B, wl.W, dev)
+    keys = ckv.Plane(wl.idx_fmt, 128, B, cap, dev)
+    ws = ckv.new_workspace(256, dev)
+    for b in range(B):
+        kvr, kr, wr = wlmod.sequence_rows(wl, b, n, dev)
+        base = torch.arange(n, dtype=torch.int64, device=dev) + b * cap
+        ckv.kv_append_quant(kv, kvr, base, ws=ws)
+        ckv.kv_append_quant(keys, kr, base, ws=ws)
+        ckv.kv_append_quant(win, wr, torch.arange(wl.W, dtype=torch.int64, device=dev) + b * wl.W, ws=ws)
+        if wl.ties:
+            # ~5 % exact ties crowded at the top-k boundary: rank this
+            # sequence's entries with the kernel's own scores, copy donors
+            q, qi, w = wlmod.step_queries(wl, 0, dev, batch=[b])
+            dbg = torch.zeros((1, n), device=dev)
+            one = ckv.Plane(wl.idx_fmt, 128, 1, cap, dev, data=keys.data[b:b + 1], scale=keys.scale[b:b + 1])
+            ckv.csa_index_topk(one, torch.tensor([n], dtype=torch.int32, device=dev), n, qi, w, wl.topk,
+                               dbg_scores=dbg)
+            order = torch.argsort(dbg[0], descending=True, stable=True).cpu()
+            kr2 = wlmod.inject_ties(kr, order, seed=wl.seed + b)
+            ckv.kv_append_quant(keys, kr2, base, ws=ws)
+        del kvr, kr, wr
+    torch.cuda.synchronize()
+    assert ckv.read_device_status(ws) == 0
+    return kv, win, keys, cap
+
+
+def make_step(wl, dev, ckv, wlmod):
+    """Returns (step_fn(timer), dominant-kernel tag, algorithmic bytes of the
+    dominant kernel per launch, launches per step, layer-steps per step,
+    host-input spec for the end-to-end run)."""
+    import torch
+    B = wl.B
+    n = wl.n_comp
+    tau = wl.tau
+    n_comp = torch.full((B,), n, dtype=torch.int32, device=dev)
+    win_len = torch.full((B,), wl.W, dtype=torch.int32, device=dev)
+    q, qi, w = wlmod.step_queries(wl, 0, dev)
+    if wl.kind == "csa":
+        kv, win, keys, cap = setup_csa(wl, dev, ckv, wlmod)
+        new_kv = wlmod.append_rows(wl, B, 512, 0, dev)
+        new_key = wlmod.append_rows(wl, B, 128, 1, dev)
+        slot = torch.arange(B, dtype=torch.int64, device=dev) * cap + n
+        idx = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((B, wl.H), device=dev)
+        ws = ckv.new_workspace(ckv.workspace_bytes(ckv.OP_INDEX_TOPK, B, wl.H, wl.HI, n, wl.topk, 0), dev)
+        ent = {"bf16": 256, "fp4": 72}[wl.idx_fmt]
+        main_row = {"bf16": 1024, "mixed": 580, "fp4": 288}[wl.main_fmt]
+        dom_bytes = B * n * ent + qi.numel() * 2 + w.numel() * 4 + idx.numel() * 4
+
+        def step(timer=None):
+            ckv.kv_append_quant(kv, new_kv, slot, ws=ws)
+            ckv.kv_append_quant(keys, new_key, slot, ws=ws)
+            if timer:
+                timer[0].record()
+            ckv.csa_index_topk(keys, n_comp, n, qi, w, wl.topk, out_idx=idx, ws=ws)
+            if timer:
+                timer[1].record()
+            ckv.csa_sparse_attn(kv, win, win_len, idx, q, tau, out=out, lse=lse, ws=ws)
+            return out
+
+        host = {"inputs": (q, qi, w, new_kv, new_key), "outputs": (out,)}
+        return step, "csa_index_topk", dom_bytes, 4, 1, host, ws
+    if wl.kind == "hca":
+        cap = n + 8
+        kv = ckv.Plane("bf16", 512, B, cap, dev)
+        win = ckv.Plane("bf16", 512, B, wl.W, dev)
+        ws = ckv.new_workspace(256, dev)
+        for b in range(B):
+            kvr, _, wr = wlmod.sequence_rows(wl, b, n, dev)
+            ckv.kv_append_quant(kv, kvr, torch.arange(n, dtype=torch.int64, device=dev) + b * cap, ws=ws)
+            ckv.kv_append_quant(win, wr, torch.arange(wl.W, dtype=torch.int64, device=dev) + b * wl.W, ws=ws)
+        new_kv = wlmod.append_rows(wl, B, 512, 0, dev)
+        slot = torch.arange(B, dtype=torch.int64, device=dev) * cap + n
+        out = torch.empty_like(q)
+        lse = torch.empty((B, wl.H), device=dev)
+        dom_bytes = B * (n + wl.W) * 1024 + q.numel() * 2 + out.numel() * 2
+
+        def step(timer=None):
+            ckv.kv_append_quant(kv, new_kv, slot, ws=ws)
+            if timer:
+                timer[0].record()
+            ckv.hca_attn(kv, n_comp, n, win, win_len, q, tau, out=out, lse=lse, ws=ws)
+            if timer:
+                timer[1].record()
+            return out
+
+        host = {"inputs": (q, new_kv), "outputs": (out,)}
+        return step, "hca_attn", dom_bytes, 2, 1, host, ws
+    # csa2 group
+    L = wl.n_layers
+    cap = n + 16
+    keys = ckv.Plane("fp4", 128, B, cap, dev)
+    kvs = [ckv.Plane("fp4", 512, B, cap, dev) for _ in range(L)]
+    wins = [ckv.Plane("fp4", 512, B, wl.W, dev) for _ in range(L)]
+    ws0 = ckv.new_workspace(256, dev)
+    for l in range(L):
+        for b in range(B):
+            kvr, kr, wr = wlmod.sequence_rows(wl, b, n, dev, layer=l)
+            base = torch.arange(n, dtype=torch.int64, device=dev) + b * cap
+            ckv.kv_append_quant(kvs[l], kvr, base, ws=ws0)
+            ckv.kv_append_quant(wins[l], wr, torch.arange(wl.W, dtype=torch.int64, device=dev) + b * wl.W, ws=ws0)
+            if l == 0:
+                ckv.kv_append_quant(keys, kr, base, ws=ws0)
+    qs, qis, ws_ = [], [], []
+    for l in range(L):
+        ql, qil, wl_ = wlmod.step_queries(wl, 0, dev, layer=l)
+        qs.append(ql)
+        qis.append(qil if l < 2 else None)
+        ws_.append(wl_ if l < 2 else None)
+    outs = [torch.empty_like(qs[0]) for _ in range(L)]
+    roles = [ckv.CSA2_FULL, ckv.CSA2_REINDEX] + [ckv.CSA2_REUSE] * (L - 2)
+    g = ckv.make_group(roles, [0, 0] + list(range(2, L)), [0, 0] + [0] * (L - 2), kvs, wins, keys, qs,
+                       qis, ws_, outs, pool_len=wl.pool_len)
+    app = wlmod.append_rows(wl, wl.n_append, 512, 0, dev)
+    per = wl.n_append // B
+    app_slot = (torch.arange(B, device=dev)[:, None] * cap + n + torch.arange(per, device=dev)[None]).flatten().to(torch.int64)
+    ws = ckv.new_workspace(ckv.workspace_bytes(ckv.OP_CSA2, B, wl.H, wl.HI, n, wl.topk, wl.pool_len), dev)
+    dom_bytes = (B * n * 72 + B * wl.pool_len * 72 + L * B * (wl.topk + wl.W) * 288
+                 + L * 2 * qs[0].numel() * 2 + wl.n_append * (1024 + 288))
+
+    def step(timer=None):
+        if timer:
+            timer[0].record()
+        ckv.csa2_group_decode(g, n_comp, n, win_len, B, wl.H, wl.HI, wl.topk, tau, append_dst=kvs[0],
+                              append_src=app, append_slot=app_slot, ws=ws)
+        if timer:
+            timer[1].record()
+        return outs[0]
+
+    host = {"inputs": tuple(qs) + tuple(t for t in qis + ws_ if t is not None) + (app,),
+            "outputs": tuple(outs)}
+    # launches: append + Full index + Reindex index + L attention
+    return step, "csa2_group_decode", dom_bytes, 3 + L, L, host, ws
+
+
+# ------------------------------------------------------------------ timing --
+
+def time_steps(step, K, W, dev):
+    import torch
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(W):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        step(timer=(ev[i][2], ev[i][3]))
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dom_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    return step_ms, dom_ms
+
+
+def time_e2e(step, host, K, W, dev):
+    """Same steps through the public API, with every step's inputs (queries,
+    indexer queries, head weights, new rows) copied from pinned host memory
+    into the device tensors the step reads, and the outputs copied back to
+    pinned host memory, inside the timed region."""
+    import torch
+    d_in = list(host["inputs"])
+    h_in = [t.cpu().pin_memory() for t in d_in]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in host["outputs"]]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def one():
+        for hsrc, ddst in zip(h_in, d_in):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for dsrc, hdst in zip(host["outputs"], h_out):
+            hdst.copy_(dsrc, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(W):
+        flush.zero_()
+        one()
+    tot = 0.0
+    for _ in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        one()
+        e1.record()
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+    return tot / K, bi, bo
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_oracle_sample(wl, budget_s):
+    """Times the oracle (as it stands) on a bounded sample of the workload:
+    whole sequences of one layer-step, generated on the host with the same
+    recipe.  Returns (layer-steps/s, cores, sample description, seconds)."""
+    import numpy as np
+    from compressed_kv_sparse_append_gb300 import workloads as wlmod
+    from oracle import attention as oa, fp_formats as ff, indexer as oi, csa2 as oc
+
+    f = lambda t: t.float().numpy()
+    n = wl.n_comp
+    t_total, seqs = 0.0, 0
+    b = 0
+    while t_total < budget_s and seqs < 64:
+        kv, keys, win = wlmod.sequence_rows(wl, b % wl.B, n, "cpu")
+        q, qi, w = wlmod.step_queries(wl, 0, "cpu", batch=[b % wl.B])
+        kvf, winf = f(kv), f(win)
+        t0 = time.perf_counter()
+        if wl.kind == "hca":
+            d, s = ff.quantize_entries(kvf[:1], "bf16")            # the step's append
+            kd, ks = ff.quantize_entries(kvf, "bf16")
+            wd, wsc = ff.quantize_entries(winf, "bf16")
+            oa.hca_attention(f(q[0]), kd, ks, "bf16", n, wd, wsc, wl.W, wl.tau)
+            layers = 1
+        elif wl.kind == "csa":
+            kd, ks = ff.quantize_entries(kvf, wl.main_fmt)
+            wd, wsc = ff.quantize_entries(winf, wl.main_fmt)
+            kk, kks = ff.quantize_entries(f(keys), wl.idx_fmt)
+            kvals = ff.dequantize_entries(kk, kks, wl.idx_fmt)
+            qv = oi.indexer_query(f(qi[0]), wl.idx_fmt == "fp4")
+            sc = oi.index_scores(qv, f(w[0]).astype(np.float64), kvals)
+            idx = oi.topk_set(sc, wl.topk)
+            oa.csa_sparse_attention(f(q[0]), kd, ks, wl.main_fmt, idx, wd, wsc, wl.W, wl.tau)
+            layers = 1
+        else:
+            kk, kks = ff.fp4_quantize(f(keys))
+            kvals = ff.fp4_dequantize(kk, kks)
+            kd, ks = ff.fp4_quantize(kvf)
+            wd, wsc = ff.fp4_quantize(winf)
+            L = wl.n_layers
+            qis = [f(qi[0])] * L
+            wsl = [f(w[0]).astype(np.float64)] * L
+            qs = [f(q[0])] * L
+            roles = [oc.FULL, oc.REINDEX] + [oc.REUSE] * (L - 2)
+            oc.csa2_group_sequence(roles, [0] * L, [0] * L, kvals, n, qis, wsl, True, wl.topk,
+                                   wl.pool_len, qs, [(kd, ks, "fp4")] * L, [(wd, wsc)] * L, wl.W, wl.tau)
+            layers = L
+        t_total += time.perf_counter() - t0
+        seqs += 1
+        b += 1
+    per_layer_step = t_total / seqs * wl.B / layers   # whole batch, one layer
+    desc = "%d sequence(s) x 1 layer-step of %s (of batch %d), oracle float64 NumPy, %.1f s" % (
+        seqs, wl.name, wl.B, t_total)
+    return 1.0 / per_layer_step, os.cpu_count(), desc, t_total
+
+
+# ------------------------------------------------------------------- main --
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    return dist.get_rank(), ws, dist
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, wl, rank, world, dist):
+    if rank != 0:
+        return
+    budget = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, cores, desc, secs = cpu_oracle_sample(wl, budget)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "context_tokens": wl.T,
+            "compressed_entries": wl.n_comp, "heads": wl.H, "indexer_heads": wl.HI, "topk": wl.topk,
+            "window": wl.W, "main_kv": wl.main_fmt, "indexer_keys": wl.idx_fmt or None,
+            "layers_per_step": wl.n_layers, "l2": "flushed (256 MB write) before every step"}
+
+
+def main():
+    args = parse()
+    from compressed_kv_sparse_append_gb300 import workloads as wlmod
+    wl = wlmod.WORKLOADS[args.workload]
+    rank, world, dist = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world, dist)
+        return
+    import torch
+    from compressed_kv_sparse_append_gb300 import binding as ckv
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    step, dom_tag, dom_bytes, launches, layers, host, ws = make_step(wl, dev, ckv, wlmod)
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        step_ms, dom_ms = time_steps(step, args.steps, args.warmup, dev)
+    status = ckv.read_device_status(ws)
+    if status != 0:
+        raise RuntimeError("device status %d after the timed steps" % status)
+    total_ms = max_over_ranks(sum(step_ms), dist)
+    ms_per_step = total_ms / args.steps
+    value = world * layers * args.steps / (total_ms / 1000.0)
+    e2e_ms, bi, bo = time_e2e(step, host, max(3, args.steps // 2), max(3, args.warmup), dev)
+    e2e_ms = max_over_ranks(e2e_ms, dist)
+    peak, peak_kind = measured_peaks()
+    dom_avg_ms = statistics.mean(dom_ms)
+    achieved = dom_bytes / (dom_avg_ms / 1000.0) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4/fp8/bf16 in, f32 accumulate",
+            "data": "synthetic", "config": workload_config(wl),
+            "roofline": {"bound": "hbm", "kernel": dom_tag, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": profiled_traffic(dom_tag + ":" + wl.name),
+                         "algorithmic_bytes": dom_bytes, "avg_launch_us": dom_avg_ms * 1000.0},
+            "e2e": {"value": world * layers / (e2e_ms / 1000.0), "unit": UNIT,
+                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
+            "gpu_launches": launches * args.steps,
+            "clocks": clk.result,
+            "step_ms_median": statistics.median(step_ms)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = cpu_oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+"""ctypes binding of libckv (argument marshalling only).
+
+Every compute step runs in the library's CUDA kernels; this module turns torch
+tensors into device pointers, the current torch stream into a cudaStream_t and
+status codes into exceptions.  It raises at import when ``libckv.so`` has not
+been built: there is no fallback path.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libckv.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError("libckv.so is not built (run __graft_entry__.build() or "
+                      "python compressed_kv_sparse_append_gb300/build.py)")
+lib = ctypes.CDLL(_LIB_PATH)
+
+FMT = {"bf16": 0, "mixed": 1, "fp4": 2}
+OP_APPEND, OP_INDEX_TOPK, OP_SPARSE_ATTN, OP_HCA_ATTN, OP_CSA2 = range(5)
+CSA2_FULL, CSA2_REINDEX, CSA2_REUSE = 0, 1, 2
+MAX_LAYERS = 8
+
+_vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+
+class CPlane(ctypes.Structure):
+    _fields_ = [("fmt", _i32), ("dim", _i32), ("nope_block", _i32), ("batch", _i32),
+                ("cap", _i64), ("data", _vp), ("scale", _vp)]
+
+
+class CGroup(ctypes.Structure):
+    _fields_ = [("n_layers", _i32), ("role", _i32 * MAX_LAYERS), ("kv_src", _i32 * MAX_LAYERS),
+                ("idx_src", _i32 * MAX_LAYERS), ("kv", CPlane * MAX_LAYERS),
+                ("win", CPlane * MAX_LAYERS), ("idx_keys", CPlane), ("q", _vp * MAX_LAYERS),
+                ("q_idx", _vp * MAX_LAYERS), ("w", _vp * MAX_LAYERS), ("out", _vp * MAX_LAYERS),
+                ("lse", _vp * MAX_LAYERS), ("idx_out", _vp * MAX_LAYERS), ("pool_len", _i32)]
+
+
+_P = ctypes.POINTER(CPlane)
+lib.ckv_workspace_bytes.restype = _sz
+lib.ckv_workspace_bytes.argtypes = [_i32] * 7
+lib.ckv_kv_append_quant.restype = _i32
+lib.ckv_kv_append_quant.argtypes = [_P, _vp, _vp, _i32, _vp, _sz, _vp]
+lib.ckv_csa_index_topk.restype = _i32
+lib.ckv_csa_index_topk.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp,
+                                   _i32, _vp, _vp, _sz, _vp]
+lib.ckv_csa_sparse_attn.restype = _i32
+lib.ckv_csa_sparse_attn.argtypes = [_P, _P, _vp, _vp, _i32, _i32, _vp, _i32, _f32, _vp, _vp, _vp,
+                                    _sz, _vp]
+lib.ckv_hca_attn.restype = _i32
+lib.ckv_hca_attn.argtypes = [_P, _vp, _i32, _P, _vp, _i32, _vp, _i32, _f32, _vp, _vp, _vp, _sz, _vp]
+lib.ckv_csa2_group_decode.restype = _i32
+lib.ckv_csa2_group_decode.argtypes = [ctypes.POINTER(CGroup), _vp, _i32, _vp, _i32, _i32, _i32,
+                                      _i32, _f32, _P, _vp, _vp, _i32, _vp, _sz, _vp]
+lib.ckv_read_device_status.restype = _i32
+lib.ckv_read_device_status.argtypes = [_vp, _vp]
+lib.ckv_status_string.restype = ctypes.c_char_p
+lib.ckv_status_string.argtypes = [_i32]
+
+
+class CkvError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__("%s: %s (%d)" % (where, lib.ckv_status_string(code).decode(), code))
+        self.code = code
+
+
+def _check(code, where):
+    if code != 0:
+        raise CkvError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def entry_bytes(fmt: str, dim: int) -> int:
+    return {"bf16": dim * 2, "mixed": 576, "fp4": dim // 2}[fmt]
+
+
+def scale_shape(fmt: str, dim: int, nope_block: int = 448):
+    if fmt == "mixed":
+        return (448 // nope_block,), torch.float32
+    if fmt == "fp4":
+        return (dim // 16,), torch.uint8
+    return None, None
+
+
+class Plane:
+    """A cache plane of ``batch`` sequences x ``cap`` entry slots in device
+    memory (data [batch, cap, entry_bytes] uint8, scale per format)."""
+
+    def __init__(self, fmt, dim, batch, cap, device="cuda", nope_block=448, data=None, scale=None):
+        self.fmt, self.dim, self.batch, self.cap, self.nope_block = fmt, dim, batch, cap, nope_block
+        eb = entry_bytes(fmt, dim)
+        self.data = data if data is not None else torch.zeros((batch, cap, eb), dtype=torch.uint8,
+                                                              device=device)
+        shp, dt = scale_shape(fmt, dim, nope_block)
+        if scale is not None or shp is None:
+            self.scale = scale
+        else:
+            self.scale = torch.zeros((batch, cap) + shp, dtype=dt, device=device)
+
+    def c(self) -> CPlane:
+        return CPlane(FMT[self.fmt], self.dim, self.nope_block, self.batch, self.cap,
+                      self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr())
+
+
+def workspace_bytes(op, B, H=0, HI=0, n_comp_max=0, topk=0, pool_len=0) -> int:
+    return int(lib.ckv_workspace_bytes(op, B, H, HI, n_comp_max, topk, pool_len))
+
+
+def new_workspace(nbytes, device="cuda"):
+    """Zero-filled workspace (256-byte aligned, as torch's allocator returns)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def kv_append_quant(plane: Plane, src, slot, ws=None, stream=None):
+    n = 0 if src is None else src.shape[0]
+    ws = ws if ws is not None else new_workspace(workspace_bytes(OP_APPEND, 1), plane.data.device)
+    c = plane.c()
+    _check(lib.ckv_kv_append_quant(ctypes.byref(c), _ptr(src), _ptr(slot), n, _ptr(ws), ws.numel(),
+                                   _stream(stream)), "kv_append_quant")
+    return ws
+
+
+def csa_index_topk(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, pool_out=0,
+                   out_idx=None, out_pool=None, dbg_scores=None, ws=None, stream=None):
+    B, HI = q_idx.shape[0], q_idx.shape[1]
+    dev = q_idx.device
+    if out_idx is None:
+        out_idx = torch.empty((B, topk), dtype=torch.int32, device=dev)
+    if pool_out and out_pool is None:
+        out_pool = torch.empty((B, pool_out), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = new_workspace(workspace_bytes(OP_INDEX_TOPK, B, 0, HI, n_comp_max, topk, pool_out), dev)
+    pool_len = 0 if pool is None else pool.shape[1]
+    c = keys.c()
+    _check(lib.ckv_csa_index_topk(ctypes.byref(c), _ptr(n_comp), B, n_comp_max, _ptr(q_idx), _ptr(w),
+                                  HI, topk, _ptr(pool), pool_len, _ptr(out_idx), _ptr(out_pool),
+                                  pool_out if out_pool is not None else 0, _ptr(dbg_scores),
+                                  _ptr(ws), ws.numel(), _stream(stream)), "csa_index_topk")
+    return (out_idx, out_pool) if out_pool is not None else out_idx
+
+
+def csa_sparse_attn(kv: Plane, win: Plane, win_len, idx, q, sm_scale, out=None, lse=None, ws=None,
+                    stream=None):
+    B, H = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    ws = ws if ws is not None else new_workspace(workspace_bytes(OP_SPARSE_ATTN, B), q.device)
+    ck, cw = kv.c(), win.c()
+    _check(lib.ckv_csa_sparse_attn(ctypes.byref(ck), ctypes.byref(cw), _ptr(win_len), _ptr(idx), B,
+                                   idx.shape[1], _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "csa_sparse_attn")
+    return out
+
+
+def hca_attn(kv: Plane, n_comp, n_comp_max, win: Plane, win_len, q, sm_scale, out=None, lse=None,
+             ws=None, stream=None):
+    B, H = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    ws = ws if ws is not None else new_workspace(workspace_bytes(OP_HCA_ATTN, B), q.device)
+    ck, cw = kv.c(), win.c()
+    _check(lib.ckv_hca_attn(ctypes.byref(ck), _ptr(n_comp), n_comp_max, ctypes.byref(cw),
+                            _ptr(win_len), B, _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
+                            ws.numel(), _stream(stream)), "hca_attn")
+    return out
+
+
+def make_group(roles, kv_src, idx_src, kv, win, idx_keys, q, q_idx, w, out, lse=None,
+               idx_out=None, pool_len=2048) -> CGroup:
+    g = CGroup()
+    L = len(roles)
+    g.n_layers = L
+    for l in range(L):
+        g.role[l], g.kv_src[l], g.idx_src[l] = roles[l], kv_src[l], idx_src[l]
+        g.kv[l] = kv[l].c()
+        g.win[l] = win[l].c()
+        g.q[l] = q[l].data_ptr()
+        g.q_idx[l] = q_idx[l].data_ptr() if q_idx[l] is not None else None
+        g.w[l] = w[l].data_ptr() if w[l] is not None else None
+        g.out[l] = out[l].data_ptr()
+        g.lse[l] = lse[l].data_ptr() if lse is not None and lse[l] is not None else None
+        g.idx_out[l] = idx_out[l].data_ptr() if idx_out is not None and idx_out[l] is not None else None
+    g.idx_keys = idx_keys.c()
+    g.pool_len = pool_len
+    return g
+
+
+def csa2_group_decode(group: CGroup, n_comp, n_comp_max, win_len, B, H, HI, topk, sm_scale,
+                      append_dst: Plane = None, append_src=None, append_slot=None, ws=None,
+                      stream=None, device="cuda"):
+    if ws is None:
+        ws = new_workspace(workspace_bytes(OP_CSA2, B, H, HI, n_comp_max, topk, group.pool_len), device)
+    n_app = 0 if append_src is None else append_src.shape[0]
+    cad = append_dst.c() if append_dst is not None else None
+    _check(lib.ckv_csa2_group_decode(ctypes.byref(group), _ptr(n_comp), n_comp_max, _ptr(win_len), B,
+                                     H, HI, topk, sm_scale,
+                                     ctypes.byref(cad) if cad is not None else None,
+                                     _ptr(append_src), _ptr(append_slot), n_app, _ptr(ws), ws.numel(),
+                                     _stream(stream)), "csa2_group_decode")
+    return ws
+
+
+def read_device_status(ws, stream=None) -> int:
+    """Synchronises, returns and clears the sticky device status of ``ws``."""
+    return int(lib.ckv_read_device_status(_ptr(ws), _stream(stream)))

@@ -1,0 +1,419 @@
+// Host side of the libckv C ABI: argument validation, workspace layout,
+// kernel dispatch and the CSA2 group driver.  Every check runs before any
+// work is enqueued; nothing here allocates device memory.
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "indexer.cuh"
+#include "attention.cuh"
+
+namespace ckv {
+cudaError_t launch_append(const ckv_plane& p, const void* src, const int64_t* slot, int32_t n,
+                          DevStatus* st, cudaStream_t stream);
+}
+
+using namespace ckv;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a plane of the given dim for `B` sequences.
+ckv_status check_plane(const ckv_plane* p, int dim, int B) {
+  if (!p || !p->data || !aligned16(p->data)) return CKV_ERR_INVALID;
+  if (p->dim != dim || p->cap <= 0 || p->batch < B) return CKV_ERR_INVALID;
+  if (p->fmt == CKV_FMT_BF16) return CKV_OK;
+  if (p->fmt == CKV_FMT_FP4) {
+    if (!p->scale || (dim != 512 && dim != 128)) return CKV_ERR_INVALID;
+    return CKV_OK;
+  }
+  if (p->fmt == CKV_FMT_MIXED) {
+    if (dim != 512) return CKV_ERR_UNSUPPORTED;
+    if (!p->scale || !aligned16(p->scale)) return CKV_ERR_INVALID;
+    if (p->nope_block != 448 && p->nope_block != 64) return CKV_ERR_UNSUPPORTED;
+    return CKV_OK;
+  }
+  return CKV_ERR_INVALID;
+}
+
+struct IndexLayout {
+  int chunk, n_chunks, K_sel;
+  size_t counters_off, key_off, idx_off, bytes;  // relative to the index region
+};
+
+IndexLayout index_layout(int B, int n_comp_max, int K_sel, bool pool_mode, int pool_len) {
+  IndexLayout L;
+  L.K_sel = K_sel;
+  if (pool_mode) {
+    L.chunk = 256;
+    L.n_chunks = (pool_len + 255) / 256;
+    if (L.n_chunks < 1) L.n_chunks = 1;
+  } else {
+    const int64_t total = (int64_t)B * n_comp_max;
+    int64_t per = (total + 151) / 152;
+    int c = (int)align_up((size_t)per, 256);
+    c = c < 1024 ? 1024 : c;
+    c = c > kMaxChunk ? kMaxChunk : c;
+    L.chunk = c;
+    L.n_chunks = (n_comp_max + c - 1) / c;
+    if (L.n_chunks < 1) L.n_chunks = 1;
+  }
+  L.counters_off = 0;
+  L.key_off = align_up((size_t)B * 4, 256);
+  const size_t cand = (size_t)B * L.n_chunks * K_sel * 4;
+  L.idx_off = L.key_off + align_up(cand, 256);
+  L.bytes = L.idx_off + align_up(cand, 256);
+  return L;
+}
+
+ckv_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CKV_ERR_WORKSPACE;
+  if (ws_bytes < need) return CKV_ERR_WORKSPACE;
+  return CKV_OK;
+}
+
+// FP4 keys are scored on the block-scaled tensor cores; CKV_INDEXER=simt in
+// the environment selects the CUDA-core scorer (used to cross-check them).
+bool use_umma_indexer() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CKV_INDEXER");
+    v = (e && strcmp(e, "simt") == 0) ? 0 : 1;
+  }
+  return v == 1;
+}
+
+ckv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CKV_OK;
+  (void)cudaGetLastError();
+  return CKV_ERR_CUDA;
+}
+
+// Enqueues one index/top-k pass; `region` is the index scratch.
+ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_comp_max,
+                     const void* q_idx, const float* w, int HI, int topk, const int32_t* pool,
+                     int pool_len, int32_t* out_idx, int32_t* out_pool, int pool_out, float* dbg,
+                     DevStatus* st, uint8_t* region, cudaStream_t stream) {
+  const int K_sel = out_pool ? pool_out : topk;
+  IndexLayout L = index_layout(B, n_comp_max, K_sel, pool != nullptr, pool_len);
+  IndexArgs a;
+  a.kdata = static_cast<const uint8_t*>(keys->data);
+  a.kscale = static_cast<const uint8_t*>(keys->scale);
+  a.cap = keys->cap;
+  a.fmt = keys->fmt;
+  a.n_comp = n_comp;
+  a.B = B;
+  a.n_comp_max = n_comp_max;
+  a.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  a.w = w;
+  a.HI = HI;
+  a.pool = pool;
+  a.pool_len = pool_len;
+  a.topk = topk;
+  a.pool_out = out_pool ? pool_out : 0;
+  a.K_sel = K_sel;
+  a.chunk = L.chunk;
+  a.n_chunks = L.n_chunks;
+  a.counters = reinterpret_cast<uint32_t*>(region + L.counters_off);
+  a.cand_key = reinterpret_cast<uint32_t*>(region + L.key_off);
+  a.cand_idx = reinterpret_cast<int32_t*>(region + L.idx_off);
+  a.out_idx = out_idx;
+  a.out_pool = out_pool;
+  a.dbg = dbg;
+  a.st = st;
+  const int64_t rows = (int64_t)keys->batch * keys->cap;
+  if (use_umma_indexer() && index_umma_supported(a, rows))
+    return cuda_status(launch_index_umma(a, rows, stream));
+  return cuda_status(launch_index_simt(a, stream));
+}
+
+ckv_status check_index_args(const ckv_plane* keys, const int32_t* n_comp, int B, int n_comp_max,
+                            const void* q_idx, const float* w, int HI, int topk,
+                            const int32_t* pool, int pool_len, const int32_t* out_idx,
+                            const int32_t* out_pool, int pool_out) {
+  if (B <= 0 || !n_comp || !q_idx || !w || !out_idx) return CKV_ERR_INVALID;
+  if (!aligned16(q_idx)) return CKV_ERR_INVALID;
+  ckv_status s = check_plane(keys, 128, B);
+  if (s) return s;
+  if (keys->fmt != CKV_FMT_FP4 && keys->fmt != CKV_FMT_BF16) return CKV_ERR_UNSUPPORTED;
+  if (HI <= 0 || HI > kMaxHI) return CKV_ERR_UNSUPPORTED;
+  if (n_comp_max < 0 || n_comp_max > keys->cap) return CKV_ERR_INVALID;
+  if (topk <= 0 || topk > kMaxPool) return CKV_ERR_UNSUPPORTED;
+  if (pool) {
+    if (out_pool || pool_len <= 0 || pool_len > kMaxChunk) return CKV_ERR_INVALID;
+  }
+  if (out_pool && (pool_out < topk || pool_out > kMaxPool)) return CKV_ERR_INVALID;
+  return CKV_OK;
+}
+
+// Scratch of one index pass: K_sel candidates per chunk (pool_out for a
+// CSA2 Full layer, else topk); a pool-mode pass is one chunk of pool_len.
+size_t index_ws_bytes(int B, int n_comp_max, int K_sel, bool pool_mode, int pool_len) {
+  return index_layout(B, n_comp_max, K_sel, pool_mode, pool_len).bytes;
+}
+
+// Picks the number of CTA pairs per sequence (cluster of 2G CTAs).
+int choose_pairs(int B, int n_rows_max) {
+  const int tiles = (n_rows_max + 63) / 64;
+  int G = 4;
+  while (G > 1 && tiles < G * 2) G >>= 1;
+  (void)B;
+  return G;
+}
+
+ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
+                             int B, const void* q, int H, void* out) {
+  if (B <= 0 || !win_len || !q || !out || !aligned16(q) || !aligned16(out)) return CKV_ERR_INVALID;
+  if (H <= 0 || H > kMaxHeads) return CKV_ERR_UNSUPPORTED;
+  ckv_status s = check_plane(kv, 512, B);
+  if (s) return s;
+  s = check_plane(win, 512, B);
+  if (s) return s;
+  if (win->fmt != kv->fmt || (kv->fmt == CKV_FMT_MIXED && win->nope_block != kv->nope_block))
+    return CKV_ERR_INVALID;
+  return CKV_OK;
+}
+
+AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
+                   const void* q, int H, float sm_scale, void* out, float* lse, DevStatus* st) {
+  AttnArgs a;
+  a.kv_data = static_cast<const uint8_t*>(kv->data);
+  a.kv_scale = kv->scale;
+  a.kv_cap = kv->cap;
+  a.win_data = static_cast<const uint8_t*>(win->data);
+  a.win_scale = win->scale;
+  a.win_cap = win->cap;
+  a.fmt = kv->fmt;
+  a.nope_block = kv->nope_block;
+  a.idx = nullptr;
+  a.topk = 0;
+  a.n_comp = nullptr;
+  a.n_comp_max = 0;
+  a.win_len = win_len;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.H = H;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.G = 1;
+  a.st = st;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t n_comp_max,
+                           int32_t topk, int32_t pool_len) {
+  (void)H;
+  (void)HI;
+  if (B <= 0) return kStatusBytes;
+  switch (op) {
+    case CKV_OP_INDEX_TOPK:
+      // pool_len here: the pool_out of a CSA2 Full pass (0 for none); a
+      // pool-mode (Reindex) pass never needs more than a full pass.
+      return kStatusBytes +
+             index_ws_bytes(B, n_comp_max, pool_len > topk ? pool_len : topk, false, 0);
+    case CKV_OP_CSA2: {
+      size_t full = index_ws_bytes(B, n_comp_max, pool_len, false, 0);
+      size_t re = index_ws_bytes(B, n_comp_max, topk, true, pool_len);
+      size_t idx_region = align_up(full > re ? full : re, 256);
+      size_t pool = align_up((size_t)B * (pool_len > 0 ? pool_len : 1) * 4, 256);
+      size_t idxbuf = align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256);
+      return kStatusBytes + idx_region + pool + idxbuf;
+    }
+    default:
+      return kStatusBytes;
+  }
+}
+
+ckv_status ckv_kv_append_quant(const ckv_plane* dst, const void* src_bf16, const int64_t* slot,
+                               int32_t n, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0) return CKV_ERR_INVALID;
+  if (!dst) return CKV_ERR_INVALID;
+  ckv_status s = check_plane(dst, dst->dim, 1);
+  if (s) return s;
+  if (dst->dim != 512 && dst->dim != 128) return CKV_ERR_UNSUPPORTED;
+  if (n > 0 && (!src_bf16 || !slot || !aligned16(src_bf16))) return CKV_ERR_INVALID;
+  s = check_ws(ws, ws_bytes, kStatusBytes);
+  if (s) return s;
+  return cuda_status(launch_append(*dst, src_bf16, slot, n, static_cast<DevStatus*>(ws),
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_csa_index_topk(const ckv_plane* idx_keys, const int32_t* n_comp, int32_t B,
+                              int32_t n_comp_max, const void* q_idx_bf16, const float* w,
+                              int32_t HI, int32_t topk, const int32_t* pool, int32_t pool_len,
+                              int32_t* out_idx, int32_t* out_pool, int32_t pool_out,
+                              float* dbg_scores, void* ws, size_t ws_bytes, void* stream) {
+  ckv_status s = check_index_args(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool,
+                                  pool_len, out_idx, out_pool, pool_out);
+  if (s) return s;
+  const bool pool_mode = pool != nullptr;
+  const size_t need = kStatusBytes + index_ws_bytes(B, n_comp_max, out_pool ? pool_out : topk,
+                                                    pool_mode, pool_mode ? pool_len : 0);
+  s = check_ws(ws, ws_bytes, need);
+  if (s) return s;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return run_index(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool, pool_len,
+                   out_idx, out_pool, pool_out, dbg_scores, reinterpret_cast<DevStatus*>(w8),
+                   w8 + kStatusBytes, static_cast<cudaStream_t>(stream));
+}
+
+ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
+                               const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
+                               int32_t H, float sm_scale, void* out_bf16, float* lse, void* ws,
+                               size_t ws_bytes, void* stream) {
+  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16);
+  if (s) return s;
+  if (!idx || topk <= 0) return CKV_ERR_INVALID;
+  if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
+  s = check_ws(ws, ws_bytes, kStatusBytes);
+  if (s) return s;
+  AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
+                         static_cast<DevStatus*>(ws));
+  a.idx = idx;
+  a.topk = topk;
+  a.G = choose_pairs(B, topk + (int)win->cap);
+  return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_comp_max,
+                        const ckv_plane* win, const int32_t* win_len, int32_t B,
+                        const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
+                        float* lse, void* ws, size_t ws_bytes, void* stream) {
+  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16);
+  if (s) return s;
+  if (!n_comp || n_comp_max < 0 || n_comp_max > kv->cap) return CKV_ERR_INVALID;
+  s = check_ws(ws, ws_bytes, kStatusBytes);
+  if (s) return s;
+  AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
+                         static_cast<DevStatus*>(ws));
+  a.n_comp = n_comp;
+  a.n_comp_max = n_comp_max;
+  a.G = choose_pairs(B, n_comp_max + (int)win->cap);
+  return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
+                                 int32_t n_comp_max, const int32_t* win_len, int32_t B,
+                                 int32_t H, int32_t HI, int32_t topk, float sm_scale,
+                                 const ckv_plane* append_dst, const void* append_src_bf16,
+                                 const int64_t* append_slot, int32_t n_append, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  if (!g || g->n_layers < 1 || g->n_layers > CKV_CSA2_MAX_LAYERS) return CKV_ERR_INVALID;
+  const int L = g->n_layers;
+  if (g->role[0] != CKV_CSA2_FULL) return CKV_ERR_INVALID;
+  const int pool_len = g->pool_len;
+  if (pool_len < topk || pool_len > kMaxPool) return CKV_ERR_INVALID;
+  bool any_reindex = false;
+  for (int l = 0; l < L; ++l) {
+    const int r = g->role[l];
+    if (r < CKV_CSA2_FULL || r > CKV_CSA2_REUSE) return CKV_ERR_INVALID;
+    if (r == CKV_CSA2_REUSE && (g->idx_src[l] < 0 || g->idx_src[l] >= l)) return CKV_ERR_INVALID;
+    if (g->kv_src[l] < 0 || g->kv_src[l] >= L) return CKV_ERR_INVALID;
+    if (r != CKV_CSA2_REUSE) {
+      ckv_status s = check_index_args(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[l], g->w[l],
+                                      HI, topk, nullptr, 0, reinterpret_cast<int32_t*>(1),
+                                      r == CKV_CSA2_FULL ? reinterpret_cast<int32_t*>(1) : nullptr,
+                                      pool_len);
+      if (s) return s;
+    }
+    any_reindex |= r == CKV_CSA2_REINDEX;
+    const int k = g->kv_src[l];
+    ckv_status s = check_attn_common(&g->kv[k], &g->win[k], win_len, B, g->q[l], H, g->out[l]);
+    if (s) return s;
+    if (n_comp_max > g->kv[k].cap) return CKV_ERR_INVALID;
+  }
+  (void)any_reindex;
+  if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
+  if (n_append > 0) {
+    if (!append_dst || !append_src_bf16 || !append_slot || !aligned16(append_src_bf16))
+      return CKV_ERR_INVALID;
+    ckv_status s = check_plane(append_dst, append_dst->dim, 1);
+    if (s) return s;
+  }
+  const size_t need = ckv_workspace_bytes(CKV_OP_CSA2, B, H, HI, n_comp_max, topk, pool_len);
+  ckv_status s = check_ws(ws, ws_bytes, need);
+  if (s) return s;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  DevStatus* dst = reinterpret_cast<DevStatus*>(w8);
+  const size_t full = index_ws_bytes(B, n_comp_max, pool_len, false, 0);
+  const size_t re = index_ws_bytes(B, n_comp_max, topk, true, pool_len);
+  uint8_t* idx_region = w8 + kStatusBytes;
+  int32_t* pool_buf = reinterpret_cast<int32_t*>(idx_region + align_up(full > re ? full : re, 256));
+  int32_t* idxbuf = pool_buf + align_up((size_t)B * pool_len * 4, 256) / 4;
+
+  if (n_append > 0) {
+    s = cuda_status(launch_append(*append_dst, append_src_bf16, append_slot, n_append, dst, st));
+    if (s) return s;
+  }
+  const int32_t* layer_idx[CKV_CSA2_MAX_LAYERS];
+  for (int l = 0; l < L; ++l) {
+    int32_t* own = g->idx_out[l] ? g->idx_out[l] : idxbuf + (size_t)l * B * topk;
+    if (g->role[l] == CKV_CSA2_FULL) {
+      s = run_index(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[l], g->w[l], HI, topk, nullptr,
+                    0, own, pool_buf, pool_len, nullptr, dst, idx_region, st);
+      layer_idx[l] = own;
+    } else if (g->role[l] == CKV_CSA2_REINDEX) {
+      s = run_index(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[l], g->w[l], HI, topk, pool_buf,
+                    pool_len, own, nullptr, 0, nullptr, dst, idx_region, st);
+      layer_idx[l] = own;
+    } else {
+      layer_idx[l] = layer_idx[g->idx_src[l]];
+      if (g->idx_out[l])
+        s = cuda_status(cudaMemcpyAsync(g->idx_out[l], layer_idx[l], (size_t)B * topk * 4,
+                                        cudaMemcpyDeviceToDevice, st));
+    }
+    if (s) return s;
+  }
+  for (int l = 0; l < L; ++l) {
+    const int k = g->kv_src[l];
+    AttnArgs a = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l],
+                           g->lse[l], dst);
+    a.idx = layer_idx[l];
+    a.topk = topk;
+    a.G = choose_pairs(B, topk + (int)g->win[k].cap);
+    s = cuda_status(launch_attention(a, B, st));
+    if (s) return s;
+  }
+  return CKV_OK;
+}
+
+ckv_status ckv_read_device_status(void* ws, void* stream) {
+  if (!ws) return CKV_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  int32_t code = 0;
+  if (cudaMemcpy(&code, ws, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CKV_ERR_CUDA;
+  if (code != 0) {
+    if (cudaMemset(ws, 0, kStatusBytes) != cudaSuccess) return CKV_ERR_CUDA;
+  }
+  return code;
+}
+
+const char* ckv_status_string(ckv_status s) {
+  switch (s) {
+    case CKV_OK: return "CKV_OK";
+    case CKV_ERR_INVALID: return "CKV_ERR_INVALID";
+    case CKV_ERR_UNSUPPORTED: return "CKV_ERR_UNSUPPORTED";
+    case CKV_ERR_CUDA: return "CKV_ERR_CUDA";
+    case CKV_ERR_WORKSPACE: return "CKV_ERR_WORKSPACE";
+    case CKV_ERR_TIMEOUT: return "CKV_ERR_TIMEOUT";
+    case CKV_ERR_DEVICE_BOUNDS: return "CKV_ERR_DEVICE_BOUNDS";
+    default: return "CKV_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,35 @@
+// Shared declarations of the attention kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace ckv {
+
+constexpr int kMaxTopk = 2048;    // selected rows held per sequence
+constexpr int kMaxHeads = 128;    // query heads (one 128-row MMA tile)
+
+struct AttnArgs {
+  const uint8_t* kv_data;
+  const void* kv_scale;
+  int64_t kv_cap;
+  const uint8_t* win_data;
+  const void* win_scale;
+  int64_t win_cap;
+  int fmt, nope_block;
+  const int32_t* idx;     // CSA: [B][topk] selected entries; null for HCA
+  int topk;
+  const int32_t* n_comp;  // HCA: [B]
+  int n_comp_max;
+  const int32_t* win_len; // [B]
+  const __nv_bfloat16* q; // [B][H][512]
+  int H;
+  float scale_log2;       // sm_scale * log2(e)
+  __nv_bfloat16* out;     // [B][H][512]
+  float* lse;             // [B][H] or null
+  int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
+  DevStatus* st;
+};
+
+cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream);
+
+}  // namespace ckv

@@ -1,0 +1,173 @@
+// csa_index_topk: Lightning-indexer scores and exact top-k per sequence.
+//
+// "DeepSeek-V4 KV Cache 深度分析", §四: the 128-d indexer query of the current
+// token is scored against every compressed block's indexer key and the top-k
+// blocks are kept; the indexer's QK activations are held and computed in FP4.
+// Score (workload definition): s_j = sum_h w_h * ReLU(q_h . k_j) on the
+// dequantised values; for FP4 keys the query is block-quantised first.
+//
+// Grid (chunk, sequence).  Each CTA scores one chunk of entries, keeps the
+// chunk's top-K candidates (K = max(topk, pool_out)) with the radix select of
+// select.cuh and writes them to the workspace; the last CTA of a sequence to
+// finish (atomic ticket, no spinning) merges the candidate lists into the
+// exact top-K, and for a CSA2 Full layer also the top-k of that pool.
+// Candidate lists are stored in ascending entry order, so the merge's
+// ordered compaction resolves ties towards the lower index.
+//
+// Scoring engines:
+//   * score_simt: CUDA-core FMAs on dequantised values (BF16 keys, and the
+//     fallback for FP4 when a block-scaled tensor-core scorer is not used);
+//   * the block-scaled tcgen05 scorer lives in indexer_umma.cu.
+
+#include "topk_merge.cuh"
+
+namespace ckv {
+
+constexpr int kIdxThreads = 512;
+
+struct IndexSmem {
+  float q[kMaxHI * kIdxDim];       // dequantised indexer query
+  float w[kMaxHI];
+  uint32_t keys[kMaxChunk];        // scores of this chunk as order keys
+  MergeSmem<kIdxThreads> m;
+};
+
+// Dequantised indexer query into shared memory: FP4 keys -> the query is
+// quantised with the E2M1 + E4M3/16 block quantiser (the same arithmetic as
+// the append path) and its exact values stored; BF16 keys -> the BF16 values.
+__device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
+  const int t = threadIdx.x;
+  if (t < a.HI * 8) {
+    const int h = t >> 3, blk = t & 7;
+    const __nv_bfloat16* src = a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    const uint4 x0 = s4[0], x1 = s4[1];
+    const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(wd[i] << 16);
+      v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+    }
+    if (a.fmt == CKV_FMT_FP4) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const float s = e4m3_value(e4m3_code(__fdiv_rn(amax, 6.0f)));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = s > 0.f ? e2m1_value(e2m1_code(__fdiv_rn(v[i], s))) * s : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[h * kIdxDim + blk * 16 + i] = v[i];
+  }
+  if (t < a.HI) w[t] = a.w[(int64_t)b * a.HI + t];
+}
+
+__device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t entry,
+                                            const float* q, const float* w) {
+  float acc[kMaxHI];
+#pragma unroll
+  for (int h = 0; h < kMaxHI; ++h) acc[h] = 0.f;
+  const int64_t row = (int64_t)b * a.cap + entry;
+#pragma unroll 1
+  for (int blk = 0; blk < 8; ++blk) {
+    float kv[16];
+    if (a.fmt == CKV_FMT_FP4) {
+      const uint2 d = *reinterpret_cast<const uint2*>(a.kdata + row * 64 + blk * 8);
+      const float s = e4m3_value(a.kscale[row * 8 + blk]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        kv[i] = e2m1_value((d.x >> (4 * i)) & 0xF) * s;
+        kv[8 + i] = e2m1_value((d.y >> (4 * i)) & 0xF) * s;
+      }
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(a.kdata + row * 256 + blk * 32);
+      const uint4 x0 = p[0], x1 = p[1];
+      const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        kv[2 * i] = __uint_as_float(wd[i] << 16);
+        kv[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxHI; ++h) {
+      if (h < a.HI) {
+        const float4* qq = reinterpret_cast<const float4*>(q + h * kIdxDim + blk * 16);
+        float r = acc[h];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 v = qq[j];
+          r = fmaf(v.x, kv[4 * j], r);
+          r = fmaf(v.y, kv[4 * j + 1], r);
+          r = fmaf(v.z, kv[4 * j + 2], r);
+          r = fmaf(v.w, kv[4 * j + 3], r);
+        }
+        acc[h] = r;
+      }
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int h = 0; h < kMaxHI; ++h)
+    if (h < a.HI) s = fmaf(w[h], fmaxf(acc[h], 0.f), s);
+  return s;
+}
+
+__global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  IndexSmem& sm = *reinterpret_cast<IndexSmem*>(smem_raw);
+  const int b = blockIdx.y, chunk = blockIdx.x;
+  const int ncomp = min(a.n_comp[b], a.n_comp_max);
+  load_query(a, b, sm.q, sm.w);
+  if (threadIdx.x == 0) sm.m.n_real = 0;
+  __syncthreads();
+
+  int n_elem;
+  int64_t first = 0;
+  const int32_t* pool = nullptr;
+  if (a.pool) {
+    // Reindex: chunk `chunk` of the candidate list; entries come from it
+    first = (int64_t)chunk * a.chunk;
+    pool = a.pool + (int64_t)b * a.pool_len + first;
+    n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)a.pool_len - first));
+  } else {
+    first = (int64_t)chunk * a.chunk;
+    n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)ncomp - first));
+  }
+  uint32_t mine = 0;
+  for (int i = threadIdx.x; i < n_elem; i += kIdxThreads) {
+    int64_t e = pool ? (int64_t)pool[i] : first + i;
+    uint32_t key = 0u;
+    if (e >= 0 && e < ncomp) {
+      const float s = score_simt(a, b, e, sm.q, sm.w);
+      key = score_key(s);
+      if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + e] = s;
+      ++mine;
+    } else if (e >= ncomp && pool) {
+      report(a.st, CKV_ERR_DEVICE_BOUNDS, (int)e);
+    }
+    sm.keys[i] = key;
+  }
+  atomicAdd(&sm.m.n_real, mine);
+  __syncthreads();
+  chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.m);
+}
+
+size_t index_smem_bytes() { return sizeof(IndexSmem); }
+
+cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(index_topk_simt_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(IndexSmem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(a.n_chunks, a.B);
+  index_topk_simt_kernel<<<grid, kIdxThreads, sizeof(IndexSmem), stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ckv

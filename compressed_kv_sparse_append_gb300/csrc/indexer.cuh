@@ -1,0 +1,41 @@
+// Shared declarations of the indexer / top-k kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace ckv {
+
+constexpr int kIdxDim = 128;      // indexer head dim ("DeepSeek-V4 KV Cache 深度分析", §一)
+constexpr int kMaxHI = 64;        // indexer heads supported
+constexpr int kMaxChunk = 8192;   // entries scored per CTA
+constexpr int kMaxPool = 2048;    // largest pool / top-k kept by the merge
+
+struct IndexArgs {
+  const uint8_t* kdata;           // indexer-key plane data
+  const uint8_t* kscale;          // FP4: E4M3 scale bytes
+  int64_t cap;
+  int fmt;                        // CKV_FMT_FP4 or CKV_FMT_BF16
+  const int32_t* n_comp;
+  int B, n_comp_max;
+  const __nv_bfloat16* q_idx;
+  const float* w;
+  int HI;
+  const int32_t* pool;            // Reindex: candidate entries, or null
+  int pool_len;
+  int topk, pool_out, K_sel;
+  int chunk, n_chunks;
+  uint32_t* cand_key;             // workspace [B][n_chunks][K_sel]
+  int32_t* cand_idx;
+  uint32_t* counters;             // workspace [B], zero between calls
+  int32_t* out_idx;
+  int32_t* out_pool;
+  float* dbg;
+  DevStatus* st;
+};
+
+size_t index_smem_bytes();
+cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream);
+bool index_umma_supported(const IndexArgs& a, int64_t batch_rows);
+cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream_t stream);
+
+}  // namespace ckv

@@ -1,0 +1,335 @@
+// Block-scaled tcgen05 scorer of csa_index_topk for FP4 indexer keys.
+//
+// "DeepSeek-V4 KV Cache 深度分析", §四 (and the paper's Section 5.2.1 quoted
+// there): the indexer's QK activations are cached, loaded and computed in FP4.
+// Keys and query are E2M1 with one E4M3 scale per 16 channels ("V4.1-Flash
+// 공개", 핵심 내용: the same block format as the FP4 main KV), which is exactly
+// the operand format of tcgen05.mma kind::mxf4nvf4 with scale_vec::4X: the
+// tensor core applies both scales per 16-element block and accumulates in
+// f32, so the FP4 bytes go from HBM to the tensor core untouched.
+//
+// Per CTA: one chunk of C keys of one sequence.
+//   warp 0   TMA producer: 128-key tiles of packed codes (SWIZZLE_64B) and
+//            their scale bytes into a kStages-deep shared-memory ring;
+//   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, two
+//            buffers) = keys (A, M = 128) x query (B, N = 64), K = 128 in two
+//            block-scaled steps;
+//   warps 2-5 epilogue: move each tile's key scales into TMEM, then read D
+//            back (one key per thread) and form s = sum_h w_h ReLU(d_h) in f32.
+// The scores stay in shared memory; the chunk's top-K and the cross-chunk
+// merge are those of topk_merge.cuh.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "topk_merge.cuh"
+
+namespace ckv {
+
+namespace {
+
+constexpr int kUThreads = 192;
+constexpr int kUStages = 6;
+constexpr int kUTile = 128;
+constexpr uint32_t kDataBytes = kUTile * 64;                 // 8 KB
+constexpr uint32_t kScaleBytes = kUTile * 8;                 // 1 KB
+constexpr uint32_t kOffData = 0;
+constexpr uint32_t kOffScale = kOffData + kUStages * kDataBytes;
+constexpr uint32_t kOffQ = kOffScale + kUStages * kScaleBytes;     // 64 rows x 64 B
+constexpr uint32_t kOffQs = kOffQ + 64 * 64;                       // 64 x 8 scale bytes
+constexpr uint32_t kOffW = kOffQs + 64 * 8;                        // 64 f32
+constexpr uint32_t kOffKeys = kOffW + 64 * 4;                      // u32 [kMaxChunk]
+constexpr uint32_t kOffMerge = kOffKeys + kMaxChunk * 4;
+constexpr uint32_t kOffBar = (kOffMerge + sizeof(MergeSmem<kUThreads>) + 7) & ~7u;
+constexpr int kNumBarU = 3 * kUStages + 4;
+constexpr uint32_t kOffSlotU = kOffBar + kNumBarU * 8;
+constexpr uint32_t kSmemU = kOffSlotU + 16 + 1024;
+static_assert(kOffQ % 1024 == 0, "operand tiles 1024-aligned");
+static_assert(kSmemU <= 232448, "fits in shared memory");
+
+constexpr uint32_t kTmemU = 256;
+constexpr uint32_t kColD = 0;          // two 64-column accumulators
+constexpr uint32_t kColSFA = 128;      // 8 columns per stage
+constexpr uint32_t kColSFB = 192;      // 8 columns
+constexpr uint32_t kIdescNvf4 = idesc_nvf4(128, 64);
+
+enum { BU_FULL = 0, BU_EMPTY = kUStages, BU_SFA = 2 * kUStages, BU_DFULL = 3 * kUStages,
+       BU_DEMPTY = 3 * kUStages + 2 };
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 16-byte chunk c (0..3) of row r of a 64-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+
+}  // namespace
+
+struct UmmaIndexArgs {
+  IndexArgs a;
+  int64_t row_limit;  // B * cap (rows of the key plane)
+};
+
+__global__ void __launch_bounds__(kUThreads, 1)
+    index_topk_umma_kernel(const __grid_constant__ CUtensorMap map_data,
+                           const __grid_constant__ CUtensorMap map_scale, UmmaIndexArgs ua) {
+  const IndexArgs& a = ua.a;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* g = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(g + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(g + kOffSlotU);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(g + kOffKeys);
+  float* wsm = reinterpret_cast<float*>(g + kOffW);
+  MergeSmem<kUThreads>& msm = *reinterpret_cast<MergeSmem<kUThreads>*>(g + kOffMerge);
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.y, chunk = blockIdx.x;
+  const int ncomp = min(a.n_comp[b], a.n_comp_max);
+  const int64_t c0 = (int64_t)chunk * a.chunk;
+  const int n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)ncomp - c0));
+  const int T = (n_elem + kUTile - 1) / kUTile;
+  const int64_t row0 = (int64_t)b * a.cap + c0;
+
+  // ---- setup: FP4 query (B operand) + its scales, head weights, barriers
+  if (tid < 64 * 8) {
+    for (int j = tid; j < 64 * 8; j += kUThreads) {
+      const int h = j >> 3, blk = j & 7;
+      uint32_t lo = 0, hi = 0;
+      uint8_t sc = 0;
+      if (h < a.HI) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16);
+        const uint4 x0 = s4[0], x1 = s4[1];
+        const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float v[16];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = __uint_as_float(wd[i] << 16);
+          v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        sc = e4m3_code(__fdiv_rn(amax, 6.0f));
+        const float s = e4m3_value(sc);
+        if (s > 0.f) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) lo |= e2m1_code(__fdiv_rn(v[i], s)) << (4 * i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hi |= e2m1_code(__fdiv_rn(v[8 + i], s)) << (4 * i);
+        } else {
+          sc = 0;
+        }
+      }
+      // row h, bytes [8 blk, 8 blk + 8) of the SW64 tile
+      *reinterpret_cast<uint2*>(g + kOffQ + sw64(h, blk >> 1) + (blk & 1) * 8) = make_uint2(lo, hi);
+      g[kOffQs + h * 8 + blk] = sc;
+    }
+  }
+  if (tid < 64) wsm[tid] = tid < a.HI ? a.w[(int64_t)b * a.HI + tid] : 0.f;
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(&bars[BU_FULL + s], 1);
+      mbar_init(&bars[BU_EMPTY + s], 1);
+      mbar_init(&bars[BU_SFA + s], 128);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&bars[BU_DFULL + d], 1);
+      mbar_init(&bars[BU_DEMPTY + d], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, kTmemU);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp >= 2) {
+    // query scales -> TMEM (B operand scales): lane 32q + r, column j holds
+    // the four block scales (one 32-bit word per K step) of query row 32j + r.
+    const int qd = warp & 3;
+    const int m = qd * 32 + lane;
+    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = 32 * j + (m & 31);
+        v[j] = row < 64 ? *reinterpret_cast<const uint32_t*>(g + kOffQs + row * 8 + ks * 4) : 0u;
+      }
+      tmem_st4(tmem + lb + kColSFB + 4 * ks, v[0], v[1], v[2], v[3]);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA ----
+    if (lane == 0) {
+      for (int t = 0; t < T; ++t) {
+        const int s = t % kUStages;
+        if (t >= kUStages &&
+            !mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11))
+          break;
+        mbar_expect_tx(&bars[BU_FULL + s], kDataBytes + kScaleBytes);
+        const int64_t row = row0 + (int64_t)t * kUTile;
+        tma_load_2d(base + kOffData + s * kDataBytes, &map_data, 0, (int)row, &bars[BU_FULL + s]);
+        tma_load_2d(base + kOffScale + s * kScaleBytes, &map_scale, 0, (int)(row >> 1),
+                    &bars[BU_FULL + s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA ----
+    if (lane == 0) {
+      for (int t = 0; t < T; ++t) {
+        const int s = t % kUStages, d = t & 1;
+        if (!mbar_wait(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
+        if (t >= 2 && !mbar_wait(&bars[BU_DEMPTY + d], ((t >> 1) + 1) & 1, a.st, abort_p, 13)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
+          const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
+          umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
+                    tmem + kColSFB + 4 * ks, ks > 0);
+        }
+        umma_commit(&bars[BU_DFULL + d]);
+        umma_commit(&bars[BU_EMPTY + s]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- epilogue ----
+    const int qd = warp & 3;
+    const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
+    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+    auto move_scales = [&](int t) -> bool {
+      const int s = t % kUStages;
+      if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) return false;
+      const uint2 sc = *reinterpret_cast<const uint2*>(g + kOffScale + s * kScaleBytes + m * 8);
+      tmem_st4(tmem + lb + kColSFA + 8 * s, sc.x, sc.x, sc.x, sc.x);
+      tmem_st4(tmem + lb + kColSFA + 8 * s + 4, sc.y, sc.y, sc.y, sc.y);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[BU_SFA + s]);
+      return true;
+    };
+    bool ok = T > 0 ? move_scales(0) : true;
+    for (int t = 0; t < T && ok; ++t) {
+      if (t + 1 < T && !move_scales(t + 1)) break;
+      const int d = t & 1;
+      if (!mbar_wait(&bars[BU_DFULL + d], (t >> 1) & 1, a.st, abort_p, 15)) break;
+      tc_fence_after();
+      uint32_t r[64];
+      tmem_ld32(tmem + lb + kColD + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      tmem_ld32(tmem + lb + kColD + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars[BU_DEMPTY + d]);
+      float s = 0.f;
+#pragma unroll
+      for (int h4 = 0; h4 < 16; ++h4) {
+        const float4 wv = reinterpret_cast<const float4*>(wsm)[h4];
+        s = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), s);
+        s = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s);
+        s = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s);
+        s = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s);
+      }
+      const int i = t * kUTile + m;
+      if (i < n_elem) {
+        keys[i] = score_key(s);
+        if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = s;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemU);
+  }
+  if (tid == 0) msm.n_real = (uint32_t)n_elem;
+  __syncthreads();
+  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, msm);
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
+  // FP4 keys, no pool, 64 heads max, scale rows pair up (even cap), the
+  // 2-D maps' row counts fit in int32.
+  return a.fmt == CKV_FMT_FP4 && a.pool == nullptr && a.HI <= 64 && (a.cap % 2) == 0 &&
+         batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream_t stream) {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(index_topk_umma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemU);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  auto enc = encode_fn();
+  CUtensorMap md, ms;
+  {
+    cuuint64_t dims[2] = {64, (cuuint64_t)batch_rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {64, (cuuint32_t)kUTile};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.kdata), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {16, (cuuint64_t)(batch_rows / 2)};
+    cuuint64_t strides[1] = {16};
+    cuuint32_t box[2] = {16, (cuuint32_t)(kUTile / 2)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.kscale), dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  UmmaIndexArgs ua;
+  ua.a = a;
+  ua.row_limit = batch_rows;
+  dim3 grid(a.n_chunks, a.B);
+  index_topk_umma_kernel<<<grid, kUThreads, kSmemU, stream>>>(md, ms, ua);
+  return cudaGetLastError();
+}
+
+}  // namespace ckv

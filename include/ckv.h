@@ -1,0 +1,223 @@
+/*
+ * ckv.h -- C ABI of libckv: decode-time attention over the compressed KV
+ * caches of DeepSeek-V4 (CSA / HCA) and V4.1-Flash (CSA2, FP4 main KV), for
+ * GB300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *   [KVC]  "DeepSeek-V4 KV Cache 深度分析": §二 entry layout (512-d latent whose
+ *          last 64 dims carry RoPE; nope in FP8, rope in BF16), §三 CSA/HCA
+ *          (ratio 4 with top-k, ratio 128 dense, 128-token window), §四 indexer
+ *          (128-d FP4 keys, top-k), §六 precision, §十一 flow chart.
+ *   [V41]  "DeepSeek, KV 캐시를 토큰당 890바이트로 줄인 V4.1-Flash 공개",
+ *          핵심 내용: CSA2 Full / Reindex / Reuse, FP4 E2M1 with one E4M3
+ *          scale per 16 channels.
+ *   [890]  "KV cache 890 bajtów na token", "Trzy mechanizmy": shared main KV
+ *          and indexer key across layers, indexer pool of the Full layer.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless marked [host].  The caller owns
+ *     every buffer; the library allocates no device memory and keeps no
+ *     state between calls (apart from the per-device launch attributes it
+ *     sets once).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and return after enqueueing.
+ *   - Arguments are validated on the host first.  A host-detected error
+ *     returns CKV_ERR_INVALID / CKV_ERR_UNSUPPORTED / CKV_ERR_WORKSPACE and
+ *     enqueues nothing.  A failed launch returns CKV_ERR_CUDA.
+ *   - `ws` is a caller-owned device workspace of at least
+ *     ckv_workspace_bytes(op, ...) bytes, 256-byte aligned, ZERO-FILLED
+ *     before its first use; every call leaves it reusable (its counters
+ *     return to zero).  Its first 256 bytes hold a sticky device status
+ *     word: kernels that detect an out-of-range index or a bounded wait that
+ *     expired record CKV_ERR_DEVICE_BOUNDS / CKV_ERR_TIMEOUT there, skip the
+ *     offending access and never trap.  ckv_read_device_status() returns
+ *     and clears it.  Calls that overlap on the GPU must use distinct
+ *     workspaces.
+ *   - Dimensions are fixed by the pages: main-KV entries are D = 512 with
+ *     R = 64 RoPE dims, indexer keys are 128-d, heads H <= 128.
+ */
+#ifndef CKV_H
+#define CKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ckv_status;
+#define CKV_OK                 0
+#define CKV_ERR_INVALID       -1  /* bad argument (null, misaligned, out of range) */
+#define CKV_ERR_UNSUPPORTED   -2  /* valid but not implemented shape / format      */
+#define CKV_ERR_CUDA          -3  /* CUDA runtime or launch failure                */
+#define CKV_ERR_WORKSPACE     -4  /* workspace missing or smaller than required    */
+#define CKV_ERR_TIMEOUT       -5  /* device: a bounded wait expired                */
+#define CKV_ERR_DEVICE_BOUNDS -6  /* device: an index or slot was out of range     */
+
+/* Storage formats of a cache plane.
+ *  CKV_FMT_BF16  : entry = dim x bf16 (1024 B for D = 512, 256 B for 128).
+ *  CKV_FMT_MIXED : D = 512 only. Entry = 448 x E4M3 nope codes followed by
+ *                  64 x bf16 rope values = 576 B ([KVC] §二, §六).  One f32
+ *                  scale per block of `nope_block` nope channels in `scale`:
+ *                  value = decode(code) * scale.
+ *  CKV_FMT_FP4   : entry = dim/2 bytes of packed E2M1 codes, channel 2t in the
+ *                  low nibble of byte t, channel 2t+1 in the high nibble; one
+ *                  E4M3 scale byte per 16 channels in `scale` ([V41]).  */
+#define CKV_FMT_BF16  0
+#define CKV_FMT_MIXED 1
+#define CKV_FMT_FP4   2
+
+/* One cache plane (main KV, window ring, or indexer keys) of `batch`
+ * sequences with `cap` entry slots each.  Entry (b, pos) lives at
+ * data + (b * cap + pos) * entry_bytes; its scales at
+ * scale + (b * cap + pos) * n_scales * scale_size.
+ * data and scale are 16-byte aligned.  The plane struct itself is [host]. */
+typedef struct ckv_plane {
+  int32_t fmt;        /* CKV_FMT_*                                           */
+  int32_t dim;        /* 512 (main KV, window) or 128 (indexer keys)         */
+  int32_t nope_block; /* CKV_FMT_MIXED: 448 (one scale per entry) or 64      */
+  int32_t batch;      /* sequences                                           */
+  int64_t cap;        /* entry slots per sequence                            */
+  void   *data;       /* [batch][cap][entry_bytes]                           */
+  void   *scale;      /* MIXED: f32 [batch][cap][448/nope_block];
+                         FP4:   u8  [batch][cap][dim/16] (E4M3 codes);
+                         BF16:  NULL                                         */
+} ckv_plane;
+
+/* Workspace sizing.  `op` is one of CKV_OP_*; unused arguments may be 0. */
+#define CKV_OP_APPEND      0
+#define CKV_OP_INDEX_TOPK  1
+#define CKV_OP_SPARSE_ATTN 2
+#define CKV_OP_HCA_ATTN    3
+#define CKV_OP_CSA2        4
+size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI,
+                           int32_t n_comp_max, int32_t topk, int32_t pool_len);
+
+/* Append-side quantise and store ([KVC] §二 code evidence: the latent's first
+ * 448 dims quantised to FP8, the 64 RoPE dims kept BF16; [V41] / [890]: FP4
+ * E2M1 with one E4M3 scale per 16 channels, used for the V4.1 main KV and
+ * here also for the 128-d indexer keys of [KVC] §四).
+ *   dst      [host] destination plane (any format; dim 512 or 128).
+ *   src_bf16 [n][dst->dim] bf16 rows, already normalised and rotated.
+ *   slot     [n] int64: destination slot b * cap + pos.  A negative slot
+ *            skips the row; a slot >= batch * cap skips it and records
+ *            CKV_ERR_DEVICE_BOUNDS.
+ * Quantisation (bit-exact contract):
+ *   MIXED: s = fl32(amax_block / 448) (f32), code_i = E4M3_rn_satfinite(
+ *          fl32(x_i / s)); rope dims copied as bf16.
+ *   FP4:   s = E4M3_rn_satfinite(fl32(amax16 / 6)), code_i =
+ *          E2M1_rn_satfinite(fl32(x_i / decode(s))).
+ *   Codes carry the sign of x (tiny negatives give the negative-zero code);
+ *   a block whose scale is zero stores all-zero codes. */
+ckv_status ckv_kv_append_quant(const ckv_plane *dst, const void *src_bf16,
+                               const int64_t *slot, int32_t n,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/* Lightning-indexer score + exact top-k ([KVC] §四; score definition
+ * s_j = sum_h w_h * ReLU(q_h . k_j) on the dequantised values; for FP4 keys
+ * the query is first quantised with the same E2M1 + E4M3/16 block
+ * quantiser, "computed entirely in FP4").
+ *   idx_keys   [host] indexer-key plane, dim 128, CKV_FMT_FP4 or _BF16.
+ *   n_comp     [B] int32: valid entries of each sequence (<= n_comp_max).
+ *   n_comp_max [host] upper bound of n_comp (sizes the grid).
+ *   q_idx_bf16 [B][HI][128] bf16 indexer queries; w [B][HI] f32 weights.
+ *   topk       entries to select (1..2048).
+ *   pool       NULL: score every entry [0, n_comp[b]).  Otherwise
+ *              [B][pool_len] int32 candidate entries (-1 = unused); only
+ *              those are scored (the CSA2 Reindex layer, [890]).
+ *   out_idx    [B][topk] int32: the top-k entries, ascending, -1 padded.
+ *              Order: score descending, then index ascending (lower index
+ *              wins a tie); -0.0 counts as +0.0.
+ *   out_pool   NULL or [B][pool_out] int32: the top-pool_out set under the
+ *              same order, ascending, -1 padded (CSA2 Full layer's pool);
+ *              pool_out >= topk; requires pool == NULL.
+ *   dbg_scores NULL or [B][n_comp_max] f32: every computed score at its
+ *              entry index (diagnostics; costs bandwidth).
+ * Scores are f32 with an accumulation order the tensor cores fix; the
+ * selection is exact on those f32 scores. */
+ckv_status ckv_csa_index_topk(const ckv_plane *idx_keys, const int32_t *n_comp,
+                              int32_t B, int32_t n_comp_max,
+                              const void *q_idx_bf16, const float *w, int32_t HI,
+                              int32_t topk, const int32_t *pool, int32_t pool_len,
+                              int32_t *out_idx, int32_t *out_pool, int32_t pool_out,
+                              float *dbg_scores, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* CSA sparse attention ([KVC] §十一 flow chart: attention over the selected
+ * entries followed by the sliding window; §五: each entry is both key and
+ * value).  One softmax over the union of the selected rows and the valid
+ * window rows:  o_h = sum_j softmax_j(sm_scale * q_h . e_j) e_j,
+ * lse_h = log sum_j exp(sm_scale * q_h . e_j).
+ *   kv, win  [host] main-KV and window planes of the same format (dim 512).
+ *   win_len  [B] int32: valid window slots [0, win_len[b]) (<= win->cap).
+ *   idx      [B][topk] int32 entries of kv (-1 = none; >= kv->cap is skipped
+ *            and records CKV_ERR_DEVICE_BOUNDS).
+ *   q_bf16   [B][H][512] bf16, H <= 128.
+ *   out_bf16 [B][H][512] bf16; lse NULL or [B][H] f32 (natural log; -inf when
+ *            there is no row to attend, with o = 0). */
+ckv_status ckv_csa_sparse_attn(const ckv_plane *kv, const ckv_plane *win,
+                               const int32_t *win_len, const int32_t *idx,
+                               int32_t B, int32_t topk, const void *q_bf16,
+                               int32_t H, float sm_scale, void *out_bf16,
+                               float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* HCA dense attention ([KVC] §三: ratio-128 entries, no sparse selection,
+ * dense attention over all entries plus the 128-token window).  Same
+ * formula as ckv_csa_sparse_attn over entries [0, n_comp[b]) and the window.
+ *   n_comp [B] int32 (<= n_comp_max <= kv->cap). */
+ckv_status ckv_hca_attn(const ckv_plane *kv, const int32_t *n_comp,
+                        int32_t n_comp_max, const ckv_plane *win,
+                        const int32_t *win_len, int32_t B, const void *q_bf16,
+                        int32_t H, float sm_scale, void *out_bf16, float *lse,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/* CSA2 group decode ([V41] 핵심 내용; [890] "Trzy mechanizmy").  Layer roles:
+ *   FULL    scores every entry of `idx_keys` with its own q_idx / w, keeps
+ *           the top-pool_len pool and the top-k;
+ *   REINDEX rescoring of the most recent FULL layer's pool with its own
+ *           q_idx / w against the same indexer keys; takes the pool's top-k;
+ *   REUSE   takes the indices of layer idx_src[l] unchanged.
+ * Every layer then attends (as ckv_csa_sparse_attn) to the main KV and
+ * window of layer kv_src[l].  Before the layers run, the call appends
+ * n_append rows to `append_dst` (as ckv_kv_append_quant). */
+#define CKV_CSA2_FULL    0
+#define CKV_CSA2_REINDEX 1
+#define CKV_CSA2_REUSE   2
+#define CKV_CSA2_MAX_LAYERS 8
+typedef struct ckv_csa2_group {
+  int32_t n_layers;                       /* 1..8 (6 in V4.1-Flash)            */
+  int32_t role[CKV_CSA2_MAX_LAYERS];      /* CKV_CSA2_*; layer 0 must be FULL  */
+  int32_t kv_src[CKV_CSA2_MAX_LAYERS];    /* layer whose main KV / window to use */
+  int32_t idx_src[CKV_CSA2_MAX_LAYERS];   /* REUSE: earlier layer to copy from */
+  ckv_plane kv[CKV_CSA2_MAX_LAYERS];      /* main KV per layer (dim 512)       */
+  ckv_plane win[CKV_CSA2_MAX_LAYERS];     /* window per layer                  */
+  ckv_plane idx_keys;                     /* FULL layer's indexer keys (128-d) */
+  const void  *q[CKV_CSA2_MAX_LAYERS];    /* [B][H][512] bf16                   */
+  const void  *q_idx[CKV_CSA2_MAX_LAYERS];/* [B][HI][128] bf16 (FULL/REINDEX)   */
+  const float *w[CKV_CSA2_MAX_LAYERS];    /* [B][HI] f32 (FULL/REINDEX)         */
+  void    *out[CKV_CSA2_MAX_LAYERS];      /* [B][H][512] bf16                   */
+  float   *lse[CKV_CSA2_MAX_LAYERS];      /* NULL or [B][H] f32                 */
+  int32_t *idx_out[CKV_CSA2_MAX_LAYERS];  /* NULL or [B][topk] int32: indices used */
+  int32_t  pool_len;                      /* candidate pool of the FULL layer  */
+} ckv_csa2_group;
+
+ckv_status ckv_csa2_group_decode(const ckv_csa2_group *g, const int32_t *n_comp,
+                                 int32_t n_comp_max, const int32_t *win_len,
+                                 int32_t B, int32_t H, int32_t HI, int32_t topk,
+                                 float sm_scale, const ckv_plane *append_dst,
+                                 const void *append_src_bf16,
+                                 const int64_t *append_slot, int32_t n_append,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, returns the sticky device status recorded in `ws`
+ * (CKV_OK, CKV_ERR_DEVICE_BOUNDS or CKV_ERR_TIMEOUT) and clears it. */
+ckv_status ckv_read_device_status(void *ws, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *ckv_status_string(ckv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CKV_H */

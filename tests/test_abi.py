@@ -1,0 +1,78 @@
+"""The C ABI library loads and exports every symbol include/ckv.h declares,
+and host-side validation rejects bad arguments before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "compressed_kv_sparse_append_gb300", "libckv.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from compressed_kv_sparse_append_gb300.build import build
+        build()
+    return ctypes.CDLL(LIB)
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ckv.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ckv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    lib.ckv_status_string.restype = ctypes.c_char_p
+    for code, name in [(0, b"CKV_OK"), (-1, b"CKV_ERR_INVALID"), (-5, b"CKV_ERR_TIMEOUT"),
+                       (-6, b"CKV_ERR_DEVICE_BOUNDS"), (-99, b"CKV_ERR_UNKNOWN")]:
+        assert lib.ckv_status_string(code) == name
+
+
+def test_workspace_sizes(lib):
+    f = lib.ckv_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int32] * 7
+    assert f(0, 8, 128, 64, 0, 0, 0) == 256
+    a = f(1, 4, 128, 64, 262144, 512, 0)
+    b = f(1, 8, 128, 64, 262144, 512, 0)
+    assert 256 < a < b
+    assert f(1, 8, 64, 64, 65536, 512, 2048) > f(1, 8, 64, 64, 65536, 512, 0)
+    assert f(4, 8, 64, 64, 65536, 512, 2048) % 256 == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    lib.ckv_kv_append_quant.restype = ctypes.c_int32
+    # null plane
+    assert lib.ckv_kv_append_quant(None, None, None, 0, None, 0, None) == -1
+    fake = ctypes.c_void_p(0x10000)
+    p = CPlane(2, 512, 448, 1, 8, 0x10000, 0x20000)
+    # missing workspace
+    assert lib.ckv_kv_append_quant(ctypes.byref(p), fake, fake, 1, None, 0, None) == -4
+    # misaligned source
+    assert lib.ckv_kv_append_quant(ctypes.byref(p), ctypes.c_void_p(0x10008), fake, 1,
+                                   fake, 256, None) == -1
+    # unsupported dim / bad format / mixed with an odd scale block
+    for bad in (CPlane(2, 256, 448, 1, 8, 0x10000, 0x20000), CPlane(7, 512, 448, 1, 8, 0x10000, 0),
+                CPlane(1, 512, 100, 1, 8, 0x10000, 0x20000)):
+        assert lib.ckv_kv_append_quant(ctypes.byref(bad), fake, fake, 1, fake, 256, None) in (-1, -2)
+    # attention: too many heads, bad workspace size
+    kv = CPlane(0, 512, 448, 2, 64, 0x10000, 0)
+    lib.ckv_csa_sparse_attn.restype = ctypes.c_int32
+    args = [ctypes.byref(kv), ctypes.byref(kv), fake, fake, 2, 512, fake, 256, ctypes.c_float(0.04),
+            fake, None, fake, ctypes.c_size_t(256), None]
+    assert lib.ckv_csa_sparse_attn(*args) == -2
+    args[7] = 128
+    args[12] = ctypes.c_size_t(16)
+    assert lib.ckv_csa_sparse_attn(*args) == -4

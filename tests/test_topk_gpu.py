@@ -1,0 +1,134 @@
+"""csa_index_topk (through the C ABI) vs the oracle: exact top-k index sets
+(ties to the lower index), scores within the f32 accumulation bound, and
+the selection exact on the GPU's own scores."""
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_kv_sparse_append_gb300 import workloads as wl
+from oracle import fp_formats as ff
+from oracle import indexer as oi
+from tests.helpers import check_topk, ckv, gpu_plane, np32, score_eps
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(B, n_list, HI, fmt, seed, dup_frac=0.0):
+    keys = []
+    for b, n in enumerate(n_list):
+        k = wl.rms_rows((n, 128), seed * 100 + b, "cuda")
+        if dup_frac and n > 10:
+            g = torch.Generator().manual_seed(seed + b)
+            nd = int(dup_frac * n)
+            dst = torch.randperm(n, generator=g)[:nd]
+            srcs = torch.randint(0, n, (nd,), generator=g)
+            k[dst.cuda()] = k[srcs.cuda()]
+        keys.append(k)
+    qi = torch.stack([wl.rms_rows((HI, 128), seed * 1000 + b, "cuda") for b in range(B)])
+    w = torch.stack([wl.head_weights((HI,), seed * 7 + b, "cuda") for b in range(B)])
+    cap = max(n_list) + 5
+    plane = gpu_plane(fmt, 128, keys, cap)
+    return keys, qi, w, plane
+
+
+def _oracle_scores(keys_b, qi_b, w_b, fmt):
+    kv = ff.dequantize_entries(*ff.quantize_entries(np32(keys_b), fmt), fmt)
+    qv = oi.indexer_query(np32(qi_b), fmt == "fp4")
+    w = np32(w_b).astype(np.float64)
+    return oi.index_scores(qv, w, kv), score_eps(qv, w, kv)
+
+
+def _gpu_selection_of(dbg_row, n, k):
+    s = dbg_row[:n].astype(np.float64)
+    s = np.where(s == 0, 0.0, s)
+    return oi.topk_set(s, k)
+
+
+@pytest.mark.parametrize("fmt,HI,n_list,topk", [
+    ("bf16", 4, [1024], 512),                      # the tiny BF16 workload shape
+    ("fp4", 64, [3000, 1500, 700], 512),           # ragged, one sequence below... above k
+    ("fp4", 64, [300, 9000], 512),                 # n_comp < k: -1 padding
+    ("fp4", 16, [20000], 1024),                    # several chunks, k = 1024
+    ("bf16", 8, [5000, 17], 64),
+])
+def test_index_topk_matches_oracle(fmt, HI, n_list, topk):
+    b = ckv()
+    B = len(n_list)
+    keys, qi, w, plane = _case(B, n_list, HI, fmt, seed=len(n_list) * 31 + HI + topk)
+    n_comp = torch.tensor(n_list, dtype=torch.int32, device="cuda")
+    n_max = max(n_list)
+    dbg = torch.full((B, n_max), float("nan"), device="cuda")
+    idx = b.csa_index_topk(plane, n_comp, n_max, qi, w, topk, dbg_scores=dbg)
+    torch.cuda.synchronize()
+    idx = idx.cpu().numpy()
+    dbg = dbg.cpu().numpy()
+    for s in range(B):
+        sc, eps = _oracle_scores(keys[s], qi[s], w[s], fmt)
+        n = n_list[s]
+        err = np.abs(dbg[s, :n] - sc)
+        assert np.all(err <= eps + 1e-30), "score error %g > bound" % (err / np.maximum(eps, 1e-30)).max()
+        assert np.array_equal(idx[s], _gpu_selection_of(dbg[s], n, topk)), "selection on GPU scores"
+        assert check_topk(idx[s], sc, eps, topk, where="seq %d" % s) == 0
+
+
+def test_index_topk_exact_ties_go_to_lower_index():
+    """Duplicated key vectors quantise to identical bytes, so their scores tie
+    exactly (bitwise on the GPU too); the boundary must go to lower indices."""
+    b = ckv()
+    n = 6000
+    keys, qi, w, plane = _case(1, [n], 64, "fp4", seed=77, dup_frac=0.3)
+    # crowd the boundary: copy the entries ranked around 512 many times
+    sc, _ = _oracle_scores(keys[0], qi[0], w[0], "fp4")
+    order = np.lexsort((np.arange(n), -sc))
+    k2 = wl.inject_ties(keys[0], order, seed=3, frac=0.2, donor_lo=500, donor_hi=520)
+    plane = gpu_plane("fp4", 128, [k2], n)
+    sc, eps = _oracle_scores(k2, qi[0], w[0], "fp4")
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    dbg = torch.zeros((1, n), device="cuda")
+    idx = b.csa_index_topk(plane, n_comp, n, qi, w, 512, dbg_scores=dbg).cpu().numpy()[0]
+    d = dbg.cpu().numpy()[0]
+    kb = plane.data.cpu().numpy()[0]
+    # identical bytes -> identical f32 scores
+    _, inv = np.unique(np.concatenate([kb, plane.scale.cpu().numpy()[0]], axis=1), axis=0,
+                       return_inverse=True)
+    for g in np.unique(inv):
+        members = np.nonzero(inv == g)[0]
+        assert len(set(d[members].tolist())) == 1
+    boundary = sc[oi.topk_set(sc, 512)].min()
+    assert (sc == boundary).sum() > 1, "the test must put an exact tie on the boundary"
+    assert np.array_equal(idx, oi.topk_set(sc, 512))
+    assert np.array_equal(idx, _gpu_selection_of(d, n, 512))
+
+
+def test_index_pool_and_reindex():
+    """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool."""
+    b = ckv()
+    n = 12000
+    keys, qi, w, plane = _case(2, [n, n - 999], 64, "fp4", seed=5)
+    n_comp = torch.tensor([n, n - 999], dtype=torch.int32, device="cuda")
+    idx, pool = b.csa_index_topk(plane, n_comp, n, qi, w, 512, pool_out=2048)
+    qi2 = torch.stack([wl.rms_rows((64, 128), 4242 + s, "cuda") for s in range(2)])
+    w2 = torch.stack([wl.head_weights((64,), 99 + s, "cuda") for s in range(2)])
+    idx2 = b.csa_index_topk(plane, n_comp, n, qi2, w2, 512, pool=pool)
+    torch.cuda.synchronize()
+    idx, pool, idx2 = idx.cpu().numpy(), pool.cpu().numpy(), idx2.cpu().numpy()
+    for s in range(2):
+        sc, eps = _oracle_scores(keys[s], qi[s], w[s], "fp4")
+        assert check_topk(pool[s], sc, eps, 2048, where="pool") == 0
+        assert check_topk(idx[s], sc, eps, 512, where="full") == 0
+        sc2, eps2 = _oracle_scores(keys[s], qi2[s], w2[s], "fp4")
+        assert check_topk(idx2[s], sc2, eps2, 512, candidates=pool[s], where="reindex") == 0
+        assert set(idx2[s]) <= set(pool[s])
+
+
+def test_index_out_of_range_pool_entry_is_flagged():
+    b = ckv()
+    keys, qi, w, plane = _case(1, [100], 8, "fp4", seed=9)
+    n_comp = torch.tensor([100], dtype=torch.int32, device="cuda")
+    pool = torch.tensor([[5, 7, 250, -1, 9]], dtype=torch.int32, device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, 8, 100, 2, 0))
+    idx = b.csa_index_topk(plane, n_comp, 100, qi, w, 2, pool=pool, ws=ws)
+    assert b.read_device_status(ws) == -6
+    sc, _ = _oracle_scores(keys[0], qi[0], w[0], "fp4")
+    assert list(idx.cpu().numpy()[0]) == list(oi.topk_set(sc, 2, candidates=[5, 7, 9]))
