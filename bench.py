@@ -13,7 +13,7 @@ workload (see compressed_kv_sparse_append_gb300/workloads.py):
   * hca_1m: kv_append_quant + hca_attn;
   * csa2_group: one csa2_group_decode call (six layer-steps).
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
-on the launching stream, with a 256 MB L2 flush (outside the events) before
+on the launching stream, with a 1 GiB L2 flush (outside the events) before
 every step; barrier + max over ranks when launched with torchrun (each rank
 runs its own replica: batch sharding needs no collective).
 """
@@ -281,24 +281,37 @@ def make_step(wl, dev, ckv, wlmod):
 
 # ------------------------------------------------------------------ timing --
 
+FLUSH_BYTES = 1 << 30   # > L2 (129 MB); ~150 us of GPU time that also hides host enqueue
+
+
 def time_steps(step, K, W, dev):
+    """K steps, each after an L2 flush.  The flush keeps the GPU busy while
+    the host enqueues the step's launches, so the events bracket device time
+    only; the host enqueue time is returned for checking that assumption."""
     import torch
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(W):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    host_us = []
     for i in range(K):
+        fl[i][0].record()
         flush.zero_()
+        fl[i][1].record()
+        t0 = time.perf_counter()
         ev[i][0].record()
         step(timer=(ev[i][2], ev[i][3]))
         ev[i][1].record()
+        host_us.append((time.perf_counter() - t0) * 1e6)
     torch.cuda.synchronize()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     dom_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    return step_ms, dom_ms
+    flush_us = [f[0].elapsed_time(f[1]) * 1000.0 for f in fl]
+    return step_ms, dom_ms, statistics.median(host_us), statistics.median(flush_us)
 
 
 def time_e2e(step, host, K, W, dev):
@@ -310,7 +323,7 @@ def time_e2e(step, host, K, W, dev):
     d_in = list(host["inputs"])
     h_in = [t.cpu().pin_memory() for t in d_in]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in host["outputs"]]
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def one():
         for hsrc, ddst in zip(h_in, d_in):
@@ -439,7 +452,7 @@ def workload_config(wl):
     return {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "context_tokens": wl.T,
             "compressed_entries": wl.n_comp, "heads": wl.H, "indexer_heads": wl.HI, "topk": wl.topk,
             "window": wl.W, "main_kv": wl.main_fmt, "indexer_keys": wl.idx_fmt or None,
-            "layers_per_step": wl.n_layers, "l2": "flushed (256 MB write) before every step"}
+            "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step"}
 
 
 def main():
@@ -459,7 +472,7 @@ def main():
     if dist:
         dist.barrier()
     with ClockSampler(local) as clk:
-        step_ms, dom_ms = time_steps(step, args.steps, args.warmup, dev)
+        step_ms, dom_ms, host_us, flush_us = time_steps(step, args.steps, args.warmup, dev)
     status = ckv.read_device_status(ws)
     if status != 0:
         raise RuntimeError("device status %d after the timed steps" % status)
@@ -483,7 +496,8 @@ def main():
                     "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
             "gpu_launches": launches * args.steps,
             "clocks": clk.result,
-            "step_ms_median": statistics.median(step_ms)}
+            "step_ms_median": statistics.median(step_ms),
+            "host_enqueue_us": host_us, "flush_us": flush_us}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, desc, _ = cpu_oracle_sample(wl, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}

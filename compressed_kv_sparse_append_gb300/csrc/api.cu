@@ -45,7 +45,7 @@ ckv_status check_plane(const ckv_plane* p, int dim, int B) {
 
 struct IndexLayout {
   int chunk, n_chunks, K_sel;
-  size_t counters_off, key_off, idx_off, bytes;  // relative to the index region
+  size_t counters_off, hist_off, key_off, idx_off, bytes;  // relative to the index region
 };
 
 IndexLayout index_layout(int B, int n_comp_max, int K_sel, bool pool_mode, int pool_len) {
@@ -66,7 +66,8 @@ IndexLayout index_layout(int B, int n_comp_max, int K_sel, bool pool_mode, int p
     if (L.n_chunks < 1) L.n_chunks = 1;
   }
   L.counters_off = 0;
-  L.key_off = align_up((size_t)B * 4, 256);
+  L.hist_off = align_up((size_t)B * 4, 256);
+  L.key_off = L.hist_off + (size_t)B * 4096 * 4;
   const size_t cand = (size_t)B * L.n_chunks * K_sel * 4;
   L.idx_off = L.key_off + align_up(cand, 256);
   L.bytes = L.idx_off + align_up(cand, 256);
@@ -122,6 +123,7 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.chunk = L.chunk;
   a.n_chunks = L.n_chunks;
   a.counters = reinterpret_cast<uint32_t*>(region + L.counters_off);
+  a.ghist = reinterpret_cast<uint32_t*>(region + L.hist_off);
   a.cand_key = reinterpret_cast<uint32_t*>(region + L.key_off);
   a.cand_idx = reinterpret_cast<int32_t*>(region + L.idx_off);
   a.out_idx = out_idx;

@@ -27,6 +27,7 @@ struct AttnArgs {
   __nv_bfloat16* out;     // [B][H][512]
   float* lse;             // [B][H] or null
   int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
+  int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   DevStatus* st;
 };
 

@@ -27,6 +27,7 @@ struct IndexArgs {
   uint32_t* cand_key;             // workspace [B][n_chunks][K_sel]
   int32_t* cand_idx;
   uint32_t* counters;             // workspace [B], zero between calls
+  uint32_t* ghist;                // workspace [B][4096] key histogram, zero between calls
   int32_t* out_idx;
   int32_t* out_pool;
   float* dbg;

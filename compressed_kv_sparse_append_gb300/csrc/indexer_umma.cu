@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   }
   if (tid == 0) msm.n_real = (uint32_t)n_elem;
   __syncthreads();
-  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, msm);
+  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, keys, msm);
 }
 
 namespace {

@@ -1,13 +1,27 @@
-// Candidate stage of csa_index_topk shared by the scorers: the chunk's local
-// top-K goes to the workspace in ascending entry order; the last CTA of the
-// sequence (atomic ticket, no spinning) merges all chunks' candidates into
-// the exact top-K (and, for a CSA2 Full layer, the top-k of that pool).
+// Candidate stage of csa_index_topk shared by the scorers.
+//
+// Each CTA keeps its chunk's top-K candidates (K = max(topk, pool_out)) in
+// ascending entry order in the workspace and adds them to a per-sequence
+// histogram of the top 12 key bits (global atomics).  The last CTA of the
+// sequence (atomic ticket, no spinning) then
+//   (a) finds the histogram bin holding the K-th largest key,
+//   (b) compacts, in order, the candidates in or above that bin into shared
+//       memory (one pass over the candidate lists),
+//   (c) runs the exact radix select on those survivors,
+// and writes the ascending top-k (and the CSA2 Full layer's pool).  Ties at
+// the threshold go to the earliest, i.e. lowest, entries ("DeepSeek-V4 KV
+// Cache 深度分析", §四: the indexer keeps the top-k blocks).  If the threshold
+// bin is too crowded for shared memory the select runs on the full lists.
 #pragma once
 
 #include "select.cuh"
 #include "indexer.cuh"
 
 namespace ckv {
+
+constexpr int kHistShift = 20;                 // 12-bit histogram of the key
+constexpr int kHistBins = 1 << (32 - kHistShift);
+constexpr int kMaxSurv = kMaxChunk / 2;        // survivors held in shared memory
 
 template <int NT>
 struct MergeSmem {
@@ -16,62 +30,123 @@ struct MergeSmem {
   SelectSmem<NT> sel;
   int ticket;
   uint32_t n_real;
+  uint32_t bcast[2];
 };
 
-// Candidate merge and outputs (run by the last CTA of sequence b).
-template <int NT>
-__device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm) {
-  const int n_slots = a.n_chunks * a.K_sel;
-  const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
-  const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
-  if (threadIdx.x == 0) sm.n_real = 0;
-  __syncthreads();
-  uint32_t mine = 0;
-  for (int i = threadIdx.x; i < n_slots; i += NT) mine += __ldcg(ck + i) != 0u;
-  atomicAdd(&sm.n_real, mine);
-  __syncthreads();
-  const int n_real = (int)sm.n_real;
-  auto get = [&](int i) { return __ldcg(ck + i); };
+// Final outputs from an ordered candidate source of n elements.
+template <int NT, class GK, class GE>
+__device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk, GE ge,
+                             MergeSmem<NT>& sm) {
+  int32_t* oi = a.out_idx + (int64_t)b * a.topk;
   if (a.pool_out > 0) {
     const int kp = min(a.pool_out, n_real);
     block_select_ordered<NT>(
-        n_slots, kp, get,
+        n, kp, gk,
         [&](int pos, int i) {
-          sm.pool_key[pos] = __ldcg(ck + i);
-          sm.pool_ent[pos] = __ldcg(ci + i);
+          sm.pool_key[pos] = gk(i);
+          sm.pool_ent[pos] = ge(i);
         },
         sm.sel);
     int32_t* op = a.out_pool + (int64_t)b * a.pool_out;
     for (int i = threadIdx.x; i < a.pool_out; i += NT) op[i] = i < kp ? sm.pool_ent[i] : -1;
     const int kk = min(a.topk, kp);
-    int32_t* oi = a.out_idx + (int64_t)b * a.topk;
     block_select_ordered<NT>(
         kp, kk, [&](int i) { return sm.pool_key[i]; },
         [&](int pos, int i) { oi[pos] = sm.pool_ent[i]; }, sm.sel);
     for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
   } else {
     const int kk = min(a.topk, n_real);
-    int32_t* oi = a.out_idx + (int64_t)b * a.topk;
-    block_select_ordered<NT>(
-        n_slots, kk, get, [&](int pos, int i) { oi[pos] = __ldcg(ci + i); }, sm.sel);
+    block_select_ordered<NT>(n, kk, gk, [&](int pos, int i) { oi[pos] = ge(i); }, sm.sel);
     for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
   }
 }
 
-// Local top-K of a scored chunk -> workspace; then the ticket.
+// Merge of all chunks' candidates (run by the last CTA of sequence b).
+// surv_key / surv_ent: kMaxSurv-entry shared-memory scratch.
+template <int NT>
+__device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* surv_key,
+                               int32_t* surv_ent) {
+  const int n_slots = a.n_chunks * a.K_sel;
+  const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
+  const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
+  uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
+  const int K = a.pool_out > 0 ? a.pool_out : a.topk;
+
+  // (a) threshold bin: descending bins, contiguous per thread
+  constexpr int per = (kHistBins + NT - 1) / NT;
+  const int p0 = min(kHistBins, (int)threadIdx.x * per), p1 = min(kHistBins, p0 + per);
+  uint32_t cnt = 0;
+  for (int p = p0; p < p1; ++p) cnt += __ldcg(hist + (kHistBins - 1 - p));
+  uint32_t before, dummy, total, dummy2;
+  block_scan2<NT>(cnt, 0u, before, dummy, total, dummy2, sm.sel);
+  const int n_real = (int)total;
+  const uint32_t keff = (uint32_t)min(K, n_real);
+  if (threadIdx.x == 0) sm.bcast[0] = 0u;
+  __syncthreads();
+  if (keff > 0 && before < keff && before + cnt >= keff) {
+    uint32_t cum = before;
+    for (int p = p0; p < p1; ++p) {
+      const uint32_t c = __ldcg(hist + (kHistBins - 1 - p));
+      if (cum + c >= keff) {
+        sm.bcast[0] = (uint32_t)(kHistBins - 1 - p);
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  const uint32_t tb = sm.bcast[0];
+  for (int i = threadIdx.x; i < kHistBins; i += NT) hist[i] = 0u;   // ready for the next call
+
+  // (b) order-preserving compaction of the survivors (key bin >= tb)
+  const int per2 = (n_slots + NT - 1) / NT;
+  const int i0 = min(n_slots, (int)threadIdx.x * per2), i1 = min(n_slots, i0 + per2);
+  uint32_t mine = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t u = __ldcg(ck + i);
+    mine += (u != 0u) && ((u >> kHistShift) >= tb);
+  }
+  uint32_t pos, d3, n_surv, d4;
+  block_scan2<NT>(mine, 0u, pos, d3, n_surv, d4, sm.sel);
+  if (n_surv <= (uint32_t)kMaxSurv) {
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t u = __ldcg(ck + i);
+      if ((u != 0u) && ((u >> kHistShift) >= tb)) {
+        surv_key[pos] = u;
+        surv_ent[pos] = __ldcg(ci + i);
+        ++pos;
+      }
+    }
+    __syncthreads();
+    emit_outputs<NT>(
+        a, b, (int)n_surv, n_real, [&](int i) { return surv_key[i]; },
+        [&](int i) { return surv_ent[i]; }, sm);
+  } else {
+    emit_outputs<NT>(
+        a, b, n_slots, n_real, [&](int i) { return __ldcg(ck + i); },
+        [&](int i) { return __ldcg(ci + i); }, sm);
+  }
+}
+
+// Local top-K of a scored chunk -> workspace (+ histogram); then the ticket.
+// `scratch` (kMaxChunk u32 of shared memory) may alias `keys`.
 template <int NT>
 __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int n_elem,
-                                       int64_t first_entry, const uint32_t* keys, MergeSmem<NT>& sm) {
+                                       int64_t first_entry, const uint32_t* keys, uint32_t* scratch,
+                                       MergeSmem<NT>& sm) {
   const int slot0 = (b * a.n_chunks + chunk) * a.K_sel;
   uint32_t* ck = a.cand_key + slot0;
   int32_t* ci = a.cand_idx + slot0;
+  uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
   const int kk = min(a.K_sel, (int)sm.n_real);
   const int32_t* pool = a.pool ? a.pool + (int64_t)b * a.pool_len + first_entry : nullptr;
   block_select_ordered<NT>(
       n_elem, kk, [&](int i) { return keys[i]; },
       [&](int pos, int i) {
-        ck[pos] = keys[i];
+        const uint32_t u = keys[i];
+        ck[pos] = u;
         ci[pos] = pool ? pool[i] : (int32_t)(first_entry + i);
+        atomicAdd(hist + (u >> kHistShift), 1u);
       },
       sm.sel);
   for (int i = kk + threadIdx.x; i < a.K_sel; i += NT) {
@@ -84,7 +159,7 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
   __threadfence();
-  merge_and_emit(a, b, sm);
+  merge_and_emit<NT>(a, b, sm, scratch, reinterpret_cast<int32_t*>(scratch + kMaxSurv));
   if (threadIdx.x == 0) atomicExch(a.counters + b, 0u);
 }
 
