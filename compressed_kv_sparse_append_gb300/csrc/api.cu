@@ -206,6 +206,9 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.lse = lse;
   a.G = 1;
   a.st = st;
+  a.use_tma = 0;
+  const char* pe = getenv("CKV_DEBUG_PROGRESS");
+  a.progress = (pe && pe[0] == '1') ? 1 : 0;
   return a;
 }
 
@@ -379,17 +382,19 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
     }
     if (s) return s;
   }
+  // every layer's attention in one launch (grid z = layer)
+  AttnArgs la[CKV_CSA2_MAX_LAYERS];
+  int G = 4;
+  for (int l = 0; l < L; ++l) G = G < choose_pairs(B, topk + (int)g->win[g->kv_src[l]].cap)
+                                      ? G : choose_pairs(B, topk + (int)g->win[g->kv_src[l]].cap);
   for (int l = 0; l < L; ++l) {
     const int k = g->kv_src[l];
-    AttnArgs a = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l],
-                           g->lse[l], dst);
-    a.idx = layer_idx[l];
-    a.topk = topk;
-    a.G = choose_pairs(B, topk + (int)g->win[k].cap);
-    s = cuda_status(launch_attention(a, B, st));
-    if (s) return s;
+    la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
+    la[l].idx = layer_idx[l];
+    la[l].topk = topk;
+    la[l].G = G;
   }
-  return CKV_OK;
+  return cuda_status(launch_attention_layers(la, L, B, st));
 }
 
 ckv_status ckv_read_device_status(void* ws, void* stream) {

@@ -64,7 +64,21 @@ constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (factor 256)
 // barrier indices
 constexpr int B_TMA = 0, B_EFULL = kStages, B_EEMPTY = 2 * kStages;
 constexpr int B_SFULL = 3 * kStages, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-              B_XFULL = B_ODONE + 1;
+              B_XFULL = B_ODONE + 1, B_CLUSTER = B_XFULL + 2;
+
+// Cluster-wide barrier `k` built on mbarriers with a bounded wait: thread 0
+// of every CTA arrives (release, cluster scope) on barrier k of every CTA of
+// the cluster after a CTA barrier; every thread then waits on its own CTA's
+// barrier k (acquire, cluster scope).  Each barrier is used once (phase 0).
+__device__ __forceinline__ void cluster_barrier(uint64_t* bars_k, int n_cta, DevStatus* st,
+                                                volatile int* abort, int where) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t local = smem_u32(bars_k);
+    for (int r = 0; r < n_cta; ++r) mbar_arrive_remote(mapa(local, (uint32_t)r));
+  }
+  mbar_wait(bars_k, 0, st, abort, where);
+}
 
 // D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.
 __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -216,7 +230,8 @@ __device__ __forceinline__ int chunks_per_row(int fmt, int half) {
 
 __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
-                AttnArgs a) {
+                const __grid_constant__ AttnBatch batch) {
+  const AttnArgs& a = batch.layer[blockIdx.z];
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -255,6 +270,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       mbar_init(&bars[B_XFULL + k], 128);
     }
     mbar_init(&bars[B_ODONE], 1);
+    mbar_init(&bars[B_CLUSTER], 2 * G);
+    mbar_init(&bars[B_CLUSTER + 1], 2 * G);
     fence_mbar_init();
   }
   if (warp == 5) tmem_alloc(tslot, kTmemCols);
@@ -263,6 +280,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   volatile int* abort_p = &abort_flag;
+  const bool prog = a.progress != 0;
+  if (tid == 0) progress(a.st, prog, 0);
 
   if (warp >= 6) {
     // Q[b, h, half] -> TMEM as the bf16 A operand (lane h, two elements per column)
@@ -304,6 +323,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
         const CUtensorMap* map = tl.win ? &map_win : &map_kv;
         const int64_t row = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap) + tl.start;
+        progress(a.st, prog, 9);
         mbar_expect_tx(&bars[B_TMA + s], kEBytes);
 #pragma unroll
         for (int kc = 0; kc < 4; ++kc)
@@ -362,6 +382,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_EFULL + s]);
+      if (p == 0) progress(a.st, prog, 5);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------ MMA issuer ----
@@ -379,6 +400,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
         umma_commit(&bars[B_ODONE]);
         umma_commit(&bars[B_EEMPTY + sj]);
+        progress(a.st, prog, 4);
         return true;
       };
       bool ok = true;
@@ -394,6 +416,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
           umma_f16_ta(tmem + kColS + 64 * bi, tQ + 8 * ks, db, kIdescQK, ks > 0);
         }
         umma_commit(&bars[B_SFULL + bi]);
+        progress(a.st, prog, 1);
         if (i > 0) ok = issue_pv(i - 1);
       }
       if (ok && n_my > 0) issue_pv(n_my - 1);
@@ -411,6 +434,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const uint32_t tS = tmem + kColS + 64 * bi + lane_base;
       if (!mbar_wait(&bars[B_SFULL + bi], (i >> 1) & 1, a.st, abort_p, 26)) break;
       tc_fence_after();
+      if (h == 0) progress(a.st, prog, 2);
       uint32_t sr[64];
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
@@ -436,6 +460,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         vmask &= im;
       }
       if (!mbar_wait(&bars[B_XFULL + bi], (i >> 1) & 1, a.st, abort_p, 27)) break;
+      if (h == 0) progress(a.st, prog, 3);
       float tmax = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -485,8 +510,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[B_PFULL + bi]);
+      if (h == 0) progress(a.st, prog, 8);
     }
     if (n_my > 0) {
+      // s_full of the last tile implies every PV up to n_my - 3 is done, so
+      // o_done may still owe two phases: wait for them in order (a single
+      // parity wait could alias the older one).
+      if (n_my >= 2) mbar_wait(&bars[B_ODONE], (n_my - 2) & 1, a.st, abort_p, 29);
       mbar_wait(&bars[B_ODONE], (n_my - 1) & 1, a.st, abort_p, 29);
       tc_fence_after();
     }
@@ -512,7 +542,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     ml[h] = make_float2(m_used, l);
   }
   tc_fence_before();
-  cluster_sync();
+  if (tid == 0) progress(a.st, prog, 6);
+  cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
 
   if (warp >= 6) {
     // --------------------------------------------- in-cluster merge ----
@@ -565,11 +596,12 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   }
 
   tc_fence_before();
-  cluster_sync();
+  cluster_barrier(&bars[B_CLUSTER + 1], 2 * G, a.st, abort_p, 31);
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (tid == 0) progress(a.st, prog, 7);
 }
 
 namespace {
@@ -602,7 +634,7 @@ bool encode_bf16_rows(CUtensorMap* m, const void* data, int64_t rows) {
 
 }  // namespace
 
-cudaError_t launch_attention(const AttnArgs& a_in, int B, cudaStream_t stream) {
+cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream) {
   static int attr_done = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -612,30 +644,40 @@ cudaError_t launch_attention(const AttnArgs& a_in, int B, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done = dev;
   }
-  AttnArgs a = a_in;
+  if (n < 1 || n > kMaxLayers) return cudaErrorInvalidValue;
+  AttnBatch batch;
+  memset(&batch, 0, sizeof(batch));
+  for (int l = 0; l < n; ++l) {
+    batch.layer[l] = layers[l];
+    batch.layer[l].use_tma = 0;
+  }
   CUtensorMap mk, mw;
   memset(&mk, 0, sizeof(mk));
   memset(&mw, 0, sizeof(mw));
-  a.use_tma = 0;
-  // Contiguous BF16 rows (HCA) stream through TMA; gathered or quantised rows
-  // go through the producer warps.
-  if (a.fmt == CKV_FMT_BF16 && a.idx == nullptr &&
-      encode_bf16_rows(&mk, a.kv_data, (int64_t)B * a.kv_cap) &&
-      encode_bf16_rows(&mw, a.win_data, (int64_t)B * a.win_cap))
-    a.use_tma = 1;
+  // Contiguous BF16 rows (HCA, one layer) stream through TMA; gathered or
+  // quantised rows go through the producer warps.
+  const AttnArgs& a0 = layers[0];
+  if (n == 1 && a0.fmt == CKV_FMT_BF16 && a0.idx == nullptr &&
+      encode_bf16_rows(&mk, a0.kv_data, (int64_t)B * a0.kv_cap) &&
+      encode_bf16_rows(&mw, a0.win_data, (int64_t)B * a0.win_cap))
+    batch.layer[0].use_tma = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * a.G, B, 1);
+  cfg.gridDim = dim3(2 * a0.G, B, n);
   cfg.blockDim = dim3(kThreadsAttn, 1, 1);
   cfg.dynamicSmemBytes = kSmemAttn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * a.G;
+  attr[0].val.clusterDim.x = 2 * a0.G;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_kernel, mk, mw, a);
+  return cudaLaunchKernelEx(&cfg, attn_kernel, mk, mw, batch);
+}
+
+cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream) {
+  return launch_attention_layers(&a, 1, B, stream);
 }
 
 }  // namespace ckv

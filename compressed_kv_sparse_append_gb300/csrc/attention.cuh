@@ -28,9 +28,17 @@ struct AttnArgs {
   float* lse;             // [B][H] or null
   int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
+  int progress;           // debugging: count pipeline events in the status block
   DevStatus* st;
 };
 
+constexpr int kMaxLayers = 8;
+struct AttnBatch {
+  AttnArgs layer[kMaxLayers];  // one launch runs every layer (grid z = layer)
+};
+
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream);
+// All `n` layers share B, G and the row format; layer l uses grid z = l.
+cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream);
 
 }  // namespace ckv

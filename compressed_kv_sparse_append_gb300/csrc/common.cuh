@@ -32,8 +32,12 @@ __device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t deta
   atomicExch(&st->detail, detail);
 }
 
-// Wall-clock limit of every spin-wait in the kernels (nanoseconds).
+// Limits of every spin-wait in the kernels: wall clock, SM cycles and
+// iterations -- whichever expires first ends the wait, so a wait ends even if
+// one of the clocks does not advance.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr long long kWaitLimitCycles = 4000000000ll;
+constexpr uint32_t kWaitLimitIters = 1u << 24;
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -92,17 +96,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevSta
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const long long c0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (it >= kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
+          globaltimer() - t0 > kWaitLimitNs) {
         report(st, CKV_ERR_TIMEOUT, where);
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+// Optional progress counters (debugging): slot k of the status block's
+// spare words counts events of kind k.  Enabled per launch.
+__device__ __forceinline__ void progress(DevStatus* st, bool on, int k) {
+  if (on && st != nullptr) atomicAdd(reinterpret_cast<unsigned int*>(&st->pad[k]), 1u);
 }
 
 // ------------------------------------------------------------- fences ----

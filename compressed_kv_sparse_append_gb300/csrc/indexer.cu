@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
   }
   atomicAdd(&sm.m.n_real, mine);
   __syncthreads();
-  chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.keys, sm.m);
+  chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.keys, kMaxChunk / 2,
+                                      sm.m);
 }
 
 size_t index_smem_bytes() { return sizeof(IndexSmem); }

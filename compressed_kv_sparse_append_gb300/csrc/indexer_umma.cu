@@ -265,7 +265,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
   }
   if (tid == 0) msm.n_real = (uint32_t)n_elem;
   __syncthreads();
-  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, keys, msm);
+  // The merge's survivors may use everything below the merge state: the
+  // pipeline ring, the query tiles and the chunk's scores are all dead here.
+  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, reinterpret_cast<uint32_t*>(g),
+                                    (int)(kOffMerge / 8), msm);
 }
 
 namespace {

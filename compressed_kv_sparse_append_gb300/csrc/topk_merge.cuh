@@ -21,7 +21,6 @@ namespace ckv {
 
 constexpr int kHistShift = 20;                 // 12-bit histogram of the key
 constexpr int kHistBins = 1 << (32 - kHistShift);
-constexpr int kMaxSurv = kMaxChunk / 2;        // survivors held in shared memory
 
 template <int NT>
 struct MergeSmem {
@@ -62,10 +61,10 @@ __device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk
 }
 
 // Merge of all chunks' candidates (run by the last CTA of sequence b).
-// surv_key / surv_ent: kMaxSurv-entry shared-memory scratch.
+// surv_key / surv_ent: `surv_cap`-entry shared-memory scratch.
 template <int NT>
 __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* surv_key,
-                               int32_t* surv_ent) {
+                               int32_t* surv_ent, int surv_cap) {
   const int n_slots = a.n_chunks * a.K_sel;
   const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
   const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
@@ -108,7 +107,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   }
   uint32_t pos, d3, n_surv, d4;
   block_scan2<NT>(mine, 0u, pos, d3, n_surv, d4, sm.sel);
-  if (n_surv <= (uint32_t)kMaxSurv) {
+  if (n_surv <= (uint32_t)surv_cap) {
     for (int i = i0; i < i1; ++i) {
       const uint32_t u = __ldcg(ck + i);
       if ((u != 0u) && ((u >> kHistShift) >= tb)) {
@@ -129,11 +128,12 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
 }
 
 // Local top-K of a scored chunk -> workspace (+ histogram); then the ticket.
-// `scratch` (kMaxChunk u32 of shared memory) may alias `keys`.
+// `scratch` (2 * surv_cap words of shared memory, free once the chunk's own
+// selection is done) may alias `keys`.
 template <int NT>
 __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int n_elem,
                                        int64_t first_entry, const uint32_t* keys, uint32_t* scratch,
-                                       MergeSmem<NT>& sm) {
+                                       int surv_cap, MergeSmem<NT>& sm) {
   const int slot0 = (b * a.n_chunks + chunk) * a.K_sel;
   uint32_t* ck = a.cand_key + slot0;
   int32_t* ci = a.cand_idx + slot0;
@@ -159,7 +159,7 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
   __threadfence();
-  merge_and_emit<NT>(a, b, sm, scratch, reinterpret_cast<int32_t*>(scratch + kMaxSurv));
+  merge_and_emit<NT>(a, b, sm, scratch, reinterpret_cast<int32_t*>(scratch + surv_cap), surv_cap);
   if (threadIdx.x == 0) atomicExch(a.counters + b, 0u);
 }
 

@@ -16,12 +16,13 @@ def _rows(n, dim, seed, device="cuda"):
     x = wl.rms_rows((n, dim), seed, device, spikes=True).float()
     # special rows: zeros, negative zeros / tiny negatives, the FP4 extreme
     # (+-2688 and beyond), huge dynamic range within a block
-    x[0] = 0.0
-    x[1] = -0.0
-    x[1, ::3] = -1e-30
-    x[2, :16] = torch.tensor([2688.0, -2688.0, 5000.0, 1.0] + [0.5] * 12)
-    x[3] = x[3] * 1e-3
-    x[4, ::2] *= 300.0
+    specials = [lambda r: r.zero_(),
+                lambda r: (r.fill_(-0.0), r[::3].fill_(-1e-30)),
+                lambda r: r[:16].copy_(torch.tensor([2688.0, -2688.0, 5000.0, 1.0] + [0.5] * 12)),
+                lambda r: r.mul_(1e-3),
+                lambda r: r[::2].mul_(300.0)]
+    for i, f in enumerate(specials[:n]):
+        f(x[i])
     return x.to(torch.bfloat16)
 
 
