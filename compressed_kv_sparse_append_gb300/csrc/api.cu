@@ -48,8 +48,12 @@ struct IndexLayout {
   size_t counters_off, hist_off, key_off, idx_off, bytes;  // relative to the index region
 };
 
-IndexLayout index_layout(int B, int n_comp_max, int K_sel, bool pool_mode, int pool_len) {
+// Candidate rows hold K_sel slots, a multiple of 4 (16-byte rows).
+int pad4(int k) { return (k + 3) & ~3; }
+
+IndexLayout index_layout(int B, int n_comp_max, int K_sel_in, bool pool_mode, int pool_len) {
   IndexLayout L;
+  const int K_sel = pad4(K_sel_in);
   L.K_sel = K_sel;
   if (pool_mode) {
     L.chunk = 256;
@@ -102,7 +106,7 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
                      const void* q_idx, const float* w, int HI, int topk, const int32_t* pool,
                      int pool_len, int32_t* out_idx, int32_t* out_pool, int pool_out, float* dbg,
                      DevStatus* st, uint8_t* region, cudaStream_t stream) {
-  const int K_sel = out_pool ? pool_out : topk;
+  const int K_sel = pad4(out_pool ? pool_out : topk);
   IndexLayout L = index_layout(B, n_comp_max, K_sel, pool != nullptr, pool_len);
   IndexArgs a;
   a.kdata = static_cast<const uint8_t*>(keys->data);

@@ -77,7 +77,7 @@ __device__ __forceinline__ void cluster_barrier(uint64_t* bars_k, int n_cta, Dev
     const uint32_t local = smem_u32(bars_k);
     for (int r = 0; r < n_cta; ++r) mbar_arrive_remote(mapa(local, (uint32_t)r));
   }
-  mbar_wait(bars_k, 0, st, abort, where);
+  mbar_wait_poll(bars_k, 0, st, abort, where);
 }
 
 // D(tmem) (+)= A(tmem) * B(smem desc), kind::f16.
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
         vmask &= im;
       }
-      if (!mbar_wait(&bars[B_XFULL + bi], (i >> 1) & 1, a.st, abort_p, 27)) break;
+      if (!mbar_wait_poll(&bars[B_XFULL + bi], (i >> 1) & 1, a.st, abort_p, 27)) break;
       if (h == 0) progress(a.st, prog, 3);
       float tmax = -INFINITY;
 #pragma unroll
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   if (warp >= 6) {
     // --------------------------------------------- in-cluster merge ----
     const int h = (warp & 3) * 32 + lane;
-    float mq[4], wq[4];
+    float mq[4] = {0.f, 0.f, 0.f, 0.f}, wq[4] = {0.f, 0.f, 0.f, 0.f};
     float M = -INFINITY;
     for (int q = 0; q < G; ++q) {
       const uint32_t rq = 2u * q + half;
@@ -567,20 +567,32 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     if (h < a.H) {
       __nv_bfloat16* out = a.out + ((int64_t)b * a.H + h) * 512 + half * 256;
       const uint32_t orow = base + kOffO + h * 1024;
+      uint32_t rbase[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rbase[q] = mapa(orow, 2u * (q < G ? q : 0) + half);
       for (int c4 = c4_0; c4 < c4_0 + cols / 4; c4 += 2) {
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int q = 0; q < G; ++q) {
-          if (mq[q] == 0.f) continue;
-          const uint32_t rq = 2u * q + half;
+        // issue every partial's loads first, then accumulate
+        float4 v[4][2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int cc = c4 + u;
-            const uint32_t addr = orow + (((cc & ~7) | ((cc & 7) ^ (h & 7))) << 4);
-            const float4 v = ld_cluster_v4(mapa(addr, rq));
-            acc[4 * u] += mq[q] * v.x;
-            acc[4 * u + 1] += mq[q] * v.y;
-            acc[4 * u + 2] += mq[q] * v.z;
-            acc[4 * u + 3] += mq[q] * v.w;
+            v[q][u] = (q < G && mq[q] != 0.f)
+                          ? ld_cluster_v4(rbase[q] + (((cc & ~7) | ((cc & 7) ^ (h & 7))) << 4))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float f = q < G ? mq[q] : 0.f;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            acc[4 * u] += f * v[q][u].x;
+            acc[4 * u + 1] += f * v[q][u].y;
+            acc[4 * u + 2] += f * v[q][u].z;
+            acc[4 * u + 3] += f * v[q][u].w;
           }
         }
         uint4 o;

@@ -88,6 +88,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded polling wait (non-suspending test_wait) for barriers whose
+// arrivals come from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, DevStatus* st,
+                                               volatile int* abort, int where) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer();
+  const long long c0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test_wait(a, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      if (it >= 16u * kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
+          globaltimer() - t0 > kWaitLimitNs) {
+        report(st, CKV_ERR_TIMEOUT, where);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait for the phase with parity `parity` to complete.  On expiry
 // it records CKV_ERR_TIMEOUT (detail = `where`), raises *abort and returns
 // false; once *abort is set every later wait returns false at once.

@@ -61,21 +61,28 @@ __device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk
 }
 
 // Merge of all chunks' candidates (run by the last CTA of sequence b).
-// surv_key / surv_ent: `surv_cap`-entry shared-memory scratch.
+// surv_key / surv_ent: `surv_cap`-entry shared-memory scratch (>= kHistBins
+// words for surv_key).  Every global read is a coalesced 16-byte load.
 template <int NT>
 __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* surv_key,
                                int32_t* surv_ent, int surv_cap) {
-  const int n_slots = a.n_chunks * a.K_sel;
+  const int n_slots = a.n_chunks * a.K_sel;   // K_sel is a multiple of 4
   const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
   const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
   uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
   const int K = a.pool_out > 0 ? a.pool_out : a.topk;
 
-  // (a) threshold bin: descending bins, contiguous per thread
-  constexpr int per = (kHistBins + NT - 1) / NT;
+  // (a) the histogram into shared memory (and zeroed for the next call)
+  uint32_t* hs = surv_key;
+  for (int v = threadIdx.x; v < kHistBins / 4; v += NT) {
+    reinterpret_cast<uint4*>(hs)[v] = __ldcg(reinterpret_cast<const uint4*>(hist) + v);
+    reinterpret_cast<uint4*>(hist)[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  constexpr int per = (kHistBins + NT - 1) / NT;   // descending bins, contiguous per thread
   const int p0 = min(kHistBins, (int)threadIdx.x * per), p1 = min(kHistBins, p0 + per);
   uint32_t cnt = 0;
-  for (int p = p0; p < p1; ++p) cnt += __ldcg(hist + (kHistBins - 1 - p));
+  for (int p = p0; p < p1; ++p) cnt += hs[kHistBins - 1 - p];
   uint32_t before, dummy, total, dummy2;
   block_scan2<NT>(cnt, 0u, before, dummy, total, dummy2, sm.sel);
   const int n_real = (int)total;
@@ -85,7 +92,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   if (keff > 0 && before < keff && before + cnt >= keff) {
     uint32_t cum = before;
     for (int p = p0; p < p1; ++p) {
-      const uint32_t c = __ldcg(hist + (kHistBins - 1 - p));
+      const uint32_t c = hs[kHistBins - 1 - p];
       if (cum + c >= keff) {
         sm.bcast[0] = (uint32_t)(kHistBins - 1 - p);
         break;
@@ -95,32 +102,51 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   }
   __syncthreads();
   const uint32_t tb = sm.bcast[0];
-  for (int i = threadIdx.x; i < kHistBins; i += NT) hist[i] = 0u;   // ready for the next call
+  __syncthreads();   // hs is reused below
 
-  // (b) order-preserving compaction of the survivors (key bin >= tb)
-  const int per2 = (n_slots + NT - 1) / NT;
-  const int i0 = min(n_slots, (int)threadIdx.x * per2), i1 = min(n_slots, i0 + per2);
-  uint32_t mine = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t u = __ldcg(ck + i);
-    mine += (u != 0u) && ((u >> kHistShift) >= tb);
-  }
-  uint32_t pos, d3, n_surv, d4;
-  block_scan2<NT>(mine, 0u, pos, d3, n_surv, d4, sm.sel);
-  if (n_surv <= (uint32_t)surv_cap) {
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t u = __ldcg(ck + i);
-      if ((u != 0u) && ((u >> kHistShift) >= tb)) {
-        surv_key[pos] = u;
-        surv_ent[pos] = __ldcg(ci + i);
-        ++pos;
+  // (b) survivors (key bin >= tb) in slot order, 16 slots per thread per pass
+  constexpr int kPer = 16;
+  uint32_t n_surv = 0;
+  for (int base = 0; base < n_slots; base += kPer * NT) {
+    const int s0 = base + kPer * (int)threadIdx.x;
+    uint32_t kk[kPer];
+    int32_t ii[kPer];
+#pragma unroll
+    for (int v = 0; v < kPer / 4; ++v) {
+      const int sv = s0 + 4 * v;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      int4 e = make_int4(-1, -1, -1, -1);
+      if (sv < n_slots) {
+        u = __ldcg(reinterpret_cast<const uint4*>(ck + sv));
+        e = __ldcg(reinterpret_cast<const int4*>(ci + sv));
       }
+      kk[4 * v] = u.x; kk[4 * v + 1] = u.y; kk[4 * v + 2] = u.z; kk[4 * v + 3] = u.w;
+      ii[4 * v] = e.x; ii[4 * v + 1] = e.y; ii[4 * v + 2] = e.z; ii[4 * v + 3] = e.w;
     }
-    __syncthreads();
+    uint32_t f = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) f |= (uint32_t)((kk[e] != 0u) && ((kk[e] >> kHistShift) >= tb)) << e;
+    uint32_t pos, d0, tot, d1;
+    block_scan2<NT>((uint32_t)__popc(f), 0u, pos, d0, tot, d1, sm.sel);
+    if (n_surv + tot <= (uint32_t)surv_cap) {
+      pos += n_surv;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e)
+        if ((f >> e) & 1u) {
+          surv_key[pos] = kk[e];
+          surv_ent[pos] = ii[e];
+          ++pos;
+        }
+    }
+    n_surv += tot;
+  }
+  __syncthreads();
+  if (n_surv <= (uint32_t)surv_cap) {
     emit_outputs<NT>(
         a, b, (int)n_surv, n_real, [&](int i) { return surv_key[i]; },
         [&](int i) { return surv_ent[i]; }, sm);
   } else {
+    // a crowded threshold bin: select on the full lists in global memory
     emit_outputs<NT>(
         a, b, n_slots, n_real, [&](int i) { return __ldcg(ck + i); },
         [&](int i) { return __ldcg(ci + i); }, sm);
