@@ -54,6 +54,9 @@ lib.ckv_hca_attn.argtypes = [_P, _vp, _i32, _P, _vp, _i32, _vp, _i32, _f32, _vp,
 lib.ckv_csa2_group_decode.restype = _i32
 lib.ckv_csa2_group_decode.argtypes = [ctypes.POINTER(CGroup), _vp, _i32, _vp, _i32, _i32, _i32,
                                       _i32, _f32, _P, _vp, _vp, _i32, _vp, _sz, _vp]
+lib.ckv_csa_index_topk_static.restype = _i32
+lib.ckv_csa_index_topk_static.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp,
+                                          _vp, _i32, _vp, _vp]
 lib.ckv_read_device_status.restype = _i32
 lib.ckv_read_device_status.argtypes = [_vp, _vp]
 lib.ckv_status_string.restype = ctypes.c_char_p
@@ -147,6 +150,25 @@ def csa_index_topk(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, p
                                   HI, topk, _ptr(pool), pool_len, _ptr(out_idx), _ptr(out_pool),
                                   pool_out if out_pool is not None else 0, _ptr(dbg_scores),
                                   _ptr(ws), ws.numel(), _stream(stream)), "csa_index_topk")
+    return (out_idx, out_pool) if out_pool is not None else out_idx
+
+
+def csa_index_topk_static(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, pool_out=0,
+                          out_idx=None, out_pool=None, dbg_scores=None, stream=None):
+    """csa_index_topk with the library's static device scratch instead of a
+    caller workspace (for callers that cannot allocate; see include/ckv.h)."""
+    B, HI = q_idx.shape[0], q_idx.shape[1]
+    dev = q_idx.device
+    if out_idx is None:
+        out_idx = torch.empty((B, topk), dtype=torch.int32, device=dev)
+    if pool_out and out_pool is None:
+        out_pool = torch.empty((B, pool_out), dtype=torch.int32, device=dev)
+    pool_len = 0 if pool is None else pool.shape[1]
+    c = keys.c()
+    _check(lib.ckv_csa_index_topk_static(ctypes.byref(c), _ptr(n_comp), B, n_comp_max, _ptr(q_idx),
+                                         _ptr(w), HI, topk, _ptr(pool), pool_len, _ptr(out_idx),
+                                         _ptr(out_pool), pool_out if out_pool is not None else 0,
+                                         _ptr(dbg_scores), _stream(stream)), "csa_index_topk_static")
     return (out_idx, out_pool) if out_pool is not None else out_idx
 
 

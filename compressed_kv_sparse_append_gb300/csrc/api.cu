@@ -428,3 +428,44 @@ const char* ckv_status_string(ckv_status s) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Static-scratch variant of csa_index_topk (no allocation by anyone).  The
+// scratch is this file's device array; host code finds its device address
+// with cudaGetSymbolAddress once per device (the array's name is only a
+// host-side stand-in) and passes that address to the same kernels.
+static __device__ __align__(256) uint8_t g_index_scratch[CKV_STATIC_SCRATCH_BYTES];
+static constexpr int kMaxDevices = 64;
+static void* g_index_scratch_dev[kMaxDevices] = {};
+
+extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const int32_t* n_comp,
+                                                int32_t B, int32_t n_comp_max,
+                                                const void* q_idx_bf16, const float* w,
+                                                int32_t HI, int32_t topk, const int32_t* pool,
+                                                int32_t pool_len, int32_t* out_idx,
+                                                int32_t* out_pool, int32_t pool_out,
+                                                float* dbg_scores, void* stream) {
+  ckv_status s = check_index_args(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool,
+                                  pool_len, out_idx, out_pool, pool_out);
+  if (s) return s;
+  const bool pool_mode = pool != nullptr;
+  const int K_sel = out_pool ? pool_out : topk;
+  const IndexLayout L = index_layout(B, n_comp_max, K_sel, pool_mode, pool_mode ? pool_len : 0);
+  if (kStatusBytes + L.bytes > (size_t)CKV_STATIC_SCRATCH_BYTES) return CKV_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CKV_ERR_CUDA;
+  if (g_index_scratch_dev[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr)
+      return cuda_status(cudaErrorUnknown);
+    g_index_scratch_dev[dev] = p;
+  }
+  uint8_t* w8 = static_cast<uint8_t*>(g_index_scratch_dev[dev]);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // status, per-sequence tickets and key histograms must start at zero
+  s = cuda_status(cudaMemsetAsync(w8, 0, kStatusBytes + L.key_off, st));
+  if (s) return s;
+  return run_index(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool, pool_len,
+                   out_idx, out_pool, pool_out, dbg_scores, reinterpret_cast<DevStatus*>(w8),
+                   w8 + kStatusBytes, st);
+}

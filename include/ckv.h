@@ -144,6 +144,33 @@ ckv_status ckv_csa_index_topk(const ckv_plane *idx_keys, const int32_t *n_comp,
                               float *dbg_scores, void *ws, size_t ws_bytes,
                               void *stream);
 
+/* csa_index_topk for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment convenience.  Some callers cannot
+ * call cudaMalloc at all -- code running inside a CUDA graph being captured,
+ * plug-ins of serving engines that own every allocation, or embedded
+ * runtimes with a fixed memory plan -- and so cannot provide the workspace
+ * of ckv_csa_index_topk.  This entry point computes exactly the same outputs
+ * with its scratch in a statically sized device array inside libckv
+ * (CKV_STATIC_SCRATCH_BYTES, held on every GPU that loads the library until
+ * the process exits); it allocates nothing.
+ *   Arguments as ckv_csa_index_topk, without ws / ws_bytes.
+ *   Returns CKV_ERR_WORKSPACE when the call needs more scratch than
+ *   CKV_STATIC_SCRATCH_BYTES (see ckv_workspace_bytes(CKV_OP_INDEX_TOPK, ...)).
+ *   The first call on a device looks the array up (cudaGetSymbolAddress)
+ *   with that device current: make that first call before any stream
+ *   capture.  Every call clears the scratch's counters on `stream` first.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or graphs replayed concurrently) race and must be serialised by
+ *   the caller.  Device-side range errors are recorded in the array's status
+ *   word, which this entry point does not report. */
+#define CKV_STATIC_SCRATCH_BYTES (8u << 20)
+ckv_status ckv_csa_index_topk_static(const ckv_plane *idx_keys, const int32_t *n_comp,
+                                     int32_t B, int32_t n_comp_max,
+                                     const void *q_idx_bf16, const float *w, int32_t HI,
+                                     int32_t topk, const int32_t *pool, int32_t pool_len,
+                                     int32_t *out_idx, int32_t *out_pool, int32_t pool_out,
+                                     float *dbg_scores, void *stream);
+
 /* CSA sparse attention ([KVC] §十一 flow chart: attention over the selected
  * entries followed by the sliding window; §五: each entry is both key and
  * value).  One softmax over the union of the selected rows and the valid
