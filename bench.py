@@ -188,7 +188,8 @@ def make_step(wl, dev, ckv, wlmod):
         idx = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
         out = torch.empty_like(q)
         lse = torch.empty((B, wl.H), device=dev)
-        ws = ckv.new_workspace(ckv.workspace_bytes(ckv.OP_INDEX_TOPK, B, wl.H, wl.HI, n, wl.topk, 0), dev)
+        ws = ckv.new_workspace(max(ckv.workspace_bytes(ckv.OP_INDEX_TOPK, B, wl.H, wl.HI, n, wl.topk, 0),
+                                   ckv.workspace_bytes(ckv.OP_SPARSE_ATTN, B)), dev)
         ent = {"bf16": 256, "fp4": 72}[wl.idx_fmt]
         main_row = {"bf16": 1024, "mixed": 580, "fp4": 288}[wl.main_fmt]
         dom_bytes = B * n * ent + qi.numel() * 2 + w.numel() * 4 + idx.numel() * 4
@@ -210,7 +211,7 @@ def make_step(wl, dev, ckv, wlmod):
         cap = n + 8
         kv = ckv.Plane("bf16", 512, B, cap, dev)
         win = ckv.Plane("bf16", 512, B, wl.W, dev)
-        ws = ckv.new_workspace(256, dev)
+        ws = ckv.new_workspace(ckv.workspace_bytes(ckv.OP_HCA_ATTN, B), dev)
         for b in range(B):
             kvr, _, wr = wlmod.sequence_rows(wl, b, n, dev)
             ckv.kv_append_quant(kv, kvr, torch.arange(n, dtype=torch.int64, device=dev) + b * cap, ws=ws)

@@ -134,6 +134,8 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.out_pool = out_pool;
   a.dbg = dbg;
   a.st = st;
+  const char* pe = getenv("CKV_DEBUG_PROGRESS");
+  a.trace = (pe && pe[0] == '2') ? 1 : 0;
   const int64_t rows = (int64_t)keys->batch * keys->cap;
   if (use_umma_indexer() && index_umma_supported(a, rows))
     return cuda_status(launch_index_umma(a, rows, stream));
@@ -165,18 +167,29 @@ size_t index_ws_bytes(int B, int n_comp_max, int K_sel, bool pool_mode, int pool
   return index_layout(B, n_comp_max, K_sel, pool_mode, pool_len).bytes;
 }
 
-// Picks the number of CTA pairs per sequence (cluster of 2G CTAs).
-int choose_pairs(int B, int n_rows_max) {
+// Partials of the attention's in-cluster merge: up to 8 CTAs (4 pairs) per
+// sequence and layer, kPartFloats floats each.
+size_t attn_part_bytes(int B, int layers) {
+  return align_up((size_t)layers * B * 8 * kPartFloats * sizeof(float), 256);
+}
+
+// Picks the number of CTA pairs per sequence (cluster of 2G CTAs): the
+// largest G that leaves each pair at least two 64-row tiles and lets all
+// `n_clusters` clusters be resident at once (one wave).
+int choose_pairs(int n_clusters, int n_rows_max) {
   const int tiles = (n_rows_max + 63) / 64;
-  int G = 4;
-  while (G > 1 && tiles < G * 2) G >>= 1;
-  (void)B;
-  return G;
+  for (int G = 4; G > 1; G >>= 1) {
+    if (tiles < G * 2) continue;
+    const int fit = attn_max_active_clusters(2 * G);
+    if (fit <= 0 || n_clusters <= fit) return G;
+  }
+  return 1;
 }
 
 ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
-                             int B, const void* q, int H, void* out) {
+                             int B, const void* q, int H, void* out, float sm_scale) {
   if (B <= 0 || !win_len || !q || !out || !aligned16(q) || !aligned16(out)) return CKV_ERR_INVALID;
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return CKV_ERR_INVALID;
   if (H <= 0 || H > kMaxHeads) return CKV_ERR_UNSUPPORTED;
   ckv_status s = check_plane(kv, 512, B);
   if (s) return s;
@@ -209,10 +222,11 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.G = 1;
+  a.part = nullptr;
   a.st = st;
   a.use_tma = 0;
   const char* pe = getenv("CKV_DEBUG_PROGRESS");
-  a.progress = (pe && pe[0] == '1') ? 1 : 0;
+  a.progress = (pe && (pe[0] == '1' || pe[0] == '2')) ? pe[0] - '0' : 0;
   return a;
 }
 
@@ -237,8 +251,11 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t
       size_t idx_region = align_up(full > re ? full : re, 256);
       size_t pool = align_up((size_t)B * (pool_len > 0 ? pool_len : 1) * 4, 256);
       size_t idxbuf = align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256);
-      return kStatusBytes + idx_region + pool + idxbuf;
+      return kStatusBytes + idx_region + pool + idxbuf + attn_part_bytes(B, CKV_CSA2_MAX_LAYERS);
     }
+    case CKV_OP_SPARSE_ATTN:
+    case CKV_OP_HCA_ATTN:
+      return kStatusBytes + attn_part_bytes(B, 1);
     default:
       return kStatusBytes;
   }
@@ -281,14 +298,15 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
                                const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
                                int32_t H, float sm_scale, void* out_bf16, float* lse, void* ws,
                                size_t ws_bytes, void* stream) {
-  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16);
+  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!idx || topk <= 0) return CKV_ERR_INVALID;
   if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
-  s = check_ws(ws, ws_bytes, kStatusBytes);
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_part_bytes(B, 1));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   a.idx = idx;
   a.topk = topk;
   a.G = choose_pairs(B, topk + (int)win->cap);
@@ -299,13 +317,14 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
                         const ckv_plane* win, const int32_t* win_len, int32_t B,
                         const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
                         float* lse, void* ws, size_t ws_bytes, void* stream) {
-  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16);
+  ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!n_comp || n_comp_max < 0 || n_comp_max > kv->cap) return CKV_ERR_INVALID;
-  s = check_ws(ws, ws_bytes, kStatusBytes);
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_part_bytes(B, 1));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
+  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
   a.n_comp = n_comp;
   a.n_comp_max = n_comp_max;
   a.G = choose_pairs(B, n_comp_max + (int)win->cap);
@@ -338,7 +357,7 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
     }
     any_reindex |= r == CKV_CSA2_REINDEX;
     const int k = g->kv_src[l];
-    ckv_status s = check_attn_common(&g->kv[k], &g->win[k], win_len, B, g->q[l], H, g->out[l]);
+    ckv_status s = check_attn_common(&g->kv[k], &g->win[k], win_len, B, g->q[l], H, g->out[l], sm_scale);
     if (s) return s;
     if (n_comp_max > g->kv[k].cap) return CKV_ERR_INVALID;
   }
@@ -362,6 +381,9 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   uint8_t* idx_region = w8 + kStatusBytes;
   int32_t* pool_buf = reinterpret_cast<int32_t*>(idx_region + align_up(full > re ? full : re, 256));
   int32_t* idxbuf = pool_buf + align_up((size_t)B * pool_len * 4, 256) / 4;
+  float* part = reinterpret_cast<float*>(
+      reinterpret_cast<uint8_t*>(idxbuf) +
+      align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256));
 
   if (n_append > 0) {
     s = cuda_status(launch_append(*append_dst, append_src_bf16, append_slot, n_append, dst, st));
@@ -389,14 +411,17 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   // every layer's attention in one launch (grid z = layer)
   AttnArgs la[CKV_CSA2_MAX_LAYERS];
   int G = 4;
-  for (int l = 0; l < L; ++l) G = G < choose_pairs(B, topk + (int)g->win[g->kv_src[l]].cap)
-                                      ? G : choose_pairs(B, topk + (int)g->win[g->kv_src[l]].cap);
+  for (int l = 0; l < L; ++l) {
+    const int gl = choose_pairs(B * L, topk + (int)g->win[g->kv_src[l]].cap);
+    G = G < gl ? G : gl;
+  }
   for (int l = 0; l < L; ++l) {
     const int k = g->kv_src[l];
     la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
     la[l].idx = layer_idx[l];
     la[l].topk = topk;
     la[l].G = G;
+    la[l].part = part;   // one region for all layers, indexed by layer inside
   }
   return cuda_status(launch_attention_layers(la, L, B, st));
 }

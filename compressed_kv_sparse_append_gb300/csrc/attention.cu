@@ -39,20 +39,20 @@ namespace ckv {
 namespace {
 
 constexpr int kTile = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kThreadsAttn = 320;
 constexpr uint32_t kEBytes = kTile * 256 * 2;         // 32 KB
-constexpr uint32_t kXBytes = 128 * kTile * 4;         // 32 KB
+constexpr uint32_t kXBytes = 128 * kTile * 2;         // 16 KB: fp16 partial scores
 constexpr uint32_t kOffE = 0;
 constexpr uint32_t kOffX = kOffE + kStages * kEBytes;
-constexpr uint32_t kOffO = 0;                         // final O staging reuses E
-constexpr uint32_t kOffML = kOffX + 2 * kXBytes;
-constexpr uint32_t kOffBar = kOffML + 128 * 8;
+constexpr int kXBufs = 4;                              // send-ahead needs four
+constexpr uint32_t kOffRowSrc = kOffX + kXBufs * kXBytes;    // int32 [kStages][64]
+constexpr uint32_t kOffVmask = kOffRowSrc + kStages * 64 * 4;  // u32 [kStages][2]
+constexpr uint32_t kOffBar = kOffVmask + kStages * 8;
 constexpr uint32_t kNumBars = 4 * kStages + 10;
 constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffSlot + 16;
 constexpr uint32_t kSmemAttn = kSmemUsed + 1024;
-static_assert(128 * 256 * 4 <= kOffX, "O staging fits in the E ring");
 static_assert(kSmemAttn <= 232448, "fits the 227 KB opt-in limit");
 
 constexpr uint32_t kTmemCols = 512;
@@ -64,7 +64,7 @@ constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (factor 256)
 // barrier indices
 constexpr int B_TMA = 0, B_EFULL = kStages, B_EEMPTY = 2 * kStages;
 constexpr int B_SFULL = 3 * kStages, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-              B_XFULL = B_ODONE + 1, B_CLUSTER = B_XFULL + 2;
+              B_XFULL = B_ODONE + 1, B_CLUSTER = B_XFULL + kXBufs, B_XREAD = B_CLUSTER + 2;
 
 // Cluster-wide barrier `k` built on mbarriers with a bounded wait: thread 0
 // of every CTA arrives (release, cluster scope) on barrier k of every CTA of
@@ -148,70 +148,80 @@ __device__ __forceinline__ Tile tile_of(int t, int nt_main, int n_sel, int n_win
   return r;
 }
 
-struct RowSrc {
-  const uint8_t* data;
-  const void* scale;
-  int64_t entry;  // global slot (b * cap + pos), or -1 when the row is empty
+// Raw bytes of one 16-byte source chunk of a row plus its scale bits.
+struct Raw {
+  uint4 v;
+  uint32_t s;   // MIXED: f32 scale bits; FP4: two E4M3 scale bytes
 };
 
-// Dequantise local latent chunk `q` of row `src` (half `half`) into the bf16
-// tile `tile` at row `r`.  Writes zeros for an empty row.
-__device__ __forceinline__ void fill_chunk(const AttnArgs& a, uint32_t tile, int r, int q,
-                                           const RowSrc& src, int half) {
-  const bool empty = src.entry < 0;
+// Load local latent chunk `q` of cache entry `entry` (-1: empty row).
+__device__ __forceinline__ Raw load_chunk(const AttnArgs& a, int q, int64_t entry, bool win,
+                                          int half) {
+  Raw r;
+  r.v = make_uint4(0u, 0u, 0u, 0u);
+  r.s = 0u;
+  if (entry < 0) return r;
+  const uint8_t* data = win ? a.win_data : a.kv_data;
+  const void* scale = win ? a.win_scale : a.kv_scale;
   if (a.fmt == CKV_FMT_BF16) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (!empty) v = *reinterpret_cast<const uint4*>(src.data + src.entry * 1024 + half * 512 + q * 16);
-    const int d0 = q * 8;
-    st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), v);
+    r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 1024 + half * 512 + q * 16));
   } else if (a.fmt == CKV_FMT_MIXED) {
     const int n_fp8 = half == 0 ? 16 : 12;
     if (q < n_fp8) {
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (!empty) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(src.data + src.entry * 576 + half * 256 + q * 16);
-        const int nblk = 448 / a.nope_block;
-        const float s = reinterpret_cast<const float*>(src.scale)[src.entry * nblk + (half * 256 + q * 16) / a.nope_block];
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3);
-          __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-          float2 f0 = __half22float2(__half2(h0)), f1 = __half22float2(__half2(h1));
-          o[2 * i] = pack_bf16(f0.x * s, f0.y * s);
-          o[2 * i + 1] = pack_bf16(f1.x * s, f1.y * s);
-        }
-        v0 = make_uint4(o[0], o[1], o[2], o[3]);
-        v1 = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-      const int d0 = q * 16;
-      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), v0);
-      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, ((d0 & 63) >> 3) + 1), v1);
-    } else {  // rope dims 448..511 (half 1 only), bf16
-      const int k = q - 12;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (!empty) v = *reinterpret_cast<const uint4*>(src.data + src.entry * 576 + 448 + k * 16);
-      const int d0 = 192 + k * 8;
-      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), v);
+      r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 576 + half * 256 + q * 16));
+      const int nblk = 448 / a.nope_block;
+      r.s = __ldg(reinterpret_cast<const uint32_t*>(scale) + entry * nblk +
+                  (half * 256 + q * 16) / a.nope_block);
+    } else {
+      r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 576 + 448 + (q - 12) * 16));
     }
-  } else {  // CKV_FMT_FP4: 8 chunks of 32 channels
-    uint32_t o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0;
-    if (!empty) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(src.data + src.entry * 256 + half * 128 + q * 16);
-      const uint8_t* sp = reinterpret_cast<const uint8_t*>(src.scale) + src.entry * 32 + half * 16 + q * 2;
-      const float s0 = e4m3_value(sp[0]), s1 = e4m3_value(sp[1]);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  } else {
+    r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 256 + half * 128 + q * 16));
+    r.s = __ldg(reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(scale) +
+                                                  entry * 32 + half * 16 + q * 2));
+  }
+  return r;
+}
+
+// Dequantise a loaded chunk to bf16 and store it at row `r` of the swizzled
+// tile (an empty row stores zeros: its raw bytes and scale are zero).
+__device__ __forceinline__ void store_chunk(const AttnArgs& a, uint32_t tile, int r, int q,
+                                            const Raw& raw, int half) {
+  if (a.fmt == CKV_FMT_BF16) {
+    const int d0 = q * 8;
+    st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), raw.v);
+  } else if (a.fmt == CKV_FMT_MIXED) {
+    const int n_fp8 = half == 0 ? 16 : 12;
+    if (q < n_fp8) {
+      const float s = __uint_as_float(raw.s);
+      const uint32_t w[4] = {raw.v.x, raw.v.y, raw.v.z, raw.v.w};
+      uint32_t o[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float s = i < 2 ? s0 : s1;
+        __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3);
+        __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+        float2 f0 = __half22float2(__half2(h0)), f1 = __half22float2(__half2(h1));
+        o[2 * i] = pack_bf16(f0.x * s, f0.y * s);
+        o[2 * i + 1] = pack_bf16(f1.x * s, f1.y * s);
+      }
+      const int d0 = q * 16;
+      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), make_uint4(o[0], o[1], o[2], o[3]));
+      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, ((d0 & 63) >> 3) + 1), make_uint4(o[4], o[5], o[6], o[7]));
+    } else {  // rope dims 448..511 (half 1 only), bf16
+      const int d0 = 192 + (q - 12) * 8;
+      st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), raw.v);
+    }
+  } else {  // FP4: 32 channels
+    const float s0 = e4m3_value((uint8_t)(raw.s & 0xFF)), s1 = e4m3_value((uint8_t)(raw.s >> 8));
+    const uint32_t w[4] = {raw.v.x, raw.v.y, raw.v.z, raw.v.w};
+    uint32_t o[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t byte = (w[i] >> (8 * k)) & 0xFF;
-          o[4 * i + k] = pack_bf16(e2m1_value(byte & 0xF) * s, e2m1_value(byte >> 4) * s);
-        }
+    for (int i = 0; i < 4; ++i) {
+      const float sc = i < 2 ? s0 : s1;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t byte = (w[i] >> (8 * k)) & 0xFF;
+        o[4 * i + k] = pack_bf16(e2m1_value(byte & 0xF) * sc, e2m1_value(byte >> 4) * sc);
       }
     }
     const int d0 = q * 32;
@@ -228,6 +238,12 @@ __device__ __forceinline__ int chunks_per_row(int fmt, int half) {
 
 }  // namespace
 
+// Debug timeline (progress mode 2): CTA (0, 0, 0) stores clock64 offsets of
+// its pipeline hand-offs in the status block's spare words.
+__device__ __forceinline__ void trace(DevStatus* st, bool on, int slot, long long t0) {
+  if (on && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
+}
+
 __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
                 const __grid_constant__ AttnBatch batch) {
@@ -238,7 +254,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   uint8_t* gbase = smem_raw + (base - raw_base);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbase + kOffSlot);
-  float2* ml = reinterpret_cast<float2*>(gbase + kOffML);
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -267,8 +282,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     for (int k = 0; k < 2; ++k) {
       mbar_init(&bars[B_SFULL + k], 1);
       mbar_init(&bars[B_PFULL + k], 128);
-      mbar_init(&bars[B_XFULL + k], 128);
     }
+    for (int k = 0; k < kXBufs; ++k) mbar_init(&bars[B_XFULL + k], 128);
+    mbar_init(&bars[B_XREAD], 128);
+    mbar_init(&bars[B_XREAD + 1], 128);
     mbar_init(&bars[B_ODONE], 1);
     mbar_init(&bars[B_CLUSTER], 2 * G);
     mbar_init(&bars[B_CLUSTER + 1], 2 * G);
@@ -280,8 +297,35 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   volatile int* abort_p = &abort_flag;
-  const bool prog = a.progress != 0;
+  const bool prog = a.progress == 1;
+  const bool tr = a.progress == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  const long long tr0 = clock64();
   if (tid == 0) progress(a.st, prog, 0);
+
+  // Rounds this CTA's partial scores S(k) of head row `hq` (TMEM lane
+  // quadrant of the calling warp) to fp16 and stores them into the peer's
+  // exchange buffer k % kXBufs; the caller arrives on the peer's barrier.
+  auto send_scores = [&](int k, int hq) {
+    const uint32_t tS = tmem + kColS + 64 * (k & 1) + ((uint32_t)(hq & ~31) << 16);
+    const uint32_t xrow_peer = mapa(base + kOffX + (k % kXBufs) * kXBytes + hq * 128, peer);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t sr[32];
+      tmem_ld32(tS + 32 * hh, sr);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 4 * hh; c < 4 * hh + 4; ++c) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = 8 * (c - 4 * hh) + 2 * u;
+          __half2 hv = __floats2half2_rn(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
+          w4[u] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        st_cluster_u4(xrow_peer + ((c ^ (hq & 7)) << 4), make_uint4(w4[0], w4[1], w4[2], w4[3]));
+      }
+    }
+  };
 
   if (warp >= 6) {
     // Q[b, h, half] -> TMEM as the bf16 A operand (lane h, two elements per column)
@@ -311,6 +355,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) trace(a.st, tr, 0, tr0);
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA issuer ----
@@ -336,48 +381,96 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     // ------------------------------------------- producers / TMA fix-up ----
     const int p = tid - 32;
     const int J = chunks_per_row(a.fmt, half);
-    for (int i = 0; i < n_my; ++i) {
+    if (use_tma) {
+      // TMA-fed tiles: these warps release each landed tile to the MMA
+      // (zeroing rows past the end of its segment, so that P = 0 meets finite
+      // values in P.E) and run the score exchange, so that the DSMEM transfer
+      // of S(i) overlaps the softmax of tile i - 1.  A tile is released two
+      // tiles ahead of the exchange, which waits on the MMA.
+      const int hq = ((warp & 3) * 32) + lane;
+      int next_fix = 0;
+      bool ok = true;
+      for (int i = 0; i < n_my && ok; ++i) {
+        for (; next_fix < n_my && next_fix <= i + 2; ++next_fix) {
+          const int j = next_fix, s = j % kStages;
+          const uint32_t tile = base + kOffE + s * kEBytes;
+          const Tile tl = tile_of(t0 + j, nt_main, n_sel, n_win);
+          if (!mbar_wait(&bars[B_TMA + s], (j / kStages) & 1, a.st, abort_p, 22)) {
+            ok = false;
+            break;
+          }
+          if (p == 0 && j < 8) trace(a.st, tr, 49 + j, tr0);
+          for (int e = p; e < (kTile - tl.valid) * 32; e += 128) {
+            const int r = tl.valid + (e >> 5), cc = e & 31;
+            st_shared_v4(sw128(tile + (cc >> 3) * 8192, r, cc & 7), make_uint4(0, 0, 0, 0));
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars[B_EFULL + s]);
+          if (p == 0) progress(a.st, prog, 5);
+        }
+        if (!ok || !mbar_wait(&bars[B_SFULL + (i & 1)], (i >> 1) & 1, a.st, abort_p, 33)) break;
+        tc_fence_after();
+        send_scores(i, hq);
+        tc_fence_before();
+        mbar_arrive(&bars[B_XREAD + (i & 1)]);   // S(i) may now be overwritten by P(i)
+        mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + i % kXBufs]), peer));
+      }
+    }
+    for (int i = 0; i < n_my && !use_tma; ++i) {
       const int s = i % kStages;
       const uint32_t tile = base + kOffE + s * kEBytes;
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-      if (use_tma) {
-        if (!mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, a.st, abort_p, 22)) break;
-        if (tl.valid < kTile) {
-          // rows past the end of the segment: zero them so that P = 0 meets
-          // finite values in P.E
-          for (int j = p; j < (kTile - tl.valid) * 32; j += 128) {
-            const int r = tl.valid + (j >> 5), cc = j & 31;
-            st_shared_v4(sw128(tile + (cc >> 3) * 8192, r, cc & 7), make_uint4(0, 0, 0, 0));
-          }
-        }
-      } else {
+      {
         if (i >= kStages &&
             !mbar_wait(&bars[B_EEMPTY + s], ((i / kStages) + 1) & 1, a.st, abort_p, 23))
           break;
-        for (int j = p; j < kTile * J; j += 128) {
-          const int r = j / J, q = j - r * J;
-          RowSrc src;
-          src.entry = -1;
-          if (r < tl.valid) {
-            const int row = tl.start + r;
+        // row of the tile's plane within sequence b (one thread per row; -1
+        // for an invalid row), validity mask
+        int32_t* rsrc = reinterpret_cast<int32_t*>(gbase + kOffRowSrc) + s * 64;
+        if (p < 64) {
+          int32_t e = -1;
+          if (p < tl.valid) {
+            const int row = tl.start + p;
             if (!tl.win) {
-              int64_t e = idx_b ? (int64_t)__ldg(idx_b + row) : row;
-              if (e >= a.kv_cap) {
-                if (q == 0 && half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, (int)e);
-                e = -1;
+              int32_t x = idx_b ? __ldg(idx_b + row) : row;
+              if (x >= a.kv_cap) {
+                if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
+                x = -1;
               }
-              if (e >= 0) {
-                src.data = a.kv_data;
-                src.scale = a.kv_scale;
-                src.entry = (int64_t)b * a.kv_cap + e;
-              }
+              e = x >= 0 ? x : -1;
             } else {
-              src.data = a.win_data;
-              src.scale = a.win_scale;
-              src.entry = (int64_t)b * a.win_cap + row;
+              e = row;
             }
           }
-          fill_chunk(a, tile, r, q, src, half);
+          rsrc[p] = e;
+          const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
+          if ((p & 31) == 0) reinterpret_cast<uint32_t*>(gbase + kOffVmask)[s * 2 + (p >> 5)] = bal;
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
+        // every chunk load of a batch is issued before any conversion
+        constexpr int U = 8;
+        for (int j0 = p; j0 < kTile * J; j0 += 128 * U) {
+          Raw raw[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 128;
+            raw[u].v = make_uint4(0u, 0u, 0u, 0u);
+            raw[u].s = 0u;
+            if (j < kTile * J) {
+              const int r = j / J, q = j - r * J;
+              const int32_t x = rsrc[r];
+              raw[u] = load_chunk(a, q, x >= 0 ? row0 + x : -1, tl.win != 0, half);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 128;
+            if (j < kTile * J) {
+              const int r = j / J, q = j - r * J;
+              store_chunk(a, tile, r, q, raw[u], half);
+            }
+          }
         }
       }
       fence_proxy_async_smem();
@@ -392,6 +485,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const int sj = j % kStages, bj = j & 1;
         if (!mbar_wait(&bars[B_PFULL + bj], (j >> 1) & 1, a.st, abort_p, 24)) return false;
         tc_fence_after();
+        if (j < 8) trace(a.st, tr, 17 + j, tr0);
         const uint32_t tile = base + kOffE + sj * kEBytes;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -409,6 +503,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const uint32_t tile = base + kOffE + s * kEBytes;
         if (!mbar_wait(&bars[B_EFULL + s], (i / kStages) & 1, a.st, abort_p, 25)) break;
         tc_fence_after();
+        if (i < 8) trace(a.st, tr, 1 + i, tr0);
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
           const uint32_t kc = ks >> 2, w = ks & 3;
@@ -417,6 +512,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
         umma_commit(&bars[B_SFULL + bi]);
         progress(a.st, prog, 1);
+        if (i < 8) trace(a.st, tr, 9 + i, tr0);
         if (i > 0) ok = issue_pv(i - 1);
       }
       if (ok && n_my > 0) issue_pv(n_my - 1);
@@ -429,51 +525,71 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t tO = tmem + kColO + lane_base;
     float m_used = -INFINITY, l = 0.f;
-    for (int i = 0; i < n_my; ++i) {
+    // Partial scores of tile i: the exchange warps send S(i) for TMA-fed
+    // tiles; for gathered tiles this thread sends its own row first.
+    bool ok = true;
+    for (int i = 0; i < n_my && ok; ++i) {
       const int bi = i & 1;
       const uint32_t tS = tmem + kColS + 64 * bi + lane_base;
       if (!mbar_wait(&bars[B_SFULL + bi], (i >> 1) & 1, a.st, abort_p, 26)) break;
       tc_fence_after();
       if (h == 0) progress(a.st, prog, 2);
-      uint32_t sr[64];
-      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_wait_ld();
-      // swap the partial scores with the other half of the pair
-      const uint32_t xrow = base + kOffX + bi * kXBytes + h * 256;
-      const uint32_t xrow_peer = mapa(xrow, peer);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_cluster_v4(xrow_peer + ((c ^ (h & 7)) << 4),
-                      make_float4(__uint_as_float(sr[4 * c]), __uint_as_float(sr[4 * c + 1]),
-                                  __uint_as_float(sr[4 * c + 2]), __uint_as_float(sr[4 * c + 3])));
-      mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + bi]), peer));
+      if (h == 0 && i < 8) trace(a.st, tr, 25 + i, tr0);
+      if (!use_tma) {
+        send_scores(i, h);
+        mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + i % kXBufs]), peer));
+      }
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
       // validity of the tile's rows (selected entries may be -1 / out of range)
       uint64_t vmask = tl.valid >= 64 ? ~0ull : ((1ull << tl.valid) - 1ull);
-      if (!tl.win && idx_b) {
-        uint64_t im = 0;
-        for (int j = 0; j < tl.valid; ++j) {
-          const int e = __ldg(idx_b + tl.start + j);
-          im |= (uint64_t)(e >= 0 && e < a.kv_cap) << j;
-        }
-        vmask &= im;
+      if (!use_tma) {
+        // the producers' mask of tile i (their e_full arrive released it)
+        const int s = i % kStages;
+        mbar_wait(&bars[B_EFULL + s], (i / kStages) & 1, a.st, abort_p, 32);
+        const uint32_t* vm = reinterpret_cast<const uint32_t*>(gbase + kOffVmask) + s * 2;
+        vmask = (uint64_t)vm[0] | ((uint64_t)vm[1] << 32);
       }
-      if (!mbar_wait_poll(&bars[B_XFULL + bi], (i >> 1) & 1, a.st, abort_p, 27)) break;
+      const uint32_t xi = i % kXBufs;
+      if (!mbar_wait_poll(&bars[B_XFULL + xi], (i / kXBufs) & 1, a.st, abort_p, 27)) break;
       if (h == 0) progress(a.st, prog, 3);
-      float tmax = -INFINITY;
+      if (h == 0 && i < 8) trace(a.st, tr, 33 + i, tr0);
+      const uint32_t xrow = base + kOffX + xi * kXBytes + h * 128;
+      // Raw scores of row h: s_j = own_j + peer_j (own: S(i) in TMEM, fp32;
+      // peer: its fp16 partial), -inf for an invalid column.  All 64 stay in
+      // registers; z_j = s_j * scale * log2(e) is folded into the exponent.
+      float sv[64];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tS, r0);
+        tmem_ld32(tS + 32, r1);
+        float4 o[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 o = ld_shared_v4f(xrow + ((c ^ (h & 7)) << 4));
-        const float ov[4] = {o.x, o.y, o.z, o.w};
+        for (int c = 0; c < 8; ++c) o[c] = ld_shared_v4f(xrow + ((c ^ (h & 7)) << 4));
+        tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = 4 * c + k;
-          const float z = ((vmask >> j) & 1ull) ? (__uint_as_float(sr[j]) + ov[k]) * a.scale_log2 : -INFINITY;
-          sr[j] = __float_as_uint(z);
-          tmax = fmaxf(tmax, z);
+        for (int c = 0; c < 8; ++c) {
+          const float ow[4] = {o[c].x, o[c].y, o[c].z, o[c].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 8 * c + 2 * u;
+            const uint32_t pwd = __float_as_uint(ow[u]);
+            const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pwd));
+            const uint32_t o0 = j < 32 ? r0[j] : r1[j - 32], o1 = j < 32 ? r0[j + 1] : r1[j - 31];
+            sv[j] = __uint_as_float(o0) + pf.x;
+            sv[j + 1] = __uint_as_float(o1) + pf.y;
+          }
         }
       }
+      if (vmask != ~0ull) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (!((vmask >> j) & 1ull)) sv[j] = -INFINITY;
+      }
+      float mx[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int j = 4; j < 64; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
+      // scale_log2 > 0 (checked on the host), so max z = max s * scale_log2
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
       if (tmax > m_used + kRescaleLog2 || (m_used == -INFINITY && tmax > -INFINITY)) {
         const float m_new = tmax;
         if (i > 0 && m_used != -INFINITY) {
@@ -495,22 +611,33 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
         m_used = m_new;
       }
+      // the exchange warps must have read S(i) before P(i) overwrites it
+      if (use_tma && !mbar_wait(&bars[B_XREAD + bi], (i >> 1) & 1, a.st, abort_p, 34)) break;
+      // P(i) = 2^(z - m) as bf16 pairs over columns 0 .. 31 of this S
+      // buffer; l sums the unrounded p
       uint32_t pk[32];
+      if (m_used == -INFINITY) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float z0 = __uint_as_float(sr[2 * k]), z1 = __uint_as_float(sr[2 * k + 1]);
-        const float p0 = m_used == -INFINITY ? 0.f : fast_exp2(z0 - m_used);
-        const float p1 = m_used == -INFINITY ? 0.f : fast_exp2(z1 - m_used);
-        __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        const float2 pr = __bfloat1622float2(pb);
-        l += pr.x + pr.y;
-        pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+        for (int k = 0; k < 32; ++k) pk[k] = 0u;
+      } else {
+        const float negm = -m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = fast_exp2(fmaf(sv[2 * k], a.scale_log2, negm));
+          const float p1 = fast_exp2(fmaf(sv[2 * k + 1], a.scale_log2, negm));
+          ls[k & 3] += p0 + p1;
+          __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          pk[k] = *reinterpret_cast<uint32_t*>(&pb);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       }
-      tmem_st32(tS, pk);   // P over the first 32 columns of this S buffer
+      tmem_st32(tS, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[B_PFULL + bi]);
       if (h == 0) progress(a.st, prog, 8);
+      if (h == 0 && i < 8) trace(a.st, tr, 41 + i, tr0);
     }
     if (n_my > 0) {
       // s_full of the last tile implies every PV up to n_my - 3 is done, so
@@ -520,10 +647,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       mbar_wait(&bars[B_ODONE], (n_my - 1) & 1, a.st, abort_p, 29);
       tc_fence_after();
     }
-    // stage this CTA's partial accumulator for the in-cluster merge
-    const uint32_t orow = base + kOffO + h * 1024;
+    // this CTA's partial (unnormalised O, m, l) -> workspace, laid out
+    // [16-byte column chunk][head] so that every store and load is coalesced
+    float4* po = reinterpret_cast<float4*>(a.part) +
+                 (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + rank) * (kPartFloats / 4);
+    float4* pw = po + h;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 8; ++c, pw += 8 * 128) {
       uint32_t r[32];
       if (n_my > 0) {
         tmem_ld32(tO + c * 32, r);
@@ -533,32 +663,42 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         for (int k = 0; k < 32; ++k) r[k] = 0u;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c4 = c * 8 + k;
-        st_shared_v4(orow + (((c4 & ~7) | ((c4 & 7) ^ (h & 7))) << 4),
-                     make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]));
-      }
+      for (int k = 0; k < 8; ++k)
+        __stcg(pw + k * 128, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                         __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
     }
-    ml[h] = make_float2(m_used, l);
+    reinterpret_cast<float2*>(po + 64 * 128)[h] = make_float2(m_used, l);
+    __threadfence();
   }
   tc_fence_before();
   if (tid == 0) progress(a.st, prog, 6);
+  if (tid == 0) trace(a.st, tr, 57, tr0);
   cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
+  if (tid == 0) trace(a.st, tr, 58, tr0);
 
   if (warp >= 6) {
-    // --------------------------------------------- in-cluster merge ----
+    // ------------------------------- merge of the G partials of half c ----
     const int h = (warp & 3) * 32 + lane;
+    const float4* pq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      pq[q] = reinterpret_cast<const float4*>(
+          a.part + (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + 2 * (q < G ? q : 0) + half) * kPartFloats);
     float mq[4] = {0.f, 0.f, 0.f, 0.f}, wq[4] = {0.f, 0.f, 0.f, 0.f};
     float M = -INFINITY;
-    for (int q = 0; q < G; ++q) {
-      const uint32_t rq = 2u * q + half;
-      mq[q] = ld_cluster_f32(mapa(smem_u32(&ml[h].x), rq));
-      wq[q] = ld_cluster_f32(mapa(smem_u32(&ml[h].y), rq));
-      M = fmaxf(M, mq[q]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q < G) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq[q] + 64 * 128) + h);
+        mq[q] = v.x;
+        wq[q] = v.y;
+        M = fmaxf(M, v.x);
+      }
     }
     float L = 0.f;
-    for (int q = 0; q < G; ++q) {
-      const float f = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - M);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float f = (q >= G || mq[q] == -INFINITY) ? 0.f : exp2f(mq[q] - M);
       L += wq[q] * f;
       mq[q] = f;
     }
@@ -566,33 +706,22 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     const int cols = 256 / G, c4_0 = pair * cols / 4;
     if (h < a.H) {
       __nv_bfloat16* out = a.out + ((int64_t)b * a.H + h) * 512 + half * 256;
-      const uint32_t orow = base + kOffO + h * 1024;
-      uint32_t rbase[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) rbase[q] = mapa(orow, 2u * (q < G ? q : 0) + half);
       for (int c4 = c4_0; c4 < c4_0 + cols / 4; c4 += 2) {
-        // issue every partial's loads first, then accumulate
         float4 v[4][2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int cc = c4 + u;
-            v[q][u] = (q < G && mq[q] != 0.f)
-                          ? ld_cluster_v4(rbase[q] + (((cc & ~7) | ((cc & 7) ^ (h & 7))) << 4))
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
+          for (int u = 0; u < 2; ++u)
+            v[q][u] = (mq[q] != 0.f) ? __ldcg(pq[q] + (c4 + u) * 128 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float f = q < G ? mq[q] : 0.f;
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            acc[4 * u] += f * v[q][u].x;
-            acc[4 * u + 1] += f * v[q][u].y;
-            acc[4 * u + 2] += f * v[q][u].z;
-            acc[4 * u + 3] += f * v[q][u].w;
+            acc[4 * u] += mq[q] * v[q][u].x;
+            acc[4 * u + 1] += mq[q] * v[q][u].y;
+            acc[4 * u + 2] += mq[q] * v[q][u].z;
+            acc[4 * u + 3] += mq[q] * v[q][u].w;
           }
         }
         uint4 o;
@@ -607,13 +736,17 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
   }
 
+  // every DSMEM transfer into this CTA completed before the cluster barrier
+  // and the partials live in global memory, so no second barrier is needed
   tc_fence_before();
-  cluster_barrier(&bars[B_CLUSTER + 1], 2 * G, a.st, abort_p, 31);
+  __syncthreads();
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
   if (tid == 0) progress(a.st, prog, 7);
+  if (tid == 0) trace(a.st, tr, 59, tr0);
+  if (tr && tid == 0) a.st->pad[60] = n_my;
 }
 
 namespace {
@@ -686,6 +819,41 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, attn_kernel, mk, mw, batch);
+}
+
+// Clusters of `cluster_size` CTAs of attn_kernel that fit on the GPU at once
+// (cached per device and size).
+int attn_max_active_clusters(int cluster_size) {
+  static int cache_dev = -1;
+  static int cache[9] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cache_dev != dev) {
+    for (int i = 0; i < 9; ++i) cache[i] = -1;
+    cache_dev = dev;
+  }
+  if (cluster_size < 1 || cluster_size > 8) return 0;
+  if (cache[cluster_size] < 0) {
+    cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster_size, 1, 1);
+    cfg.blockDim = dim3(kThreadsAttn, 1, 1);
+    cfg.dynamicSmemBytes = kSmemAttn;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cache[cluster_size] = n;
+  }
+  return cache[cluster_size];
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream) {

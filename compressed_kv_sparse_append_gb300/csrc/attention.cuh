@@ -7,6 +7,8 @@ namespace ckv {
 
 constexpr int kMaxTopk = 2048;    // selected rows held per sequence
 constexpr int kMaxHeads = 128;    // query heads (one 128-row MMA tile)
+// Floats of one CTA's partial: O [64 column chunks][128 heads][4] + (m, l) [128].
+constexpr int64_t kPartFloats = 64 * 128 * 4 + 128 * 2;
 
 struct AttnArgs {
   const uint8_t* kv_data;
@@ -27,6 +29,7 @@ struct AttnArgs {
   __nv_bfloat16* out;     // [B][H][512]
   float* lse;             // [B][H] or null
   int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
+  float* part;            // workspace: [layer][B][2G][kPartFloats] partial O, m, l
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   int progress;           // debugging: count pipeline events in the status block
   DevStatus* st;
@@ -38,6 +41,7 @@ struct AttnBatch {
 };
 
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream);
+int attn_max_active_clusters(int cluster_size);
 // All `n` layers share B, G and the row format; layer l uses grid z = l.
 cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream);
 

@@ -32,6 +32,7 @@ struct IndexArgs {
   int32_t* out_pool;
   float* dbg;
   DevStatus* st;
+  int trace;                      // debugging: timeline in the status block
 };
 
 size_t index_smem_bytes();

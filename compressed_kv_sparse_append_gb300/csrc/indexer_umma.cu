@@ -14,8 +14,10 @@
 //   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, two
 //            buffers) = keys (A, M = 128) x query (B, N = 64), K = 128 in two
 //            block-scaled steps;
-//   warps 2-5 epilogue: move each tile's key scales into TMEM, then read D
-//            back (one key per thread) and form s = sum_h w_h ReLU(d_h) in f32.
+//   warps 6-9 move each tile's key scales into TMEM (lane = key), running
+//            ahead of the MMA by up to the ring depth;
+//   warps 2-5 epilogue: read D back (one key per thread) and form
+//            s = sum_h w_h ReLU(d_h) in f32.
 // The scores stay in shared memory; the chunk's top-K and the cross-chunk
 // merge are those of topk_merge.cuh.
 
@@ -28,7 +30,7 @@ namespace ckv {
 
 namespace {
 
-constexpr int kUThreads = 192;
+constexpr int kUThreads = 320;   // TMA, MMA, 4 epilogue warps, 4 scale-mover warps
 constexpr int kUStages = 6;
 constexpr int kUTile = 128;
 constexpr uint32_t kDataBytes = kUTile * 64;                 // 8 KB
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   const int64_t row0 = (int64_t)b * a.cap + c0;
 
   // ---- setup: FP4 query (B operand) + its scales, head weights, barriers
-  if (tid < 64 * 8) {
+  {
     for (int j = tid; j < 64 * 8; j += kUThreads) {
       const int h = j >> 3, blk = j & 7;
       uint32_t lo = 0, hi = 0;
@@ -154,8 +156,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   volatile int* abort_p = &abort_flag;
+  const bool tr = a.trace && b == 0 && chunk == 0;
+  const long long tr0 = clock64();
 
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
     // query scales -> TMEM (B operand scales): lane 32q + r, column j holds
     // the four block scales (one 32-bit word per K step) of query row 32j + r.
     const int qd = warp & 3;
@@ -176,6 +180,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) trace_at(a.st, tr, 0, tr0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA ----
@@ -213,25 +218,27 @@ __global__ void __launch_bounds__(kUThreads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------- epilogue ----
+  } else if (warp >= 6) {
+    // --------------------------------------------------- scale movers ----
     const int qd = warp & 3;
-    const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
+    const int m = qd * 32 + lane;
     const uint32_t lb = (uint32_t)(qd * 32) << 16;
-    auto move_scales = [&](int t) -> bool {
+    for (int t = 0; t < T; ++t) {
       const int s = t % kUStages;
-      if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) return false;
+      if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) break;
       const uint2 sc = *reinterpret_cast<const uint2*>(g + kOffScale + s * kScaleBytes + m * 8);
       tmem_st4(tmem + lb + kColSFA + 8 * s, sc.x, sc.x, sc.x, sc.x);
       tmem_st4(tmem + lb + kColSFA + 8 * s + 4, sc.y, sc.y, sc.y, sc.y);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[BU_SFA + s]);
-      return true;
-    };
-    bool ok = T > 0 ? move_scales(0) : true;
-    for (int t = 0; t < T && ok; ++t) {
-      if (t + 1 < T && !move_scales(t + 1)) break;
+    }
+  } else {
+    // ------------------------------------------------------- epilogue ----
+    const int qd = warp & 3;
+    const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
+    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+    for (int t = 0; t < T; ++t) {
       const int d = t & 1;
       if (!mbar_wait(&bars[BU_DFULL + d], (t >> 1) & 1, a.st, abort_p, 15)) break;
       tc_fence_after();
@@ -241,19 +248,20 @@ __global__ void __launch_bounds__(kUThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars[BU_DEMPTY + d]);
-      float s = 0.f;
+      float sc = 0.f;
 #pragma unroll
       for (int h4 = 0; h4 < 16; ++h4) {
         const float4 wv = reinterpret_cast<const float4*>(wsm)[h4];
-        s = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), s);
-        s = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), s);
-        s = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), s);
-        s = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), s);
+        sc = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), sc);
+        sc = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), sc);
+        sc = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), sc);
+        sc = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), sc);
       }
+      if (m == 0 && t < 8) trace_at(a.st, tr, 1 + t, tr0);
       const int i = t * kUTile + m;
       if (i < n_elem) {
-        keys[i] = score_key(s);
-        if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = s;
+        keys[i] = score_key(sc);
+        if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = sc;
       }
     }
   }
@@ -264,6 +272,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
     tmem_dealloc(tmem, kTmemU);
   }
   if (tid == 0) msm.n_real = (uint32_t)n_elem;
+  if (tid == 0) trace_at(a.st, tr, 9, tr0);
+  if (tr && tid == 0) a.st->pad[24] = T;
   __syncthreads();
   // The merge's survivors may use everything below the merge state: the
   // pipeline ring, the query tiles and the chunk's scores are all dead here.

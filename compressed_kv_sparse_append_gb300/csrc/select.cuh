@@ -79,9 +79,18 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
     for (int i = threadIdx.x; i < 256; i += NT) sm.hist[i] = 0;
     __syncthreads();
     const uint32_t mask = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    for (int i = threadIdx.x; i < n; i += NT) {
-      const uint32_t u = get(i);
-      if (((u ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u >> shift) & 255u], 1u);
+    // Scores of similar magnitude share their top key bits, so lanes are
+    // aggregated per digit before the shared-memory atomic.
+    const int n_round = (n + NT - 1) / NT * NT;
+    for (int i = threadIdx.x; i < n_round; i += NT) {
+      uint32_t digit = 0xFFFFFFFFu;
+      if (i < n) {
+        const uint32_t u = get(i);
+        if (((u ^ prefix) & mask) == 0) digit = (u >> shift) & 255u;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (digit != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane)
+        atomicAdd(&sm.hist[digit], (uint32_t)__popc(peers));
     }
     __syncthreads();
     if (warp == 0) {

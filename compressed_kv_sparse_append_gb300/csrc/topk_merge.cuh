@@ -66,6 +66,8 @@ __device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk
 template <int NT>
 __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* surv_key,
                                int32_t* surv_ent, int surv_cap) {
+  const bool tr = a.trace && b == 0 && threadIdx.x == 0;
+  const long long t0 = clock64();
   const int n_slots = a.n_chunks * a.K_sel;   // K_sel is a multiple of 4
   const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
   const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
@@ -103,26 +105,37 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   __syncthreads();
   const uint32_t tb = sm.bcast[0];
   __syncthreads();   // hs is reused below
+  trace_at(a.st, tr, 20, t0);
 
-  // (b) survivors (key bin >= tb) in slot order, 16 slots per thread per pass
+  // (b) survivors (key bin >= tb) in slot order, 16 slots per thread per
+  // pass; the next pass's loads are issued before this pass is compacted
   constexpr int kPer = 16;
   uint32_t n_surv = 0;
-  for (int base = 0; base < n_slots; base += kPer * NT) {
+  uint4 nk[kPer / 4];
+  int4 ni[kPer / 4];
+  auto fetch = [&](int base) {
     const int s0 = base + kPer * (int)threadIdx.x;
+#pragma unroll
+    for (int v = 0; v < kPer / 4; ++v) {
+      const int sv = s0 + 4 * v;
+      nk[v] = make_uint4(0u, 0u, 0u, 0u);
+      ni[v] = make_int4(-1, -1, -1, -1);
+      if (sv < n_slots) {
+        nk[v] = __ldcg(reinterpret_cast<const uint4*>(ck + sv));
+        ni[v] = __ldcg(reinterpret_cast<const int4*>(ci + sv));
+      }
+    }
+  };
+  fetch(0);
+  for (int base = 0; base < n_slots; base += kPer * NT) {
     uint32_t kk[kPer];
     int32_t ii[kPer];
 #pragma unroll
     for (int v = 0; v < kPer / 4; ++v) {
-      const int sv = s0 + 4 * v;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      int4 e = make_int4(-1, -1, -1, -1);
-      if (sv < n_slots) {
-        u = __ldcg(reinterpret_cast<const uint4*>(ck + sv));
-        e = __ldcg(reinterpret_cast<const int4*>(ci + sv));
-      }
-      kk[4 * v] = u.x; kk[4 * v + 1] = u.y; kk[4 * v + 2] = u.z; kk[4 * v + 3] = u.w;
-      ii[4 * v] = e.x; ii[4 * v + 1] = e.y; ii[4 * v + 2] = e.z; ii[4 * v + 3] = e.w;
+      kk[4 * v] = nk[v].x; kk[4 * v + 1] = nk[v].y; kk[4 * v + 2] = nk[v].z; kk[4 * v + 3] = nk[v].w;
+      ii[4 * v] = ni[v].x; ii[4 * v + 1] = ni[v].y; ii[4 * v + 2] = ni[v].z; ii[4 * v + 3] = ni[v].w;
     }
+    if (base + kPer * NT < n_slots) fetch(base + kPer * NT);
     uint32_t f = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) f |= (uint32_t)((kk[e] != 0u) && ((kk[e] >> kHistShift) >= tb)) << e;
@@ -141,6 +154,8 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     n_surv += tot;
   }
   __syncthreads();
+  trace_at(a.st, tr, 21, t0);
+  if (tr) a.st->pad[23] = (int32_t)n_surv;
   if (n_surv <= (uint32_t)surv_cap) {
     emit_outputs<NT>(
         a, b, (int)n_surv, n_real, [&](int i) { return surv_key[i]; },
@@ -151,6 +166,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
         a, b, n_slots, n_real, [&](int i) { return __ldcg(ck + i); },
         [&](int i) { return __ldcg(ci + i); }, sm);
   }
+  trace_at(a.st, tr, 22, t0);
 }
 
 // Local top-K of a scored chunk -> workspace (+ histogram); then the ticket.
@@ -166,6 +182,8 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
   const int kk = min(a.K_sel, (int)sm.n_real);
   const int32_t* pool = a.pool ? a.pool + (int64_t)b * a.pool_len + first_entry : nullptr;
+  const bool tr = a.trace && b == 0 && chunk == 0 && threadIdx.x == 0;
+  const long long t0 = clock64();
   block_select_ordered<NT>(
       n_elem, kk, [&](int i) { return keys[i]; },
       [&](int pos, int i) {
@@ -179,6 +197,7 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
     ck[i] = 0u;
     ci[i] = -1;
   }
+  trace_at(a.st, tr, 10, t0);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(a.counters + b, 1u);

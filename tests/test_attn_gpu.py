@@ -42,7 +42,7 @@ def test_hca_matches_oracle(fmt, blk, H, n_list, win_lens):
     n_comp = torch.tensor(n_list, dtype=torch.int32, device="cuda")
     wl_t = torch.tensor(win_lens, dtype=torch.int32, device="cuda")
     lse = torch.empty((B, H), device="cuda")
-    ws = b.new_workspace(256)
+    ws = b.new_workspace(b.workspace_bytes(b.OP_HCA_ATTN, B))
     out = b.hca_attn(kvp, n_comp, max(n_list), wp, wl_t, q, TAU, lse=lse, ws=ws)
     assert b.read_device_status(ws) == 0
     okv, owin = oracle_plane(fmt, kv, blk), oracle_plane(fmt, win, blk)
@@ -74,7 +74,7 @@ def test_csa_matches_oracle(fmt, blk, H, topk):
     win_lens = [128, 60, 0]
     wl_t = torch.tensor(win_lens, dtype=torch.int32, device="cuda")
     lse = torch.empty((B, H), device="cuda")
-    ws = b.new_workspace(256)
+    ws = b.new_workspace(b.workspace_bytes(b.OP_SPARSE_ATTN, B))
     out = b.csa_sparse_attn(kvp, wp, wl_t, idx.cuda(), q, TAU, lse=lse, ws=ws)
     assert b.read_device_status(ws) == 0
     okv, owin = oracle_plane(fmt, kv, blk), oracle_plane(fmt, win, blk)
@@ -106,7 +106,7 @@ def test_csa_out_of_range_index_is_flagged():
     q = wl.rms_rows((1, H, 512), 6, "cuda")
     idx = torch.tensor([[3, 500, 7]], dtype=torch.int32, device="cuda")
     wl_t = torch.tensor([4], dtype=torch.int32, device="cuda")
-    ws = b.new_workspace(256)
+    ws = b.new_workspace(b.workspace_bytes(b.OP_SPARSE_ATTN, 1))
     out = b.csa_sparse_attn(kvp, wp, wl_t, idx, q, TAU, ws=ws)
     assert b.read_device_status(ws) == -6
     okv, owin = oracle_plane("bf16", kv), oracle_plane("bf16", win)

@@ -46,7 +46,8 @@ def test_csa_full_size(name, sample):
             rows[s] = (kvr.cpu(), kr.cpu(), wr.cpu())
     n_comp = torch.full((B,), n, dtype=torch.int32, device="cuda")
     win_len = torch.full((B,), wl.W, dtype=torch.int32, device="cuda")
-    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, B, wl.H, wl.HI, n, wl.topk, 0))
+    ws = b.new_workspace(max(b.workspace_bytes(b.OP_INDEX_TOPK, B, wl.H, wl.HI, n, wl.topk, 0),
+                             b.workspace_bytes(b.OP_SPARSE_ATTN, B)))
     idx = b.csa_index_topk(keys, n_comp, n, qi, w, wl.topk, ws=ws)
     lse = torch.empty((B, wl.H), device="cuda")
     out = b.csa_sparse_attn(kv, win, win_len, idx, q, wl.tau, lse=lse, ws=ws)
@@ -91,7 +92,7 @@ def test_hca_full_size():
     n_comp = torch.full((B,), n, dtype=torch.int32, device="cuda")
     win_len = torch.full((B,), wl.W, dtype=torch.int32, device="cuda")
     lse = torch.empty((B, wl.H), device="cuda")
-    ws = b.new_workspace(256)
+    ws = b.new_workspace(b.workspace_bytes(b.OP_HCA_ATTN, B))
     out = b.hca_attn(kv, n_comp, n, win, win_len, q, wl.tau, lse=lse, ws=ws)
     assert b.read_device_status(ws) == 0
     for s in sample:
