@@ -167,10 +167,10 @@ size_t index_ws_bytes(int B, int n_comp_max, int K_sel, bool pool_mode, int pool
   return index_layout(B, n_comp_max, K_sel, pool_mode, pool_len).bytes;
 }
 
-// Partials of the attention's in-cluster merge: up to 8 CTAs (4 pairs) per
+// Partials of the attention's split-KV merge: up to 2 * kMaxPairs CTAs per
 // sequence and layer, kPartFloats floats each.
 size_t attn_part_bytes(int B, int layers) {
-  return align_up((size_t)layers * B * 8 * kPartFloats * sizeof(float), 256);
+  return align_up((size_t)layers * B * 2 * kMaxPairs * kPartFloats * sizeof(float), 256);
 }
 
 // Picks the number of CTA pairs per sequence (cluster of 2G CTAs): the
@@ -178,12 +178,12 @@ size_t attn_part_bytes(int B, int layers) {
 // `n_clusters` clusters be resident at once (one wave).
 int choose_pairs(int n_clusters, int n_rows_max) {
   const int tiles = (n_rows_max + 63) / 64;
-  for (int G = 4; G > 1; G >>= 1) {
-    if (tiles < G * 2) continue;
+  int best = 1;
+  for (int G = 2; G <= kMaxPairs && tiles >= 2 * G; ++G) {
     const int fit = attn_max_active_clusters(2 * G);
-    if (fit <= 0 || n_clusters <= fit) return G;
+    if (fit > 0 && n_clusters <= fit) best = G;
   }
-  return 1;
+  return best;
 }
 
 ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,

@@ -352,9 +352,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     tmem_wait_st();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  // Only the MMA and softmax warps need Q in TMEM: the loader warps start
+  // fetching the first tiles while Q is being loaded.
+  if (warp >= 5) {
+    tc_fence_before();
+    asm volatile("bar.sync 3, 160;" ::: "memory");
+    tc_fence_after();
+  }
   if (tid == 0) trace(a.st, tr, 0, tr0);
 
   if (warp == 0) {
@@ -416,6 +420,15 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + i % kXBufs]), peer));
       }
     }
+    // selected index of row p of this pair's tile i (main segment only)
+    auto fetch_sel = [&](int i) -> int32_t {
+      if (i >= n_my || p >= 64) return -1;
+      const Tile tn = tile_of(t0 + i, nt_main, n_sel, n_win);
+      if (tn.win || p >= tn.valid) return -1;
+      const int row = tn.start + p;
+      return idx_b ? __ldg(idx_b + row) : row;
+    };
+    int32_t x_next = use_tma ? -1 : fetch_sel(0);
     for (int i = 0; i < n_my && !use_tma; ++i) {
       const int s = i % kStages;
       const uint32_t tile = base + kOffE + s * kEBytes;
@@ -425,31 +438,33 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
             !mbar_wait(&bars[B_EEMPTY + s], ((i / kStages) + 1) & 1, a.st, abort_p, 23))
           break;
         // row of the tile's plane within sequence b (one thread per row; -1
-        // for an invalid row), validity mask
+        // for an invalid row), validity mask.  The selected index of the
+        // next tile is fetched here and used one tile later.
         int32_t* rsrc = reinterpret_cast<int32_t*>(gbase + kOffRowSrc) + s * 64;
         if (p < 64) {
           int32_t e = -1;
           if (p < tl.valid) {
-            const int row = tl.start + p;
             if (!tl.win) {
-              int32_t x = idx_b ? __ldg(idx_b + row) : row;
+              int32_t x = x_next;
               if (x >= a.kv_cap) {
                 if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
                 x = -1;
               }
               e = x >= 0 ? x : -1;
             } else {
-              e = row;
+              e = tl.start + p;
             }
           }
+          x_next = fetch_sel(i + 1);
           rsrc[p] = e;
           const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
           if ((p & 31) == 0) reinterpret_cast<uint32_t*>(gbase + kOffVmask)[s * 2 + (p >> 5)] = bal;
         }
         asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
         const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
         // every chunk load of a batch is issued before any conversion
-        constexpr int U = 8;
+        constexpr int U = 10;   // a whole MIXED / FP4 tile in one batch
         for (int j0 = p; j0 < kTile * J; j0 += 128 * U) {
           Raw raw[U];
 #pragma unroll
@@ -476,6 +491,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars[B_EFULL + s]);
       if (p == 0) progress(a.st, prog, 5);
+      if (p == 0 && i < 4) trace(a.st, tr, 53 + i, tr0);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------ MMA issuer ----
@@ -672,56 +688,56 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   }
   tc_fence_before();
   if (tid == 0) progress(a.st, prog, 6);
-  if (tid == 0) trace(a.st, tr, 57, tr0);
+  if (tid == 8 * 32) trace(a.st, tr, 57, tr0);   // a softmax thread (h = 64)
   cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
   if (tid == 0) trace(a.st, tr, 58, tr0);
 
   if (warp >= 6) {
     // ------------------------------- merge of the G partials of half c ----
+    // pair `pair` writes columns [8 u0, 8 u1) of this half (units of 8)
     const int h = (warp & 3) * 32 + lane;
-    const float4* pq[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      pq[q] = reinterpret_cast<const float4*>(
-          a.part + (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + 2 * (q < G ? q : 0) + half) * kPartFloats);
-    float mq[4] = {0.f, 0.f, 0.f, 0.f}, wq[4] = {0.f, 0.f, 0.f, 0.f};
+    const float4* pq0 = reinterpret_cast<const float4*>(
+        a.part + (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * kPartFloats);
+    constexpr int64_t kPart4 = 2 * kPartFloats / 4;   // float4 stride between pairs
+    float fq[kMaxPairs], wq[kMaxPairs];
     float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kMaxPairs; ++q) {
+      fq[q] = -INFINITY;
+      wq[q] = 0.f;
       if (q < G) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq[q] + 64 * 128) + h);
-        mq[q] = v.x;
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart4 + 64 * 128) + h);
+        fq[q] = v.x;
         wq[q] = v.y;
         M = fmaxf(M, v.x);
       }
     }
     float L = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float f = (q >= G || mq[q] == -INFINITY) ? 0.f : exp2f(mq[q] - M);
+    for (int q = 0; q < kMaxPairs; ++q) {
+      const float f = (q >= G || fq[q] == -INFINITY) ? 0.f : exp2f(fq[q] - M);
       L += wq[q] * f;
-      mq[q] = f;
+      fq[q] = f;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int cols = 256 / G, c4_0 = pair * cols / 4;
+    const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
     if (h < a.H) {
       __nv_bfloat16* out = a.out + ((int64_t)b * a.H + h) * 512 + half * 256;
-      for (int c4 = c4_0; c4 < c4_0 + cols / 4; c4 += 2) {
-        float4 v[4][2];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-            v[q][u] = (mq[q] != 0.f) ? __ldcg(pq[q] + (c4 + u) * 128 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = u0; u < u1; ++u) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            acc[4 * u] += mq[q] * v[q][u].x;
-            acc[4 * u + 1] += mq[q] * v[q][u].y;
-            acc[4 * u + 2] += mq[q] * v[q][u].z;
-            acc[4 * u + 3] += mq[q] * v[q][u].w;
+        for (int q = 0; q < kMaxPairs; ++q) {
+          if (q < G && fq[q] != 0.f) {
+            const float4* src = pq0 + q * kPart4 + (2 * u) * 128 + h;
+            const float4 v0 = __ldcg(src), v1 = __ldcg(src + 128);
+            acc[0] += fq[q] * v0.x;
+            acc[1] += fq[q] * v0.y;
+            acc[2] += fq[q] * v0.z;
+            acc[3] += fq[q] * v0.w;
+            acc[4] += fq[q] * v1.x;
+            acc[5] += fq[q] * v1.y;
+            acc[6] += fq[q] * v1.z;
+            acc[7] += fq[q] * v1.w;
           }
         }
         uint4 o;
@@ -729,7 +745,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
         o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
         o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(out + c4 * 4) = o;
+        *reinterpret_cast<uint4*>(out + 8 * u) = o;
       }
       if (rank == 0 && a.lse)
         a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
@@ -787,6 +803,8 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
     cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemAttn);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     attr_done = dev;
   }
   if (n < 1 || n > kMaxLayers) return cudaErrorInvalidValue;
@@ -825,16 +843,17 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
 // (cached per device and size).
 int attn_max_active_clusters(int cluster_size) {
   static int cache_dev = -1;
-  static int cache[9] = {0};
+  static int cache[2 * kMaxPairs + 1] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (cache_dev != dev) {
-    for (int i = 0; i < 9; ++i) cache[i] = -1;
+    for (int i = 0; i <= 2 * kMaxPairs; ++i) cache[i] = -1;
     cache_dev = dev;
   }
-  if (cluster_size < 1 || cluster_size > 8) return 0;
+  if (cluster_size < 1 || cluster_size > 2 * kMaxPairs) return 0;
   if (cache[cluster_size] < 0) {
     cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn);
+    cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster_size, 1, 1);
     cfg.blockDim = dim3(kThreadsAttn, 1, 1);

@@ -36,6 +36,7 @@ struct AttnArgs {
 };
 
 constexpr int kMaxLayers = 8;
+constexpr int kMaxPairs = 8;      // CTA pairs per sequence (clusters of up to 16 CTAs)
 struct AttnBatch {
   AttnArgs layer[kMaxLayers];  // one launch runs every layer (grid z = layer)
 };
