@@ -48,6 +48,16 @@ constexpr uint32_t kOffX = kOffE + kStages * kEBytes;
 constexpr int kXBufs = 4;                              // send-ahead needs four
 constexpr uint32_t kOffRowSrc = kOffX + kXBufs * kXBytes;    // int32 [kStages][64]
 constexpr uint32_t kOffVmask = kOffRowSrc + kStages * 64 * 4;  // u32 [kStages][2]
+// Raw bytes of a gathered tile, staged inside its own 32 KB stage buffer
+// before they are dequantised over it: MIXED rows (256 or 320 bytes) from
+// byte 8192 and one f32 scale word per 16-byte chunk from byte 28672; FP4
+// rows (128 bytes) from byte 16384 and their 16 scale bytes from 24576.
+constexpr uint32_t kRawOffMixed = 8192, kScaleOffMixed = 28672;
+constexpr uint32_t kRawOffFp4 = 16384, kScaleOffFp4 = 24576;
+static_assert(kRawOffMixed + 64 * 320 <= kScaleOffMixed && kScaleOffMixed + 64 * 16 * 4 <= kEBytes,
+              "MIXED staging fits in a stage");
+static_assert(kRawOffFp4 + 64 * 128 <= kScaleOffFp4 && kScaleOffFp4 + 64 * 16 <= kEBytes,
+              "FP4 staging fits in a stage");
 constexpr uint32_t kOffBar = kOffVmask + kStages * 8;
 constexpr uint32_t kNumBars = 4 * kStages + 10;
 constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
@@ -148,49 +158,71 @@ __device__ __forceinline__ Tile tile_of(int t, int nt_main, int n_sel, int n_win
   return r;
 }
 
+// Asynchronous global -> shared copies (cp.async): the gather keeps no
+// registers while the loads are in flight.  A 16-byte copy with src_bytes =
+// 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most `n` (0..3) of this thread's newest copy groups are pending.
+__device__ __forceinline__ void cp_async_wait(int n) {
+  if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else asm volatile("cp.async.wait_group 3;" ::: "memory");
+}
+// Named barrier `id` over `n` threads that also ANDs `v` across them, so a
+// failed wait in any thread makes every thread leave the loop together.
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred pv, pr;\n setp.ne.b32 pv, %1, 0;\n bar.red.and.pred pr, %2, %3, pv;\n"
+      " selp.b32 %0, 1, 0, pr;\n}\n"
+      : "=r"(r)
+      : "r"((int)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
 // Raw bytes of one 16-byte source chunk of a row plus its scale bits.
 struct Raw {
   uint4 v;
   uint32_t s;   // MIXED: f32 scale bits; FP4: two E4M3 scale bytes
 };
 
-// Load local latent chunk `q` of cache entry `entry` (-1: empty row).
-__device__ __forceinline__ Raw load_chunk(const AttnArgs& a, int q, int64_t entry, bool win,
-                                          int half) {
-  Raw r;
-  r.v = make_uint4(0u, 0u, 0u, 0u);
-  r.s = 0u;
-  if (entry < 0) return r;
-  const uint8_t* data = win ? a.win_data : a.kv_data;
-  const void* scale = win ? a.win_scale : a.kv_scale;
-  if (a.fmt == CKV_FMT_BF16) {
-    r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 1024 + half * 512 + q * 16));
-  } else if (a.fmt == CKV_FMT_MIXED) {
-    const int n_fp8 = half == 0 ? 16 : 12;
-    if (q < n_fp8) {
-      r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 576 + half * 256 + q * 16));
-      const int nblk = 448 / a.nope_block;
-      r.s = __ldg(reinterpret_cast<const uint32_t*>(scale) + entry * nblk +
-                  (half * 256 + q * 16) / a.nope_block);
-    } else {
-      r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 576 + 448 + (q - 12) * 16));
-    }
-  } else {
-    r.v = __ldg(reinterpret_cast<const uint4*>(data + entry * 256 + half * 128 + q * 16));
-    r.s = __ldg(reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(scale) +
-                                                  entry * 32 + half * 16 + q * 2));
-  }
-  return r;
-}
-
 // Dequantise a loaded chunk to bf16 and store it at row `r` of the swizzled
 // tile (an empty row stores zeros: its raw bytes and scale are zero).
+template <int FMT>
 __device__ __forceinline__ void store_chunk(const AttnArgs& a, uint32_t tile, int r, int q,
                                             const Raw& raw, int half) {
-  if (a.fmt == CKV_FMT_BF16) {
+  if constexpr (FMT == CKV_FMT_BF16) {
     const int d0 = q * 8;
     st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), raw.v);
-  } else if (a.fmt == CKV_FMT_MIXED) {
+  } else if constexpr (FMT == CKV_FMT_MIXED) {
     const int n_fp8 = half == 0 ? 16 : 12;
     if (q < n_fp8) {
       const float s = __uint_as_float(raw.s);
@@ -232,8 +264,17 @@ __device__ __forceinline__ void store_chunk(const AttnArgs& a, uint32_t tile, in
   }
 }
 
-__device__ __forceinline__ int chunks_per_row(int fmt, int half) {
-  return fmt == CKV_FMT_BF16 ? 32 : fmt == CKV_FMT_MIXED ? (half == 0 ? 16 : 20) : 8;
+template <int FMT>
+__device__ __forceinline__ int chunks_per_row(int half) {
+  return FMT == CKV_FMT_BF16 ? 32 : FMT == CKV_FMT_MIXED ? (half == 0 ? 16 : 20) : 8;
+}
+
+// j / J for the chunk counts above, with constant divisors.
+template <int FMT>
+__device__ __forceinline__ int chunk_row(int j, int half) {
+  if constexpr (FMT == CKV_FMT_BF16) return j >> 5;
+  else if constexpr (FMT == CKV_FMT_MIXED) return half == 0 ? (j >> 4) : j / 20;
+  else return j >> 3;
 }
 
 }  // namespace
@@ -244,6 +285,7 @@ __device__ __forceinline__ void trace(DevStatus* st, bool on, int slot, long lon
   if (on && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
 }
 
+template <int FMT>
 __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
                 const __grid_constant__ AttnBatch batch) {
@@ -384,7 +426,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   } else if (warp >= 1 && warp <= 4) {
     // ------------------------------------------- producers / TMA fix-up ----
     const int p = tid - 32;
-    const int J = chunks_per_row(a.fmt, half);
+    const int J = chunks_per_row<FMT>(half);
     if (use_tma) {
       // TMA-fed tiles: these warps release each landed tile to the MMA
       // (zeroing rows past the end of its segment, so that P = 0 meets finite
@@ -420,71 +462,111 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + i % kXBufs]), peer));
       }
     }
-    // selected index of row p of this pair's tile i (main segment only)
-    auto fetch_sel = [&](int i) -> int32_t {
-      if (i >= n_my || p >= 64) return -1;
-      const Tile tn = tile_of(t0 + i, nt_main, n_sel, n_win);
-      if (tn.win || p >= tn.valid) return -1;
-      const int row = tn.start + p;
-      return idx_b ? __ldg(idx_b + row) : row;
+    // Gathered rows.  copies(i) copies tile i's raw bytes with cp.async into
+    // its stage buffer (BF16 rows straight to their swizzled place, quantised
+    // rows to the staging area), up to kAhead tiles ahead; finish(i) waits
+    // for them and, for quantised rows, dequantises in place: every thread
+    // first reads its raw chunks, the producers meet, then BF16 is written
+    // over the buffer.
+    constexpr int kAhead = 3;
+    constexpr int U = (kTile * (FMT == CKV_FMT_BF16 ? 32 : FMT == CKV_FMT_MIXED ? 20 : 8) + 127) / 128;
+    uint32_t* vmask_s = reinterpret_cast<uint32_t*>(gbase + kOffVmask);
+    int32_t* rsrc = reinterpret_cast<int32_t*>(gbase + kOffRowSrc);
+    // selected entry (or row) feeding row r of tile i, before range checks
+    auto raw_index = [&](int i, int r) -> int32_t {
+      if (i >= n_my) return -1;
+      const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
+      if (r >= tl.valid) return -1;
+      if (tl.win) return tl.start + r;
+      return idx_b ? __ldg(idx_b + tl.start + r) : tl.start + r;
     };
-    int32_t x_next = use_tma ? -1 : fetch_sel(0);
-    for (int i = 0; i < n_my && !use_tma; ++i) {
+    // plane row (within sequence b) of row r of tile i from its raw index,
+    // -1 for none, published with the tile's validity mask (warp-uniform i)
+    auto publish = [&](int i, int r, int32_t x) {
+      const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
+      if (!tl.win && x >= a.kv_cap) {
+        if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
+        x = -1;
+      }
+      const int32_t e = x >= 0 ? x : -1;
+      rsrc[(i % kStages) * 64 + r] = e;
+      const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
+      if ((r & 31) == 0) vmask_s[(i % kStages) * 2 + (r >> 5)] = bal;
+    };
+    // the copies of tile i (rows published, stage free)
+    auto copies = [&](int i) {
       const int s = i % kStages;
+      if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
       const uint32_t tile = base + kOffE + s * kEBytes;
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-      {
-        if (i >= kStages &&
-            !mbar_wait(&bars[B_EEMPTY + s], ((i / kStages) + 1) & 1, a.st, abort_p, 23))
-          break;
-        // row of the tile's plane within sequence b (one thread per row; -1
-        // for an invalid row), validity mask.  The selected index of the
-        // next tile is fetched here and used one tile later.
-        int32_t* rsrc = reinterpret_cast<int32_t*>(gbase + kOffRowSrc) + s * 64;
-        if (p < 64) {
-          int32_t e = -1;
-          if (p < tl.valid) {
-            if (!tl.win) {
-              int32_t x = x_next;
-              if (x >= a.kv_cap) {
-                if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
-                x = -1;
-              }
-              e = x >= 0 ? x : -1;
+      const uint8_t* data = tl.win ? a.win_data : a.kv_data;
+      const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
+      const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = p + 128 * u;
+        if (j >= kTile * J) break;
+        const int r = chunk_row<FMT>(j, half), q = j - r * J;
+        const int32_t e = rsrc[s * 64 + r];
+        const int64_t ent = row0 + e;
+        if constexpr (FMT == CKV_FMT_BF16) {
+          const int d0 = q * 8;
+          cp_async16(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3),
+                     e >= 0 ? data + ent * 1024 + half * 512 + q * 16 : data, e >= 0 ? 16u : 0u);
+        } else if constexpr (FMT == CKV_FMT_MIXED) {
+          if (e >= 0) {
+            const uint32_t dst = tile + kRawOffMixed + r * (half == 0 ? 256 : 320) + q * 16;
+            if (q < (half == 0 ? 16 : 12)) {
+              cp_async16(dst, data + ent * 576 + half * 256 + q * 16, 16u);
+              const int nblk = 448 / a.nope_block;
+              cp_async4(tile + kScaleOffMixed + (r * 16 + q) * 4,
+                        scale + (ent * nblk + (half * 256 + q * 16) / a.nope_block) * 4);
             } else {
-              e = tl.start + p;
+              cp_async16(dst, data + ent * 576 + 448 + (q - 12) * 16, 16u);
             }
           }
-          x_next = fetch_sel(i + 1);
-          rsrc[p] = e;
-          const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
-          if ((p & 31) == 0) reinterpret_cast<uint32_t*>(gbase + kOffVmask)[s * 2 + (p >> 5)] = bal;
+        } else {
+          if (e >= 0) {
+            cp_async16(tile + kRawOffFp4 + r * 128 + q * 16, data + ent * 256 + half * 128 + q * 16, 16u);
+            if (q == 0) cp_async16(tile + kScaleOffFp4 + r * 16, scale + ent * 32 + half * 16, 16u);
+          }
         }
-        asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
-        const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
-        // every chunk load of a batch is issued before any conversion
-        constexpr int U = 10;   // a whole MIXED / FP4 tile in one batch
-        for (int j0 = p; j0 < kTile * J; j0 += 128 * U) {
-          Raw raw[U];
+      }
+      cp_async_commit();
+    };
+    auto finish = [&](int i, int newer) {
+      const int s = i % kStages;
+      const uint32_t tile = base + kOffE + s * kEBytes;
+      cp_async_wait(newer);                      // this thread's copies of tile i
+      asm volatile("bar.sync 2, 128;" ::: "memory");   // everyone's
+      if constexpr (FMT != CKV_FMT_BF16) {
+        const uint64_t vbits = (uint64_t)vmask_s[s * 2] | ((uint64_t)vmask_s[s * 2 + 1] << 32);
+        Raw raw[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * 128;
-            raw[u].v = make_uint4(0u, 0u, 0u, 0u);
-            raw[u].s = 0u;
-            if (j < kTile * J) {
-              const int r = j / J, q = j - r * J;
-              const int32_t x = rsrc[r];
-              raw[u] = load_chunk(a, q, x >= 0 ? row0 + x : -1, tl.win != 0, half);
+        for (int u = 0; u < U; ++u) {
+          const int j = p + 128 * u;
+          raw[u].v = make_uint4(0u, 0u, 0u, 0u);
+          raw[u].s = 0u;
+          if (j < kTile * J) {
+            const int r = chunk_row<FMT>(j, half), q = j - r * J;
+            if ((vbits >> r) & 1ull) {
+              if constexpr (FMT == CKV_FMT_MIXED) {
+                raw[u].v = ld_shared_u4(tile + kRawOffMixed + r * (half == 0 ? 256 : 320) + q * 16);
+                if (q < (half == 0 ? 16 : 12)) raw[u].s = ld_shared_u32(tile + kScaleOffMixed + (r * 16 + q) * 4);
+              } else {
+                raw[u].v = ld_shared_u4(tile + kRawOffFp4 + r * 128 + q * 16);
+                raw[u].s = ld_shared_u16(tile + kScaleOffFp4 + r * 16 + q * 2);
+              }
             }
           }
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");   // raw bytes read: overwrite
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int j = j0 + u * 128;
-            if (j < kTile * J) {
-              const int r = j / J, q = j - r * J;
-              store_chunk(a, tile, r, q, raw[u], half);
-            }
+        for (int u = 0; u < U; ++u) {
+          const int j = p + 128 * u;
+          if (j < kTile * J) {
+            const int r = chunk_row<FMT>(j, half), q = j - r * J;
+            store_chunk<FMT>(a, tile, r, q, raw[u], half);
           }
         }
       }
@@ -492,6 +574,41 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       mbar_arrive(&bars[B_EFULL + s]);
       if (p == 0) progress(a.st, prog, 5);
       if (p == 0 && i < 4) trace(a.st, tr, 53 + i, tr0);
+    };
+    if (!use_tma) {
+      // the first kAhead + 1 tiles (free stages): every lookup in one round
+      // trip (thread p takes row p % 64 of tiles p / 64 and p / 64 + 2)
+      const int n_init = min(n_my, kAhead + 1);
+      {
+        const int r = p & 63, ta = p >> 6, tb = ta + 2;
+        const int32_t xa = ta < n_init ? raw_index(ta, r) : -1;
+        const int32_t xb = tb < n_init ? raw_index(tb, r) : -1;
+        if (ta < n_init) publish(ta, r, xa);
+        if (tb < n_init) publish(tb, r, xb);
+      }
+      int32_t x_next = p < 64 ? raw_index(n_init, p) : -1;   // used one tile later
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      for (int t = 0; t < n_init; ++t) copies(t);
+      int issued = n_init;
+      bool ok = true;
+      for (int i = 0; i < n_my && ok; ++i) {
+        finish(i, issued - 1 - i);
+        if (issued < n_my) {
+          const int t = issued, s = t % kStages;
+          ok = t < kStages ||
+               mbar_wait(&bars[B_EEMPTY + s], ((t / kStages) + 1) & 1, a.st, abort_p, 23);
+          ok = bar_and(2, 128, ok);   // every producer leaves together on a failed wait
+          if (!ok) break;
+          if (p < 64) {
+            publish(t, p, x_next);
+            x_next = raw_index(t + 1, p);
+          }
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          copies(t);
+          ++issued;
+        }
+      }
+      cp_async_wait(0);   // nothing stays in flight past this point
     }
   } else if (warp == 5) {
     // ------------------------------------------------------ MMA issuer ----
@@ -795,19 +912,35 @@ bool encode_bf16_rows(CUtensorMap* m, const void* data, int64_t rows) {
 
 }  // namespace
 
-cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream) {
+using AttnKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnBatch);
+
+// The kernel instance for a cache format (nullptr for an unknown one), with
+// its launch attributes set once per device.
+static AttnKernelFn attn_kernel_for(int fmt) {
   static int attr_done = -1;
   int dev = 0;
   cudaGetDevice(&dev);
+  const AttnKernelFn ks[3] = {attn_kernel<CKV_FMT_BF16>, attn_kernel<CKV_FMT_MIXED>,
+                              attn_kernel<CKV_FMT_FP4>};
   if (attr_done != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemAttn);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+    for (AttnKernelFn k : ks) {
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return nullptr;
+    }
     attr_done = dev;
   }
+  return fmt == CKV_FMT_BF16 ? ks[0] : fmt == CKV_FMT_MIXED ? ks[1] : fmt == CKV_FMT_FP4 ? ks[2] : nullptr;
+}
+
+cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream) {
   if (n < 1 || n > kMaxLayers) return cudaErrorInvalidValue;
+  const AttnArgs& a0 = layers[0];
+  for (int l = 1; l < n; ++l)
+    if (layers[l].fmt != a0.fmt || layers[l].G != a0.G) return cudaErrorInvalidValue;
+  const AttnKernelFn kern = attn_kernel_for(a0.fmt);
+  if (!kern) return cudaErrorInvalidValue;
   AttnBatch batch;
   memset(&batch, 0, sizeof(batch));
   for (int l = 0; l < n; ++l) {
@@ -819,7 +952,6 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   memset(&mw, 0, sizeof(mw));
   // Contiguous BF16 rows (HCA, one layer) stream through TMA; gathered or
   // quantised rows go through the producer warps.
-  const AttnArgs& a0 = layers[0];
   if (n == 1 && a0.fmt == CKV_FMT_BF16 && a0.idx == nullptr &&
       encode_bf16_rows(&mk, a0.kv_data, (int64_t)B * a0.kv_cap) &&
       encode_bf16_rows(&mw, a0.win_data, (int64_t)B * a0.win_cap))
@@ -836,7 +968,7 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_kernel, mk, mw, batch);
+  return cudaLaunchKernelEx(&cfg, kern, mk, mw, batch);
 }
 
 // Clusters of `cluster_size` CTAs of attn_kernel that fit on the GPU at once
@@ -852,8 +984,9 @@ int attn_max_active_clusters(int cluster_size) {
   }
   if (cluster_size < 1 || cluster_size > 2 * kMaxPairs) return 0;
   if (cache[cluster_size] < 0) {
-    cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn);
-    cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    // every format's instance has the same resources: ask about one
+    const AttnKernelFn kern = attn_kernel_for(CKV_FMT_MIXED);
+    if (!kern) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster_size, 1, 1);
     cfg.blockDim = dim3(kThreadsAttn, 1, 1);
@@ -866,7 +999,7 @@ int attn_max_active_clusters(int cluster_size) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;
     }
