@@ -1,8 +1,9 @@
 // Block-wide exact top-K selection on order-preserving u32 keys.
 //
 // The top-K (largest keys; among equal keys the earliest elements) of n
-// elements is found with a 4-pass, 8-bit radix select of the K-th largest key
-// T, then an order-preserving compaction that keeps every key > T and the
+// elements is found with an 8-bit radix select of the K-th largest key T
+// (over the bits the keys do not all share), then an order-preserving
+// compaction that keeps every key > T and the
 // first `need` keys == T.  Elements are visited in array order, so when the
 // array is in ascending entry order the output is the ascending index set and
 // a tie at T goes to the lower entry index ("DeepSeek-V4 KV Cache 深度分析",
@@ -69,28 +70,58 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea
 
 // Finds T (the K-th largest key among n, K <= n) and need = how many
 // elements equal to T belong to the top-K.  get(i) returns element i's key.
+// The bits every key shares (the common prefix of the smallest and largest
+// key) are settled first; the rest is resolved 8 bits per pass, so scores of
+// similar magnitude (which share their exponent bits) spread over the bins
+// instead of piling onto one.
 template <int NT, class Get>
 __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm, uint32_t& T,
                                       uint32_t& need) {
-  uint32_t prefix = 0, remaining = (uint32_t)K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t u = get(i);
+    lo = min(lo, u);
+    hi = max(hi, u);
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    sm.warp_a[warp] = lo;
+    sm.warp_b[warp] = hi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t l2 = lane < NT / 32 ? sm.warp_a[lane] : 0xFFFFFFFFu;
+    uint32_t h2 = lane < NT / 32 ? sm.warp_b[lane] : 0u;
+    l2 = __reduce_min_sync(0xffffffffu, l2);
+    h2 = __reduce_max_sync(0xffffffffu, h2);
+    if (lane == 0) {
+      sm.bcast[2] = l2;
+      sm.bcast[3] = h2;
+    }
+  }
+  __syncthreads();
+  lo = sm.bcast[2];
+  hi = sm.bcast[3];
+  __syncthreads();
+  if (lo == hi) {   // every key equal
+    T = lo;
+    need = (uint32_t)K;
+    return;
+  }
+  int top = 32 - __clz(lo ^ hi);   // bits [top, 32) are the same in every key
+  uint32_t prefix = top == 32 ? 0u : (lo & (0xFFFFFFFFu << top)), remaining = (uint32_t)K;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  while (top > 0) {
+    const int width = top < 8 ? top : 8, shift = top - width;
     for (int i = threadIdx.x; i < 256; i += NT) sm.hist[i] = 0;
     __syncthreads();
-    const uint32_t mask = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
-    // Scores of similar magnitude share their top key bits, so lanes are
-    // aggregated per digit before the shared-memory atomic.
-    const int n_round = (n + NT - 1) / NT * NT;
-    for (int i = threadIdx.x; i < n_round; i += NT) {
-      uint32_t digit = 0xFFFFFFFFu;
-      if (i < n) {
-        const uint32_t u = get(i);
-        if (((u ^ prefix) & mask) == 0) digit = (u >> shift) & 255u;
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (digit != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane)
-        atomicAdd(&sm.hist[digit], (uint32_t)__popc(peers));
+    const uint32_t mask = top == 32 ? 0u : (0xFFFFFFFFu << top);   // settled bits
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const uint32_t u = get(i);
+      if (((u ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u >> shift) & dmask], 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -124,6 +155,7 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
     __syncthreads();
     prefix |= sm.bcast[0] << shift;
     remaining = sm.bcast[1];
+    top = shift;
     __syncthreads();
   }
   T = prefix;
@@ -133,11 +165,13 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
 // Writes the top-K of n elements (or all n if n <= K) in array order via
 // emit(out_pos, i).  Returns the number emitted.
 template <int NT, class Get, class Emit>
-__device__ int block_select_ordered(int n, int K, Get get, Emit emit, SelectSmem<NT>& sm) {
+__device__ int block_select_ordered(int n, int K, Get get, Emit emit, SelectSmem<NT>& sm,
+                                    long long* marks = nullptr) {
   if (n <= 0 || K <= 0) return 0;
   const bool all = n <= K;
   uint32_t T = 0, need = 0;
   if (!all) block_radix_threshold<NT>(n, K, get, sm, T, need);
+  if (marks && threadIdx.x == 0) marks[0] = clock64();
   const int per = (n + NT - 1) / NT;
   const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
   uint32_t gt = 0, eq = 0;
@@ -152,6 +186,7 @@ __device__ int block_select_ordered(int n, int K, Get get, Emit emit, SelectSmem
   }
   uint32_t gt_before, eq_before, gt_tot, eq_tot;
   block_scan2<NT>(gt, eq, gt_before, eq_before, gt_tot, eq_tot, sm);
+  if (marks && threadIdx.x == 0) marks[1] = clock64();
   uint32_t pos = gt_before + min(eq_before, need);
   uint32_t eq_rank = eq_before;
   for (int i = i0; i < i1; ++i) {

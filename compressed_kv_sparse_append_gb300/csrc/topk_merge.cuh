@@ -184,22 +184,40 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   const int32_t* pool = a.pool ? a.pool + (int64_t)b * a.pool_len + first_entry : nullptr;
   const bool tr = a.trace && b == 0 && chunk == 0 && threadIdx.x == 0;
   const long long t0 = clock64();
+  long long marks[2] = {0, 0};
   block_select_ordered<NT>(
       n_elem, kk, [&](int i) { return keys[i]; },
       [&](int pos, int i) {
         const uint32_t u = keys[i];
         ck[pos] = u;
         ci[pos] = pool ? pool[i] : (int32_t)(first_entry + i);
-        atomicAdd(hist + (u >> kHistShift), 1u);
+        sm.pool_key[pos] = u;   // free until the merge
       },
-      sm.sel);
+      sm.sel, tr ? marks : nullptr);
+  if (tr) {
+    a.st->pad[12] = (int32_t)(marks[0] - t0);
+    a.st->pad[13] = (int32_t)(marks[1] - t0);
+  }
   for (int i = kk + threadIdx.x; i < a.K_sel; i += NT) {
     ck[i] = 0u;
     ci[i] = -1;
   }
+  __syncthreads();
+  // The candidates' keys crowd into a few histogram bins: one global atomic
+  // per distinct bin per warp instead of one per candidate.
+  {
+    const int lane = threadIdx.x & 31;
+    const int k_round = (kk + 31) / 32 * 32;
+    for (int i = threadIdx.x; i < k_round; i += NT) {
+      const uint32_t bin = i < kk ? (sm.pool_key[i] >> kHistShift) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+      if (bin != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+    }
+  }
   trace_at(a.st, tr, 10, t0);
   __threadfence();
   __syncthreads();
+  trace_at(a.st, tr, 11, t0);
   if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(a.counters + b, 1u);
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
