@@ -226,7 +226,7 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.st = st;
   a.use_tma = 0;
   const char* pe = getenv("CKV_DEBUG_PROGRESS");
-  a.progress = (pe && (pe[0] == '1' || pe[0] == '2')) ? pe[0] - '0' : 0;
+  a.progress = (pe && pe[0] >= '1' && pe[0] <= '3') ? pe[0] - '0' : 0;
   return a;
 }
 

@@ -50,16 +50,17 @@ constexpr uint32_t kOffRowSrc = kOffX + kXBufs * kXBytes;    // int32 [kStages][
 constexpr uint32_t kOffVmask = kOffRowSrc + kStages * 64 * 4;  // u32 [kStages][2]
 // Raw bytes of a gathered tile, staged inside its own 32 KB stage buffer
 // before they are dequantised over it: MIXED rows (256 or 320 bytes) from
-// byte 8192 and one f32 scale word per 16-byte chunk from byte 28672; FP4
-// rows (128 bytes) from byte 16384 and their 16 scale bytes from 24576.
+// byte 8192 and each row's f32 scale words (32 bytes a row) from 28672; FP4
+// rows (128 bytes) from byte 16384 and their 16 scale bytes from 24576, in
+// 128-byte groups of four rows (every TMA destination is 128-byte aligned).
 constexpr uint32_t kRawOffMixed = 8192, kScaleOffMixed = 28672;
 constexpr uint32_t kRawOffFp4 = 16384, kScaleOffFp4 = 24576;
-static_assert(kRawOffMixed + 64 * 320 <= kScaleOffMixed && kScaleOffMixed + 64 * 16 * 4 <= kEBytes,
+static_assert(kRawOffMixed + 64 * 320 <= kScaleOffMixed && kScaleOffMixed + 64 * 32 <= kEBytes,
               "MIXED staging fits in a stage");
-static_assert(kRawOffFp4 + 64 * 128 <= kScaleOffFp4 && kScaleOffFp4 + 64 * 16 <= kEBytes,
+static_assert(kRawOffFp4 + 64 * 128 <= kScaleOffFp4 && kScaleOffFp4 + 16 * 128 <= kEBytes,
               "FP4 staging fits in a stage");
 constexpr uint32_t kOffBar = kOffVmask + kStages * 8;
-constexpr uint32_t kNumBars = 4 * kStages + 10;
+constexpr uint32_t kNumBars = 5 * kStages + 12;
 constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffSlot + 16;
 constexpr uint32_t kSmemAttn = kSmemUsed + 1024;
@@ -74,19 +75,19 @@ constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (factor 256)
 // barrier indices
 constexpr int B_TMA = 0, B_EFULL = kStages, B_EEMPTY = 2 * kStages;
 constexpr int B_SFULL = 3 * kStages, B_PFULL = B_SFULL + 2, B_ODONE = B_PFULL + 2,
-              B_XFULL = B_ODONE + 1, B_CLUSTER = B_XFULL + kXBufs, B_XREAD = B_CLUSTER + 2;
+              B_XFULL = B_ODONE + 1, B_CLUSTER = B_XFULL + kXBufs, B_XREAD = B_CLUSTER + 2,
+              B_GFULL = B_XREAD + 2;
+static_assert(B_GFULL + kStages <= (int)kNumBars, "barrier count");
 
-// Cluster-wide barrier `k` built on mbarriers with a bounded wait: thread 0
-// of every CTA arrives (release, cluster scope) on barrier k of every CTA of
-// the cluster after a CTA barrier; every thread then waits on its own CTA's
+// Cluster-wide barrier `k` built on mbarriers with a bounded wait: after a
+// CTA barrier, thread r of every CTA arrives (release, cluster scope, which
+// also covers the writes the CTA barrier ordered before it) on barrier k of
+// CTA r, all CTAs in parallel; every thread then waits on its own CTA's
 // barrier k (acquire, cluster scope).  Each barrier is used once (phase 0).
 __device__ __forceinline__ void cluster_barrier(uint64_t* bars_k, int n_cta, DevStatus* st,
                                                 volatile int* abort, int where) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t local = smem_u32(bars_k);
-    for (int r = 0; r < n_cta; ++r) mbar_arrive_remote(mapa(local, (uint32_t)r));
-  }
+  if ((int)threadIdx.x < n_cta) mbar_arrive_remote(mapa(smem_u32(bars_k), threadIdx.x));
   mbar_wait_poll(bars_k, 0, st, abort, where);
 }
 
@@ -106,6 +107,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
       "%3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows (y0..y3; a negative or out-of-range row reads zeros) of the
+// one-row box at column x of a 2-D tensor map, stacked at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0,
+                                            int y1, int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -158,13 +171,8 @@ __device__ __forceinline__ Tile tile_of(int t, int nt_main, int n_sel, int n_win
   return r;
 }
 
-// Asynchronous global -> shared copies (cp.async): the gather keeps no
-// registers while the loads are in flight.  A 16-byte copy with src_bytes =
-// 0 writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
+// Asynchronous 4-byte global -> shared copies (cp.async) for the MIXED
+// scale words, whose rows are too narrow for TMA.
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -328,6 +336,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     for (int k = 0; k < kXBufs; ++k) mbar_init(&bars[B_XFULL + k], 128);
     mbar_init(&bars[B_XREAD], 128);
     mbar_init(&bars[B_XREAD + 1], 128);
+    for (int k = 0; k < kStages; ++k) mbar_init(&bars[B_GFULL + k], 1);
     mbar_init(&bars[B_ODONE], 1);
     mbar_init(&bars[B_CLUSTER], 2 * G);
     mbar_init(&bars[B_CLUSTER + 1], 2 * G);
@@ -342,6 +351,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const bool prog = a.progress == 1;
   const bool tr = a.progress == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
   const long long tr0 = clock64();
+  // progress mode 3: the CTAs of sequence 0 (layer 0) store %globaltimer
+  // (low 32 bits) at start, softmax end and cluster-barrier exit
+  const bool tr3 = a.progress == 3 && blockIdx.y == 0 && blockIdx.z == 0 && rank < 16;
+  auto stamp3 = [&](int k) {
+    if (tr3) a.st->pad[3 * rank + k] = (int32_t)(uint32_t)globaltimer();
+  };
+  if (tid == 0) stamp3(0);
   if (tid == 0) progress(a.st, prog, 0);
 
   // Rounds this CTA's partial scores S(k) of head row `hq` (TMEM lane
@@ -493,53 +509,82 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
       if ((r & 31) == 0) vmask_s[(i % kStages) * 2 + (r >> 5)] = bal;
     };
-    // the copies of tile i (rows published, stage free)
+    // the copies of tile i (rows published, stage free): the tile's rows by
+    // TMA gathers of four rows each, issued by one thread; MIXED scale words
+    // (4-byte row strides, which TMA cannot address) by cp.async
     auto copies = [&](int i) {
       const int s = i % kStages;
       if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
       const uint32_t tile = base + kOffE + s * kEBytes;
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-      const uint8_t* data = tl.win ? a.win_data : a.kv_data;
-      const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
       const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
+      const CUtensorMap* gm = &a.gmap[tl.win ? 2 : 0];
+      const int32_t* rs = rsrc + s * 64;
+      if ((p & 31) == 0) {
+        // lane 0 of each producer warp issues four of the sixteen groups;
+        // warp 0's also arms the barrier (the transaction count may go
+        // negative until it does)
+        constexpr uint32_t kBytes = FMT == CKV_FMT_BF16 ? 64 * 512 : FMT == CKV_FMT_FP4 ? 64 * 144 : 0;
+        const uint32_t bytes = FMT == CKV_FMT_MIXED ? 64u * (half == 0 ? 256u : 320u) : kBytes;
+        if (p == 0) mbar_expect_tx(&bars[B_GFULL + s], bytes);
+#pragma unroll 1
+        for (int g = (p >> 5) * 4; g < (p >> 5) * 4 + 4; ++g) {
+          int y[4];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = p + 128 * u;
-        if (j >= kTile * J) break;
-        const int r = chunk_row<FMT>(j, half), q = j - r * J;
-        const int32_t e = rsrc[s * 64 + r];
-        const int64_t ent = row0 + e;
-        if constexpr (FMT == CKV_FMT_BF16) {
-          const int d0 = q * 8;
-          cp_async16(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3),
-                     e >= 0 ? data + ent * 1024 + half * 512 + q * 16 : data, e >= 0 ? 16u : 0u);
-        } else if constexpr (FMT == CKV_FMT_MIXED) {
-          if (e >= 0) {
-            const uint32_t dst = tile + kRawOffMixed + r * (half == 0 ? 256 : 320) + q * 16;
-            if (q < (half == 0 ? 16 : 12)) {
-              cp_async16(dst, data + ent * 576 + half * 256 + q * 16, 16u);
-              const int nblk = 448 / a.nope_block;
-              cp_async4(tile + kScaleOffMixed + (r * 16 + q) * 4,
-                        scale + (ent * nblk + (half * 256 + q * 16) / a.nope_block) * 4);
-            } else {
-              cp_async16(dst, data + ent * 576 + 448 + (q - 12) * 16, 16u);
-            }
+          for (int k = 0; k < 4; ++k) {
+            // an empty row reads the sequence's first row (a valid address)
+            // and is zeroed or skipped by the producers from the mask
+            const int32_t e = rs[4 * g + k];
+            y[k] = (int)(row0 + (e >= 0 ? e : 0));
           }
-        } else {
-          if (e >= 0) {
-            cp_async16(tile + kRawOffFp4 + r * 128 + q * 16, data + ent * 256 + half * 128 + q * 16, 16u);
-            if (q == 0) cp_async16(tile + kScaleOffFp4 + r * 16, scale + ent * 32 + half * 16, 16u);
+          if constexpr (FMT == CKV_FMT_BF16) {
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc)
+              tma_gather4(tile + kc * 8192 + g * 512, gm, half * 256 + kc * 64, y[0], y[1], y[2], y[3],
+                          &bars[B_GFULL + s]);
+          } else if constexpr (FMT == CKV_FMT_MIXED) {
+            tma_gather4(tile + kRawOffMixed + g * 4 * (half == 0 ? 256 : 320), gm + half, half * 128,
+                        y[0], y[1], y[2], y[3], &bars[B_GFULL + s]);
+          } else {
+            tma_gather4(tile + kRawOffFp4 + g * 512, gm, half * 128, y[0], y[1], y[2], y[3],
+                        &bars[B_GFULL + s]);
+            tma_gather4(tile + kScaleOffFp4 + g * 128, gm + 1, half * 16, y[0], y[1], y[2], y[3],
+                        &bars[B_GFULL + s]);   // 128-byte aligned groups of four 16-byte rows
           }
+        }
+      }
+      if constexpr (FMT == CKV_FMT_MIXED) {
+        // row p's scale words for this half (at most 4: nope_block is 448 or 64)
+        if (p < 64 && rs[p] >= 0) {
+          const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
+          const int64_t ent = row0 + rs[p];
+          const int nblk = 448 / a.nope_block, nb0 = (half * 256) / a.nope_block;
+          const int nb1 = (half * 256 + (half == 0 ? 256 : 192) - 1) / a.nope_block;
+          for (int k = 0; k <= nb1 - nb0; ++k)
+            cp_async4(tile + kScaleOffMixed + p * 32 + k * 4, scale + (ent * nblk + nb0 + k) * 4);
         }
       }
       cp_async_commit();
     };
-    auto finish = [&](int i, int newer) {
+    auto finish = [&](int i, int newer) -> bool {
       const int s = i % kStages;
       const uint32_t tile = base + kOffE + s * kEBytes;
+      bool landed = mbar_wait(&bars[B_GFULL + s], (i / kStages) & 1, a.st, abort_p, 35);
       cp_async_wait(newer);                      // this thread's copies of tile i
-      asm volatile("bar.sync 2, 128;" ::: "memory");   // everyone's
-      if constexpr (FMT != CKV_FMT_BF16) {
+      if (!bar_and(2, 128, landed)) return false;   // everyone's
+      if (p == 0 && i < 2) trace(a.st, tr, 51 + i, tr0);   // debug: data landed
+      const bool nb64 = a.nope_block == 64;
+      if constexpr (FMT == CKV_FMT_BF16) {
+        // empty rows: zero their bytes so that P = 0 meets finite values
+        const uint64_t vbits = (uint64_t)vmask_s[s * 2] | ((uint64_t)vmask_s[s * 2 + 1] << 32);
+        if (vbits != ~0ull) {
+          for (int e = p; e < kTile * 32; e += 128) {
+            const int r = e >> 5, cc = e & 31;
+            if (!((vbits >> r) & 1ull))
+              st_shared_v4(sw128(tile + (cc >> 3) * 8192, r, cc & 7), make_uint4(0, 0, 0, 0));
+          }
+        }
+      } else {
         const uint64_t vbits = (uint64_t)vmask_s[s * 2] | ((uint64_t)vmask_s[s * 2 + 1] << 32);
         Raw raw[U];
 #pragma unroll
@@ -552,15 +597,20 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
             if ((vbits >> r) & 1ull) {
               if constexpr (FMT == CKV_FMT_MIXED) {
                 raw[u].v = ld_shared_u4(tile + kRawOffMixed + r * (half == 0 ? 256 : 320) + q * 16);
-                if (q < (half == 0 ? 16 : 12)) raw[u].s = ld_shared_u32(tile + kScaleOffMixed + (r * 16 + q) * 4);
+                if (q < (half == 0 ? 16 : 12)) {
+                  // nope_block is 448 (one scale word) or 64: no division
+                  const int blk = nb64 ? ((half * 256 + q * 16) >> 6) - ((half * 256) >> 6) : 0;
+                  raw[u].s = ld_shared_u32(tile + kScaleOffMixed + r * 32 + blk * 4);
+                }
               } else {
                 raw[u].v = ld_shared_u4(tile + kRawOffFp4 + r * 128 + q * 16);
-                raw[u].s = ld_shared_u16(tile + kScaleOffFp4 + r * 16 + q * 2);
+                raw[u].s = ld_shared_u16(tile + kScaleOffFp4 + (r >> 2) * 128 + (r & 3) * 16 + q * 2);
               }
             }
           }
         }
         asm volatile("bar.sync 2, 128;" ::: "memory");   // raw bytes read: overwrite
+        if (p == 0 && i < 2) trace(a.st, tr, 55 + i, tr0);   // debug: raw read
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int j = p + 128 * u;
@@ -574,6 +624,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       mbar_arrive(&bars[B_EFULL + s]);
       if (p == 0) progress(a.st, prog, 5);
       if (p == 0 && i < 4) trace(a.st, tr, 53 + i, tr0);
+      return true;
     };
     if (!use_tma) {
       // the first kAhead + 1 tiles (free stages): every lookup in one round
@@ -589,10 +640,12 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       int32_t x_next = p < 64 ? raw_index(n_init, p) : -1;   // used one tile later
       asm volatile("bar.sync 2, 128;" ::: "memory");
       for (int t = 0; t < n_init; ++t) copies(t);
-      int issued = n_init;
+      int issued = n_init, finished = 0;
       bool ok = true;
       for (int i = 0; i < n_my && ok; ++i) {
-        finish(i, issued - 1 - i);
+        ok = finish(i, issued - 1 - i);
+        if (!ok) break;
+        finished = i + 1;
         if (issued < n_my) {
           const int t = issued, s = t % kStages;
           ok = t < kStages ||
@@ -609,6 +662,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
       }
       cp_async_wait(0);   // nothing stays in flight past this point
+      if (p == 0 && finished < issued) {
+        // a wait failed: let the gathers already issued land (bounded)
+        // before this CTA can exit
+        volatile int keep_waiting = 0;
+        for (int t = finished; t < issued; ++t)
+          mbar_wait(&bars[B_GFULL + t % kStages], (t / kStages) & 1, a.st, &keep_waiting, 36);
+      }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------ MMA issuer ----
@@ -780,13 +840,15 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       mbar_wait(&bars[B_ODONE], (n_my - 1) & 1, a.st, abort_p, 29);
       tc_fence_after();
     }
-    // this CTA's partial (unnormalised O, m, l) -> workspace, laid out
-    // [16-byte column chunk][head] so that every store and load is coalesced
-    float4* po = reinterpret_cast<float4*>(a.part) +
-                 (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + rank) * (kPartFloats / 4);
-    float4* pw = po + h;
+    // this CTA's partial -> workspace: O / l rounded to fp16 (bounded by the
+    // largest |e|, so fp16's range holds it) and (m, l) in f32, laid out
+    // [8-column chunk][head] so that every store and load is coalesced
+    uint4* po = reinterpret_cast<uint4*>(a.part) +
+                (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + rank) * (kPartFloats / 4);
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    uint4* pw = po + h;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c, pw += 8 * 128) {
+    for (int c = 0; c < 8; ++c, pw += 4 * 128) {
       uint32_t r[32];
       if (n_my > 0) {
         tmem_ld32(tO + c * 32, r);
@@ -796,76 +858,110 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         for (int k = 0; k < 32; ++k) r[k] = 0u;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        __stcg(pw + k * 128, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                         __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
+      for (int k = 0; k < 4; ++k) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * k + 2 * e]) * inv_l,
+                                         __uint_as_float(r[8 * k + 2 * e + 1]) * inv_l);
+          w[e] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        __stcg(pw + k * 128, make_uint4(w[0], w[1], w[2], w[3]));
+      }
     }
-    reinterpret_cast<float2*>(po + 64 * 128)[h] = make_float2(m_used, l);
+    reinterpret_cast<float2*>(po + 32 * 128)[h] = make_float2(m_used, l);
     __threadfence();
   }
   tc_fence_before();
   if (tid == 0) progress(a.st, prog, 6);
   if (tid == 8 * 32) trace(a.st, tr, 57, tr0);   // a softmax thread (h = 64)
+  if (tid == 8 * 32) stamp3(1);
   cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
   if (tid == 0) trace(a.st, tr, 58, tr0);
+  if (tid == 0) stamp3(2);
 
+  // ------------------------------------ merge of the G partials of half c ----
+  // Pair `pair` writes columns [8 u0, 8 u1) of this half (units of 8).  The
+  // softmax warps turn each head row's (m, l) of the G pairs into weights
+  // l_q 2^(m_q - M) / L in shared memory (the tile ring is dead by now);
+  // then all 320 threads combine (row, unit) items with every load of an
+  // item in flight at once.
+  const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
+                     (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
+  constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pairs
+  float* wsm = reinterpret_cast<float*>(gbase + kOffE);   // [kMaxPairs][128] weights
   if (warp >= 6) {
-    // ------------------------------- merge of the G partials of half c ----
-    // pair `pair` writes columns [8 u0, 8 u1) of this half (units of 8)
     const int h = (warp & 3) * 32 + lane;
-    const float4* pq0 = reinterpret_cast<const float4*>(
-        a.part + (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * kPartFloats);
-    constexpr int64_t kPart4 = 2 * kPartFloats / 4;   // float4 stride between pairs
-    float fq[kMaxPairs], wq[kMaxPairs];
+    float mq[kMaxPairs], lq[kMaxPairs];
     float M = -INFINITY;
 #pragma unroll
     for (int q = 0; q < kMaxPairs; ++q) {
-      fq[q] = -INFINITY;
-      wq[q] = 0.f;
+      mq[q] = -INFINITY;
+      lq[q] = 0.f;
       if (q < G) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart4 + 64 * 128) + h);
-        fq[q] = v.x;
-        wq[q] = v.y;
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart16 + 32 * 128) + h);
+        mq[q] = v.x;
+        lq[q] = v.y;
         M = fmaxf(M, v.x);
       }
     }
     float L = 0.f;
 #pragma unroll
     for (int q = 0; q < kMaxPairs; ++q) {
-      const float f = (q >= G || fq[q] == -INFINITY) ? 0.f : exp2f(fq[q] - M);
-      L += wq[q] * f;
-      fq[q] = f;
+      lq[q] = (q >= G || mq[q] == -INFINITY) ? 0.f : lq[q] * exp2f(mq[q] - M);
+      L += lq[q];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxPairs; ++q) wsm[q * 128 + h] = lq[q] * inv;
+    if (rank == 0 && a.lse && h < a.H)
+      a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  {
     const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
-    if (h < a.H) {
-      __nv_bfloat16* out = a.out + ((int64_t)b * a.H + h) * 512 + half * 256;
-      for (int u = u0; u < u1; ++u) {
+    const int n_items = (u1 - u0) * 128;
+#pragma unroll 1
+    for (int k0 = tid; k0 < n_items; k0 += 2 * kThreadsAttn) {
+      // two items per pass, all their loads issued before any use
+      uint4 v[2][kMaxPairs];
+      int hh[2], uu[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int k = k0 + t * kThreadsAttn;
+        hh[t] = k & 127;
+        uu[t] = u0 + (k >> 7);
+#pragma unroll
+        for (int q = 0; q < kMaxPairs; ++q)
+          v[t][q] = (k < n_items && q < G) ? __ldcg(pq0 + q * kPart16 + uu[t] * 128 + hh[t])
+                                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int k = k0 + t * kThreadsAttn;
+        if (k >= n_items || hh[t] >= a.H) continue;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
         for (int q = 0; q < kMaxPairs; ++q) {
-          if (q < G && fq[q] != 0.f) {
-            const float4* src = pq0 + q * kPart4 + (2 * u) * 128 + h;
-            const float4 v0 = __ldcg(src), v1 = __ldcg(src + 128);
-            acc[0] += fq[q] * v0.x;
-            acc[1] += fq[q] * v0.y;
-            acc[2] += fq[q] * v0.z;
-            acc[3] += fq[q] * v0.w;
-            acc[4] += fq[q] * v1.x;
-            acc[5] += fq[q] * v1.y;
-            acc[6] += fq[q] * v1.z;
-            acc[7] += fq[q] * v1.w;
+          if (q < G) {
+            const float wq = wsm[q * 128 + hh[t]];
+            const uint32_t w[4] = {v[t][q].x, v[t][q].y, v[t][q].z, v[t][q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+              acc[2 * e] += wq * f.x;
+              acc[2 * e + 1] += wq * f.y;
+            }
           }
         }
         uint4 o;
-        o.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-        o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-        o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-        o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-        *reinterpret_cast<uint4*>(out + 8 * u) = o;
+        o.x = pack_bf16(acc[0], acc[1]);
+        o.y = pack_bf16(acc[2], acc[3]);
+        o.z = pack_bf16(acc[4], acc[5]);
+        o.w = pack_bf16(acc[6], acc[7]);
+        __nv_bfloat16* out = a.out + ((int64_t)b * a.H + hh[t]) * 512 + half * 256;
+        *reinterpret_cast<uint4*>(out + 8 * uu[t]) = o;
       }
-      if (rank == 0 && a.lse)
-        a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -908,6 +1004,51 @@ bool encode_bf16_rows(CUtensorMap* m, const void* data, int64_t rows) {
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(data), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map of one-row boxes over a plane's rows (`rows` rows of `row_elems`
+// elements of `dt`, contiguous) for TMA gathers of `box_elems` elements.
+bool encode_gather_rows(CUtensorMap* m, const void* data, CUtensorMapDataType dt, int elem_bytes,
+                        int64_t rows, int row_elems, int box_elems, CUtensorMapSwizzle sw) {
+  auto enc = encode_fn_attn();
+  if (!enc || !data || rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_elems, 1};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(data), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The gather maps of one layer: [0, 1] main plane, [2, 3] window plane.
+// BF16: 64-element boxes, 128-byte swizzle (straight into the MMA tile);
+// MIXED: 256- and 320-byte boxes (the two halves' bytes, as 16-bit
+// elements); FP4: 128-byte code boxes and 16-byte scale boxes.
+bool encode_gather_maps(AttnArgs& a, int B) {
+  const uint8_t* data[2] = {a.kv_data, a.win_data};
+  const void* scale[2] = {a.kv_scale, a.win_scale};
+  const int64_t rows[2] = {(int64_t)B * a.kv_cap, (int64_t)B * a.win_cap};
+  for (int k = 0; k < 2; ++k) {
+    CUtensorMap* m = &a.gmap[2 * k];
+    bool ok;
+    if (a.fmt == CKV_FMT_BF16) {
+      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows[k], 512, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+      m[1] = m[0];
+    } else if (a.fmt == CKV_FMT_MIXED) {
+      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, rows[k], 288, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_gather_rows(m + 1, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, rows[k], 288, 160,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows[k], 256, 128,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_gather_rows(m + 1, scale[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows[k], 32, 16,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok) return false;
+  }
+  return true;
 }
 
 }  // namespace
@@ -956,6 +1097,9 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
       encode_bf16_rows(&mk, a0.kv_data, (int64_t)B * a0.kv_cap) &&
       encode_bf16_rows(&mw, a0.win_data, (int64_t)B * a0.win_cap))
     batch.layer[0].use_tma = 1;
+  // every other layer gathers its rows with TMA
+  for (int l = 0; l < n; ++l)
+    if (!batch.layer[l].use_tma && !encode_gather_maps(batch.layer[l], B)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a0.G, B, n);
   cfg.blockDim = dim3(kThreadsAttn, 1, 1);

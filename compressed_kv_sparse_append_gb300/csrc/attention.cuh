@@ -1,14 +1,17 @@
 // Shared declarations of the attention kernels.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (the driver entry point is fetched at run time)
+
 #include "common.cuh"
 
 namespace ckv {
 
 constexpr int kMaxTopk = 2048;    // selected rows held per sequence
 constexpr int kMaxHeads = 128;    // query heads (one 128-row MMA tile)
-// Floats of one CTA's partial: O [64 column chunks][128 heads][4] + (m, l) [128].
-constexpr int64_t kPartFloats = 64 * 128 * 4 + 128 * 2;
+// One CTA's partial, in 4-byte words: O / l as fp16 [32 chunks of 8 columns]
+// [128 heads] (16 bytes each), then (m, l) as f32 pairs [128].
+constexpr int64_t kPartFloats = 32 * 128 * 4 + 128 * 2;
 
 struct AttnArgs {
   const uint8_t* kv_data;
@@ -29,10 +32,11 @@ struct AttnArgs {
   __nv_bfloat16* out;     // [B][H][512]
   float* lse;             // [B][H] or null
   int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
-  float* part;            // workspace: [layer][B][2G][kPartFloats] partial O, m, l
+  float* part;            // workspace: [layer][B][2G][kPartFloats] partial O / l, m, l
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   int progress;           // debugging: count pipeline events in the status block
   DevStatus* st;
+  CUtensorMap gmap[4];    // set by the launcher: row-gather maps (main, window)
 };
 
 constexpr int kMaxLayers = 8;

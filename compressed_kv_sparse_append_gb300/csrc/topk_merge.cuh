@@ -76,9 +76,24 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
 
   // (a) the histogram into shared memory (and zeroed for the next call)
   uint32_t* hs = surv_key;
-  for (int v = threadIdx.x; v < kHistBins / 4; v += NT) {
-    reinterpret_cast<uint4*>(hs)[v] = __ldcg(reinterpret_cast<const uint4*>(hist) + v);
-    reinterpret_cast<uint4*>(hist)[v] = make_uint4(0u, 0u, 0u, 0u);
+  {
+    // every load in flight before any store (the zeroing stores would
+    // otherwise order each load after the previous one)
+    constexpr int kV = kHistBins / 4, kPerT = (kV + NT - 1) / NT;
+    uint4 hv[kPerT];
+#pragma unroll
+    for (int k = 0; k < kPerT; ++k) {
+      const int v = threadIdx.x + k * NT;
+      hv[k] = v < kV ? __ldcg(reinterpret_cast<const uint4*>(hist) + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < kPerT; ++k) {
+      const int v = threadIdx.x + k * NT;
+      if (v < kV) {
+        reinterpret_cast<uint4*>(hs)[v] = hv[k];
+        reinterpret_cast<uint4*>(hist)[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
   }
   __syncthreads();
   constexpr int per = (kHistBins + NT - 1) / NT;   // descending bins, contiguous per thread

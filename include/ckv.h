@@ -88,8 +88,8 @@ typedef struct ckv_plane {
 /* Workspace sizing.  `op` is one of CKV_OP_*; unused arguments may be 0.
  * The attention ops (CKV_OP_SPARSE_ATTN, CKV_OP_HCA_ATTN, and CKV_OP_CSA2
  * for each of its up to CKV_CSA2_MAX_LAYERS layers) keep one partial
- * (unnormalised output, running max and sum) per CTA of a sequence in the
- * workspace for the final merge: about 2.1 MB per sequence and layer. */
+ * (output normalised by its own row sum, running max and sum) per CTA of a sequence in the
+ * workspace for the final merge: about 1.1 MB per sequence and layer. */
 #define CKV_OP_APPEND      0
 #define CKV_OP_INDEX_TOPK  1
 #define CKV_OP_SPARSE_ATTN 2

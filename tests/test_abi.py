@@ -49,7 +49,7 @@ def test_workspace_sizes(lib):
     assert 256 < a < b
     assert f(1, 8, 64, 64, 65536, 512, 2048) > f(1, 8, 64, 64, 65536, 512, 0)
     # attention: status word + the merge partials of up to 16 CTAs per sequence
-    part = 16 * (64 * 128 * 4 + 256) * 4
+    part = 16 * (32 * 128 * 4 + 256) * 4
     assert f(2, 3, 128, 0, 0, 0, 0) == 256 + 3 * part
     assert f(3, 3, 128, 0, 0, 0, 0) == 256 + 3 * part
     assert f(4, 8, 64, 64, 65536, 512, 2048) % 256 == 0
