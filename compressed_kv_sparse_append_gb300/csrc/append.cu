@@ -39,6 +39,8 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* p, float (&v)[
 }
 
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 4 + warp;
   if (row >= a.n) return;
@@ -146,8 +148,14 @@ cudaError_t launch_append(const ckv_plane& p, const void* src, const int64_t* sl
   a.dim = p.dim;
   a.nope_block = p.nope_block;
   a.st = st;
-  append_kernel<<<(n + 3) / 4, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1] = {pdl_attribute()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_kernel, a);
 }
 
 }  // namespace ckv

@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
                 const __grid_constant__ AttnBatch batch) {
   const AttnArgs& a = batch.layer[blockIdx.z];
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -879,6 +880,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
   if (tid == 0) trace(a.st, tr, 58, tr0);
   if (tid == 0) stamp3(2);
+  pdl_launch_dependents();
 
   // ------------------------------------ merge of the G partials of half c ----
   // Pair `pair` writes columns [8 u0, 8 u1) of this half (units of 8).  The
@@ -1105,13 +1107,14 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   cfg.blockDim = dim3(kThreadsAttn, 1, 1);
   cfg.dynamicSmemBytes = kSmemAttn;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2 * a0.G;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1] = pdl_attribute();
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, mk, mw, batch);
 }
 

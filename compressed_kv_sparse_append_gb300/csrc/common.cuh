@@ -155,6 +155,26 @@ __device__ __forceinline__ void trace_at(DevStatus* st, bool on, int slot, long 
   if (on && st != nullptr && slot >= 0 && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
 }
 
+// Launch attribute for programmatic stream serialisation (host side).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  return at;
+}
+
+// -------------------------------------- programmatic dependent launch ----
+// Every kernel is launched with programmatic stream serialisation, so it may
+// start while the previous kernel in the stream is finishing.  pdl_wait()
+// blocks until the grids this one depends on have completed and their
+// memory operations are visible; each kernel calls it before it reads or
+// writes anything in global memory.  pdl_launch_dependents() lets the next
+// kernel begin launching (it still waits in its own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- fences ----
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

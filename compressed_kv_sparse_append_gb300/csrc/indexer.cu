@@ -36,8 +36,7 @@ struct IndexSmem {
 // quantised with the E2M1 + E4M3/16 block quantiser (the same arithmetic as
 // the append path) and its exact values stored; BF16 keys -> the BF16 values.
 __device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
-  const int t = threadIdx.x;
-  if (t < a.HI * 8) {
+  for (int t = threadIdx.x; t < a.HI * 8; t += kIdxThreads) {
     const int h = t >> 3, blk = t & 7;
     const __nv_bfloat16* src = a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
@@ -60,29 +59,49 @@ __device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) q[h * kIdxDim + blk * 16 + i] = v[i];
   }
-  if (t < a.HI) w[t] = a.w[(int64_t)b * a.HI + t];
+  for (int t = threadIdx.x; t < a.HI; t += kIdxThreads) w[t] = a.w[(int64_t)b * a.HI + t];
 }
 
+// Score of one key, block by block (16 channels); block blk + 1's bytes are
+// loaded while block blk is multiplied, so one memory round trip per key is
+// exposed rather than one per block.
 __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t entry,
                                             const float* q, const float* w) {
   float acc[kMaxHI];
 #pragma unroll
   for (int h = 0; h < kMaxHI; ++h) acc[h] = 0.f;
   const int64_t row = (int64_t)b * a.cap + entry;
-#pragma unroll 1
-  for (int blk = 0; blk < 8; ++blk) {
-    float kv[16];
-    if (a.fmt == CKV_FMT_FP4) {
+  const bool fp4 = a.fmt == CKV_FMT_FP4;
+  auto fetch = [&](int blk, uint4& x0, uint4& x1, uint32_t& sc) {
+    if (fp4) {
       const uint2 d = *reinterpret_cast<const uint2*>(a.kdata + row * 64 + blk * 8);
-      const float s = e4m3_value(a.kscale[row * 8 + blk]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        kv[i] = e2m1_value((d.x >> (4 * i)) & 0xF) * s;
-        kv[8 + i] = e2m1_value((d.y >> (4 * i)) & 0xF) * s;
-      }
+      x0 = make_uint4(d.x, d.y, 0u, 0u);
+      x1 = make_uint4(0u, 0u, 0u, 0u);
+      sc = a.kscale[row * 8 + blk];
     } else {
       const uint4* p = reinterpret_cast<const uint4*>(a.kdata + row * 256 + blk * 32);
-      const uint4 x0 = p[0], x1 = p[1];
+      x0 = p[0];
+      x1 = p[1];
+      sc = 0u;
+    }
+  };
+  uint4 n0, n1;
+  uint32_t ns;
+  fetch(0, n0, n1, ns);
+#pragma unroll 1
+  for (int blk = 0; blk < 8; ++blk) {
+    const uint4 x0 = n0, x1 = n1;
+    const uint32_t xs = ns;
+    if (blk + 1 < 8) fetch(blk + 1, n0, n1, ns);
+    float kv[16];
+    if (fp4) {
+      const float s = e4m3_value((uint8_t)xs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        kv[i] = e2m1_value((x0.x >> (4 * i)) & 0xF) * s;
+        kv[8 + i] = e2m1_value((x0.y >> (4 * i)) & 0xF) * s;
+      }
+    } else {
       const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -117,6 +136,7 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
 __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   IndexSmem& sm = *reinterpret_cast<IndexSmem*>(smem_raw);
+  pdl_wait();
   const int b = blockIdx.y, chunk = blockIdx.x;
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
   load_query(a, b, sm.q, sm.w);
@@ -166,9 +186,15 @@ cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(a.n_chunks, a.B);
-  index_topk_simt_kernel<<<grid, kIdxThreads, sizeof(IndexSmem), stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_chunks, a.B);
+  cfg.blockDim = dim3(kIdxThreads);
+  cfg.dynamicSmemBytes = sizeof(IndexSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1] = {pdl_attribute()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, index_topk_simt_kernel, a);
 }
 
 }  // namespace ckv

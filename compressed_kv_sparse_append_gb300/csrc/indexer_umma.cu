@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   MergeSmem<kUThreads>& msm = *reinterpret_cast<MergeSmem<kUThreads>*>(g + kOffMerge);
   __shared__ int abort_flag;
 
+  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y, chunk = blockIdx.x;
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
@@ -340,9 +341,15 @@ cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream
   UmmaIndexArgs ua;
   ua.a = a;
   ua.row_limit = batch_rows;
-  dim3 grid(a.n_chunks, a.B);
-  index_topk_umma_kernel<<<grid, kUThreads, kSmemU, stream>>>(md, ms, ua);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_chunks, a.B);
+  cfg.blockDim = dim3(kUThreads);
+  cfg.dynamicSmemBytes = kSmemU;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1] = {pdl_attribute()};
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, index_topk_umma_kernel, md, ms, ua);
 }
 
 }  // namespace ckv

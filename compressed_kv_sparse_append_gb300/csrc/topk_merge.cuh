@@ -233,6 +233,7 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   __threadfence();
   __syncthreads();
   trace_at(a.st, tr, 11, t0);
+  pdl_launch_dependents();   // the next kernel may take the SMs this grid frees
   if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(a.counters + b, 1u);
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
