@@ -167,23 +167,40 @@ size_t index_ws_bytes(int B, int n_comp_max, int K_sel, bool pool_mode, int pool
   return index_layout(B, n_comp_max, K_sel, pool_mode, pool_len).bytes;
 }
 
-// Partials of the attention's split-KV merge: up to 2 * kMaxPairs CTAs per
-// sequence and layer, kPartFloats floats each.
+// The attention's split-KV merge state: the partials of up to 2 * kMaxPairs
+// CTAs per sequence and layer (kPartFloats floats each), then one counter per
+// sequence, layer and half (the merge ticket).
 size_t attn_part_bytes(int B, int layers) {
   return align_up((size_t)layers * B * 2 * kMaxPairs * kPartFloats * sizeof(float), 256);
 }
+size_t attn_ws_bytes(int B, int layers) {
+  return attn_part_bytes(B, layers) + align_up((size_t)layers * B * 2 * sizeof(uint32_t), 256);
+}
+void attn_set_ws(AttnArgs& a, uint8_t* region, int B, int layers) {
+  a.part = reinterpret_cast<float*>(region);
+  a.tickets = reinterpret_cast<uint32_t*>(region + attn_part_bytes(B, layers));
+}
 
-// Picks the number of CTA pairs per sequence (cluster of 2G CTAs): the
-// largest G that leaves each pair at least two 64-row tiles and lets all
-// `n_clusters` clusters be resident at once (one wave).
-int choose_pairs(int n_clusters, int n_rows_max) {
+// Picks the number of CTA pairs per sequence and the cluster shape.  Every
+// pair of the launch (n_seq sequence-layers x G) must be resident at once and
+// each pair keeps at least two 64-row tiles.  A cluster of all 2G CTAs of a
+// sequence merges through a hardware-scheduled cluster barrier; pair clusters
+// merge through a counter in the workspace but fit more pairs on the GPU, so
+// they are taken only when they allow a larger G.
+struct PairChoice {
+  int G;
+  int cluster_all;
+};
+PairChoice choose_pairs(int n_seq, int n_rows_max) {
   const int tiles = (n_rows_max + 63) / 64;
-  int best = 1;
+  int g_all = 1, g_pair = 1;
+  const int fit2 = attn_max_active_clusters(2);
   for (int G = 2; G <= kMaxPairs && tiles >= 2 * G; ++G) {
     const int fit = attn_max_active_clusters(2 * G);
-    if (fit > 0 && n_clusters <= fit) best = G;
+    if (fit > 0 && n_seq <= fit) g_all = G;
+    if (fit2 > 0 && n_seq * G <= fit2) g_pair = G;
   }
-  return best;
+  return g_pair > g_all ? PairChoice{g_pair, 0} : PairChoice{g_all, 1};
 }
 
 ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
@@ -222,7 +239,9 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.G = 1;
+  a.cluster_all = 1;
   a.part = nullptr;
+  a.tickets = nullptr;
   a.st = st;
   a.use_tma = 0;
   const char* pe = getenv("CKV_DEBUG_PROGRESS");
@@ -251,11 +270,11 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t
       size_t idx_region = align_up(full > re ? full : re, 256);
       size_t pool = align_up((size_t)B * (pool_len > 0 ? pool_len : 1) * 4, 256);
       size_t idxbuf = align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256);
-      return kStatusBytes + idx_region + pool + idxbuf + attn_part_bytes(B, CKV_CSA2_MAX_LAYERS);
+      return kStatusBytes + idx_region + pool + idxbuf + attn_ws_bytes(B, CKV_CSA2_MAX_LAYERS);
     }
     case CKV_OP_SPARSE_ATTN:
     case CKV_OP_HCA_ATTN:
-      return kStatusBytes + attn_part_bytes(B, 1);
+      return kStatusBytes + attn_ws_bytes(B, 1);
     default:
       return kStatusBytes;
   }
@@ -302,14 +321,16 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
   if (s) return s;
   if (!idx || topk <= 0) return CKV_ERR_INVALID;
   if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
-  s = check_ws(ws, ws_bytes, kStatusBytes + attn_part_bytes(B, 1));
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_ws_bytes(B, 1));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
-  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  attn_set_ws(a, static_cast<uint8_t*>(ws) + kStatusBytes, B, 1);
   a.idx = idx;
   a.topk = topk;
-  a.G = choose_pairs(B, topk + (int)win->cap);
+  const PairChoice pc = choose_pairs(B, topk + (int)win->cap);
+  a.G = pc.G;
+  a.cluster_all = pc.cluster_all;
   return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
 }
 
@@ -320,14 +341,16 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!n_comp || n_comp_max < 0 || n_comp_max > kv->cap) return CKV_ERR_INVALID;
-  s = check_ws(ws, ws_bytes, kStatusBytes + attn_part_bytes(B, 1));
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_ws_bytes(B, 1));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
-  a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kStatusBytes);
+  attn_set_ws(a, static_cast<uint8_t*>(ws) + kStatusBytes, B, 1);
   a.n_comp = n_comp;
   a.n_comp_max = n_comp_max;
-  a.G = choose_pairs(B, n_comp_max + (int)win->cap);
+  const PairChoice pc = choose_pairs(B, n_comp_max + (int)win->cap);
+  a.G = pc.G;
+  a.cluster_all = pc.cluster_all;
   return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
 }
 
@@ -383,9 +406,8 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   uint8_t* idx_region = w8 + kStatusBytes;
   int32_t* pool_buf = reinterpret_cast<int32_t*>(idx_region + align_up(full > re ? full : re, 256));
   int32_t* idxbuf = pool_buf + align_up((size_t)B * pool_len * 4, 256) / 4;
-  float* part = reinterpret_cast<float*>(
-      reinterpret_cast<uint8_t*>(idxbuf) +
-      align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256));
+  uint8_t* attn_region = reinterpret_cast<uint8_t*>(idxbuf) +
+                         align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256);
 
   if (n_append > 0) {
     s = cuda_status(launch_append(*append_dst, append_src_bf16, append_slot, n_append, dst, st));
@@ -412,18 +434,21 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   }
   // every layer's attention in one launch (grid z = layer)
   AttnArgs la[CKV_CSA2_MAX_LAYERS];
-  int G = 4;
+  // one shape for the whole launch: the tightest layer decides
+  int rows_max = 0;
   for (int l = 0; l < L; ++l) {
-    const int gl = choose_pairs(B * L, topk + (int)g->win[g->kv_src[l]].cap);
-    G = G < gl ? G : gl;
+    const int r = topk + (int)g->win[g->kv_src[l]].cap;
+    rows_max = rows_max > r ? rows_max : r;
   }
+  const PairChoice pc = choose_pairs(B * L, rows_max);
   for (int l = 0; l < L; ++l) {
     const int k = g->kv_src[l];
     la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
     la[l].idx = layer_idx[l];
     la[l].topk = topk;
-    la[l].G = G;
-    la[l].part = part;   // one region for all layers, indexed by layer inside
+    la[l].G = pc.G;
+    la[l].cluster_all = pc.cluster_all;
+    attn_set_ws(la[l], attn_region, B, CKV_CSA2_MAX_LAYERS);   // indexed by layer inside
   }
   return cuda_status(launch_attention_layers(la, L, B, st));
 }

@@ -132,6 +132,56 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pairs' partials
+
+// Combines the G partials of one half over units [u0, u1) of 8 columns x 128
+// head rows with the weights in `wsm`; each pass keeps 16 / GMAX items x G
+// loads of 16 bytes in flight per thread.
+template <int GMAX>
+__device__ __forceinline__ void merge_items(const uint4* pq0, const float* wsm, int G, int H,
+                                            __nv_bfloat16* out, int tid, int u0, int u1) {
+  constexpr int kItems = 16 / GMAX;
+  const int n_items = (u1 - u0) * H;   // only the H real head rows
+#pragma unroll 1
+  for (int k0 = tid; k0 < n_items; k0 += kItems * kThreadsAttn) {
+    uint4 v[kItems][GMAX];
+#pragma unroll
+    for (int t = 0; t < kItems; ++t) {
+      const int k = k0 + t * kThreadsAttn, uu = u0 + k / H, hh = k - (uu - u0) * H;
+#pragma unroll
+      for (int q = 0; q < GMAX; ++q)
+        v[t][q] = (k < n_items && q < G) ? __ldcg(pq0 + q * kPart16 + uu * 128 + hh)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int t = 0; t < kItems; ++t) {
+      const int k = k0 + t * kThreadsAttn, uu = u0 + k / H, hh = k - (uu - u0) * H;
+      if (k >= n_items) continue;
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int q = 0; q < GMAX; ++q) {
+        if (q < G) {
+          const float wq = wsm[q * 128 + hh];
+          const uint32_t w[4] = {v[t][q].x, v[t][q].y, v[t][q].z, v[t][q].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+            acc[2 * e] += wq * f.x;
+            acc[2 * e + 1] += wq * f.y;
+          }
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16(acc[0], acc[1]);
+      o.y = pack_bf16(acc[2], acc[3]);
+      o.z = pack_bf16(acc[4], acc[5]);
+      o.w = pack_bf16(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + (int64_t)hh * 512 + 8 * uu) = o;
+    }
+  }
+}
+
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -308,8 +358,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // A cluster is either one pair or all 2G CTAs of the sequence
+  // (a.cluster_all); either way CTA x of the sequence is pair x / 2, half
+  // x % 2, and its peer is the adjacent cluster rank.
   const uint32_t rank = cluster_ctarank();
-  const int pair = (int)(rank >> 1), half = (int)(rank & 1);
+  const int pair = (int)(blockIdx.x >> 1), half = (int)(blockIdx.x & 1);
   const uint32_t peer = rank ^ 1u;
   const int b = blockIdx.y;
   const int G = a.G;
@@ -339,8 +392,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     mbar_init(&bars[B_XREAD + 1], 128);
     for (int k = 0; k < kStages; ++k) mbar_init(&bars[B_GFULL + k], 1);
     mbar_init(&bars[B_ODONE], 1);
-    mbar_init(&bars[B_CLUSTER], 2 * G);
-    mbar_init(&bars[B_CLUSTER + 1], 2 * G);
+    mbar_init(&bars[B_CLUSTER], a.cluster_all ? 2 * a.G : 2);
+    mbar_init(&bars[B_CLUSTER + 1], a.cluster_all ? 2 * a.G : 2);
     fence_mbar_init();
   }
   if (warp == 5) tmem_alloc(tslot, kTmemCols);
@@ -354,9 +407,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const long long tr0 = clock64();
   // progress mode 3: the CTAs of sequence 0 (layer 0) store %globaltimer
   // (low 32 bits) at start, softmax end and cluster-barrier exit
-  const bool tr3 = a.progress == 3 && blockIdx.y == 0 && blockIdx.z == 0 && rank < 16;
+  const bool tr3 = a.progress == 3 && blockIdx.y == 0 && blockIdx.z == 0 && blockIdx.x < 12;
   auto stamp3 = [&](int k) {
-    if (tr3) a.st->pad[3 * rank + k] = (int32_t)(uint32_t)globaltimer();
+    if (tr3) a.st->pad[4 * blockIdx.x + k] = (int32_t)(uint32_t)globaltimer();
   };
   if (tid == 0) stamp3(0);
   if (tid == 0) progress(a.st, prog, 0);
@@ -845,7 +898,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     // largest |e|, so fp16's range holds it) and (m, l) in f32, laid out
     // [8-column chunk][head] so that every store and load is coalesced
     uint4* po = reinterpret_cast<uint4*>(a.part) +
-                (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + rank) * (kPartFloats / 4);
+                (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + blockIdx.x) * (kPartFloats / 4);
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     uint4* pw = po + h;
 #pragma unroll 1
@@ -877,98 +930,86 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   if (tid == 0) progress(a.st, prog, 6);
   if (tid == 8 * 32) trace(a.st, tr, 57, tr0);   // a softmax thread (h = 64)
   if (tid == 8 * 32) stamp3(1);
-  cluster_barrier(&bars[B_CLUSTER], 2 * G, a.st, abort_p, 30);
+  // The cluster meets once more: no CTA exits while another may still touch
+  // its shared memory, and with a sequence-wide cluster every partial of the
+  // sequence is written once it is through.
+  cluster_barrier(&bars[B_CLUSTER], a.cluster_all ? 2 * a.G : 2, a.st, abort_p, 30);
   if (tid == 0) trace(a.st, tr, 58, tr0);
-  if (tid == 0) stamp3(2);
   pdl_launch_dependents();
 
   // ------------------------------------ merge of the G partials of half c ----
-  // Pair `pair` writes columns [8 u0, 8 u1) of this half (units of 8).  The
-  // softmax warps turn each head row's (m, l) of the G pairs into weights
-  // l_q 2^(m_q - M) / L in shared memory (the tile ring is dead by now);
-  // then all 320 threads combine (row, unit) items with every load of an
-  // item in flight at once.
-  const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
-                     (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
-  constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pairs
-  float* wsm = reinterpret_cast<float*>(gbase + kOffE);   // [kMaxPairs][128] weights
-  if (warp >= 6) {
-    const int h = (warp & 3) * 32 + lane;
-    float mq[kMaxPairs], lq[kMaxPairs];
-    float M = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < kMaxPairs; ++q) {
-      mq[q] = -INFINITY;
-      lq[q] = 0.f;
-      if (q < G) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart16 + 32 * 128) + h);
-        mq[q] = v.x;
-        lq[q] = v.y;
-        M = fmaxf(M, v.x);
+  // With pair clusters, every CTA of the sequence (2G, all resident: the
+  // launcher sizes the grid to fit the GPU) counts itself in once its
+  // partial is written and waits (bounded) for the others.  Then pair `pair`
+  // merges units [u0, u1) of 8
+  // columns of its half: each head row's (m, l) of the G pairs become weights
+  // l_q 2^(m_q - M) / L in shared memory (the tile ring is dead by now), and
+  // all 320 threads combine (row, unit) items, 16 loads in flight each.
+  uint32_t* cnt = a.tickets + ((int64_t)blockIdx.z * gridDim.y + b) * 2;
+  if (tid == 0 && !a.cluster_all) {
+    __threadfence();
+    atomicAdd(cnt, 1u);
+    const uint64_t g0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= (uint32_t)(2 * G)) break;
+      if (*abort_p || it >= kWaitLimitIters || globaltimer() - g0 > kWaitLimitNs) {
+        report(a.st, CKV_ERR_TIMEOUT, 31);
+        *abort_p = 1;
+        break;
       }
+      __nanosleep(64);
     }
-    float L = 0.f;
-#pragma unroll
-    for (int q = 0; q < kMaxPairs; ++q) {
-      lq[q] = (q >= G || mq[q] == -INFINITY) ? 0.f : lq[q] * exp2f(mq[q] - M);
-      L += lq[q];
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int q = 0; q < kMaxPairs; ++q) wsm[q * 128 + h] = lq[q] * inv;
-    if (rank == 0 && a.lse && h < a.H)
-      a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  {
-    const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
-    const int n_items = (u1 - u0) * 128;
-#pragma unroll 1
-    for (int k0 = tid; k0 < n_items; k0 += 2 * kThreadsAttn) {
-      // two items per pass, all their loads issued before any use
-      uint4 v[2][kMaxPairs];
-      int hh[2], uu[2];
+  if (tid == 0) stamp3(2);
+  if (!*abort_p) {
+    const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
+                       (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
+    float* wsm = reinterpret_cast<float*>(gbase + kOffE);   // [kMaxPairs][128] weights
+    if (warp >= 6) {
+      const int h = (warp & 3) * 32 + lane;
+      float mq[kMaxPairs], lq[kMaxPairs];
+      float M = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int k = k0 + t * kThreadsAttn;
-        hh[t] = k & 127;
-        uu[t] = u0 + (k >> 7);
-#pragma unroll
-        for (int q = 0; q < kMaxPairs; ++q)
-          v[t][q] = (k < n_items && q < G) ? __ldcg(pq0 + q * kPart16 + uu[t] * 128 + hh[t])
-                                          : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int k = k0 + t * kThreadsAttn;
-        if (k >= n_items || hh[t] >= a.H) continue;
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-        for (int q = 0; q < kMaxPairs; ++q) {
-          if (q < G) {
-            const float wq = wsm[q * 128 + hh[t]];
-            const uint32_t w[4] = {v[t][q].x, v[t][q].y, v[t][q].z, v[t][q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-              acc[2 * e] += wq * f.x;
-              acc[2 * e + 1] += wq * f.y;
-            }
-          }
+      for (int q = 0; q < kMaxPairs; ++q) {
+        mq[q] = -INFINITY;
+        lq[q] = 0.f;
+        if (q < G) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart16 + 32 * 128) + h);
+          mq[q] = v.x;
+          lq[q] = v.y;
+          M = fmaxf(M, v.x);
         }
-        uint4 o;
-        o.x = pack_bf16(acc[0], acc[1]);
-        o.y = pack_bf16(acc[2], acc[3]);
-        o.z = pack_bf16(acc[4], acc[5]);
-        o.w = pack_bf16(acc[6], acc[7]);
-        __nv_bfloat16* out = a.out + ((int64_t)b * a.H + hh[t]) * 512 + half * 256;
-        *reinterpret_cast<uint4*>(out + 8 * uu[t]) = o;
       }
+      float L = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxPairs; ++q) {
+        lq[q] = (q >= G || mq[q] == -INFINITY) ? 0.f : lq[q] * exp2f(mq[q] - M);
+        L += lq[q];
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxPairs; ++q) wsm[q * 128 + h] = lq[q] * inv;
+      if (blockIdx.x == 0 && a.lse && h < a.H)
+        a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
+    __syncthreads();
+    __nv_bfloat16* out = a.out + (int64_t)b * a.H * 512 + half * 256;
+    const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
+    if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1);
+    else if (G <= 4) merge_items<4>(pq0, wsm, G, a.H, out, tid, u0, u1);
+    else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1);
+  }
+  // the last CTA of the sequence to leave resets the counters for the next call
+  __syncthreads();
+  if (tid == 0) stamp3(3);
+  if (tid == 0 && !a.cluster_all && atomicAdd(cnt + 1, 1u) == (uint32_t)(2 * G - 1)) {
+    cnt[0] = 0u;
+    cnt[1] = 0u;
   }
 
-  // every DSMEM transfer into this CTA completed before the cluster barrier
-  // and the partials live in global memory, so no second barrier is needed
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
@@ -1081,7 +1122,8 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   if (n < 1 || n > kMaxLayers) return cudaErrorInvalidValue;
   const AttnArgs& a0 = layers[0];
   for (int l = 1; l < n; ++l)
-    if (layers[l].fmt != a0.fmt || layers[l].G != a0.G) return cudaErrorInvalidValue;
+    if (layers[l].fmt != a0.fmt || layers[l].G != a0.G || layers[l].cluster_all != a0.cluster_all)
+      return cudaErrorInvalidValue;
   const AttnKernelFn kern = attn_kernel_for(a0.fmt);
   if (!kern) return cudaErrorInvalidValue;
   AttnBatch batch;
@@ -1109,7 +1151,7 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * a0.G;
+  attr[0].val.clusterDim.x = a0.cluster_all ? 2 * a0.G : 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1] = pdl_attribute();

@@ -31,8 +31,10 @@ struct AttnArgs {
   float scale_log2;       // sm_scale * log2(e)
   __nv_bfloat16* out;     // [B][H][512]
   float* lse;             // [B][H] or null
-  int G;                  // CTA pairs per sequence (cluster = 2G CTAs)
+  int G;                  // CTA pairs per sequence
+  int cluster_all;        // 1: one cluster of 2G CTAs per sequence; 0: one per pair
   float* part;            // workspace: [layer][B][2G][kPartFloats] partial O / l, m, l
+  uint32_t* tickets;      // workspace: [layer][B][2] finished-CTA counters (start at 0)
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   int progress;           // debugging: count pipeline events in the status block
   DevStatus* st;
@@ -40,7 +42,7 @@ struct AttnArgs {
 };
 
 constexpr int kMaxLayers = 8;
-constexpr int kMaxPairs = 8;      // CTA pairs per sequence (clusters of up to 16 CTAs)
+constexpr int kMaxPairs = 8;      // CTA pairs per sequence
 struct AttnBatch {
   AttnArgs layer[kMaxLayers];  // one launch runs every layer (grid z = layer)
 };

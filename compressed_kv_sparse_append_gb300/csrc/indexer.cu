@@ -138,10 +138,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
   IndexSmem& sm = *reinterpret_cast<IndexSmem*>(smem_raw);
   pdl_wait();
   const int b = blockIdx.y, chunk = blockIdx.x;
+  const bool tr = a.trace && b == 0 && chunk == 0 && threadIdx.x == 0;
+  const long long t0 = clock64();
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
   load_query(a, b, sm.q, sm.w);
   if (threadIdx.x == 0) sm.m.n_real = 0;
   __syncthreads();
+  trace_at(a.st, tr, 0, t0);
 
   int n_elem;
   int64_t first = 0;
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
   }
   atomicAdd(&sm.m.n_real, mine);
   __syncthreads();
+  trace_at(a.st, tr, 9, t0);
   chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.keys, kMaxChunk / 2,
                                       sm.m);
 }

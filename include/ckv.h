@@ -89,7 +89,9 @@ typedef struct ckv_plane {
  * The attention ops (CKV_OP_SPARSE_ATTN, CKV_OP_HCA_ATTN, and CKV_OP_CSA2
  * for each of its up to CKV_CSA2_MAX_LAYERS layers) keep one partial
  * (output normalised by its own row sum, running max and sum) per CTA of a sequence in the
- * workspace for the final merge: about 1.1 MB per sequence and layer. */
+ * workspace for the final merge, plus one counter per sequence, layer and
+ * half that elects the CTA doing the merge: about 1.1 MB per sequence and
+ * layer. */
 #define CKV_OP_APPEND      0
 #define CKV_OP_INDEX_TOPK  1
 #define CKV_OP_SPARSE_ATTN 2
