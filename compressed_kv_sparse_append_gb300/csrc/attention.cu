@@ -348,7 +348,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
                 const __grid_constant__ AttnBatch batch) {
   const AttnArgs& a = batch.layer[blockIdx.z];
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -367,14 +366,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const int b = blockIdx.y;
   const int G = a.G;
   const bool use_tma = a.use_tma != 0;
-
-  const int n_sel = a.idx ? a.topk : max(0, min(a.n_comp[b], a.n_comp_max));
-  const int n_win = max(0, min(a.win_len[b], (int)a.win_cap));
-  const int nt_main = (n_sel + kTile - 1) / kTile;
-  const int n_tiles = nt_main + (n_win + kTile - 1) / kTile;
-  const int t0 = (int)((int64_t)pair * n_tiles / G), t1 = (int)((int64_t)(pair + 1) * n_tiles / G);
-  const int n_my = t1 - t0;
-  const int32_t* idx_b = a.idx ? a.idx + (int64_t)b * a.topk : nullptr;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -401,6 +392,17 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // Everything above touches only this CTA's own resources; global memory
+  // (inputs included) only after the previous kernel in the stream is done.
+  pdl_wait();
+  const int n_sel = a.idx ? a.topk : max(0, min(a.n_comp[b], a.n_comp_max));
+  const int n_win = max(0, min(a.win_len[b], (int)a.win_cap));
+  const int nt_main = (n_sel + kTile - 1) / kTile;
+  const int n_tiles = nt_main + (n_win + kTile - 1) / kTile;
+  const int t0 = (int)((int64_t)pair * n_tiles / G), t1 = (int)((int64_t)(pair + 1) * n_tiles / G);
+  const int n_my = t1 - t0;
+  const int32_t* idx_b = a.idx ? a.idx + (int64_t)b * a.topk : nullptr;
+
   volatile int* abort_p = &abort_flag;
   const bool prog = a.progress == 1;
   const bool tr = a.progress == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;

@@ -92,8 +92,24 @@ __global__ void __launch_bounds__(kUThreads, 1)
   MergeSmem<kUThreads>& msm = *reinterpret_cast<MergeSmem<kUThreads>*>(g + kOffMerge);
   __shared__ int abort_flag;
 
-  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // barriers and TMEM first: they touch only this CTA's own resources; global
+  // memory (inputs included) only after the previous kernel is done
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(&bars[BU_FULL + s], 1);
+      mbar_init(&bars[BU_EMPTY + s], 1);
+      mbar_init(&bars[BU_SFA + s], 128);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&bars[BU_DFULL + d], 1);
+      mbar_init(&bars[BU_DEMPTY + d], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tslot, kTmemU);
+  pdl_wait();
   const int b = blockIdx.y, chunk = blockIdx.x;
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
   const int64_t c0 = (int64_t)chunk * a.chunk;
@@ -137,20 +153,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
     }
   }
   if (tid < 64) wsm[tid] = tid < a.HI ? a.w[(int64_t)b * a.HI + tid] : 0.f;
-  if (tid == 0) {
-    abort_flag = 0;
-    for (int s = 0; s < kUStages; ++s) {
-      mbar_init(&bars[BU_FULL + s], 1);
-      mbar_init(&bars[BU_EMPTY + s], 1);
-      mbar_init(&bars[BU_SFA + s], 128);
-    }
-    for (int d = 0; d < 2; ++d) {
-      mbar_init(&bars[BU_DFULL + d], 1);
-      mbar_init(&bars[BU_DEMPTY + d], 128);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) tmem_alloc(tslot, kTmemU);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
