@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--workload", default="csa_128k")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--graph", action="store_true",
+                   help="time replays of a CUDA graph of the step (off by default: see DESIGN.md)")
     return p.parse_args()
 
 
@@ -282,6 +284,8 @@ def make_step(wl, dev, ckv, wlmod):
 
 # ------------------------------------------------------------------ timing --
 
+USE_GRAPH = False
+TIMING = {}
 FLUSH_BYTES = 1 << 30   # > L2 (129 MB); ~150 us of GPU time that also hides host enqueue
 
 
@@ -303,13 +307,31 @@ def time_steps(step, K, W, dev):
     # events between them would serialise them, so the step times come from
     # a pass with events around whole steps only, and the dominant kernel's
     # launch duration from a second pass with events around that kernel.
+    # With --graph the timed steps replay a CUDA graph of the step (its calls
+    # captured once after the warm-up); by default they are eager calls.
+    graph = None
+    if USE_GRAPH:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            graph = g
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:   # capture not possible here: eager steps
+            print("bench: no CUDA graph (%s); timing eager steps" % e, file=sys.stderr)
+            graph = None
+    TIMING["graph"] = graph is not None
     for i in range(K):
         fl[i][0].record()
         flush.zero_()
         fl[i][1].record()
         t0 = time.perf_counter()
         ev[i][0].record()
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
         ev[i][1].record()
         host_us.append((time.perf_counter() - t0) * 1e6)
     for i in range(K):
@@ -460,7 +482,8 @@ def workload_config(wl):
     return {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "context_tokens": wl.T,
             "compressed_entries": wl.n_comp, "heads": wl.H, "indexer_heads": wl.HI, "topk": wl.topk,
             "window": wl.W, "main_kv": wl.main_fmt, "indexer_keys": wl.idx_fmt or None,
-            "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step"}
+            "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step",
+            "launch": "CUDA graph of the step's library calls" if TIMING.get("graph") else "eager calls"}
 
 
 def main():
@@ -477,6 +500,8 @@ def main():
     torch.cuda.set_device(local)
     dev = "cuda:%d" % local
     step, dom_tag, dom_bytes, launches, layers, host, ws = make_step(wl, dev, ckv, wlmod)
+    global USE_GRAPH
+    USE_GRAPH = args.graph
     if dist:
         dist.barrier()
     with ClockSampler(local) as clk:
