@@ -65,11 +65,12 @@ __device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
 // Score of one key, block by block (16 channels); block blk + 1's bytes are
 // loaded while block blk is multiplied, so one memory round trip per key is
 // exposed rather than one per block.
+template <int HMAX>
 __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t entry,
                                             const float* q, const float* w) {
-  float acc[kMaxHI];
+  float acc[HMAX];
 #pragma unroll
-  for (int h = 0; h < kMaxHI; ++h) acc[h] = 0.f;
+  for (int h = 0; h < HMAX; ++h) acc[h] = 0.f;
   const int64_t row = (int64_t)b * a.cap + entry;
   const bool fp4 = a.fmt == CKV_FMT_FP4;
   auto fetch = [&](int blk, uint4& x0, uint4& x1, uint32_t& sc) {
@@ -110,7 +111,7 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
       }
     }
 #pragma unroll
-    for (int h = 0; h < kMaxHI; ++h) {
+    for (int h = 0; h < HMAX; ++h) {
       if (h < a.HI) {
         const float4* qq = reinterpret_cast<const float4*>(q + h * kIdxDim + blk * 16);
         float r = acc[h];
@@ -128,11 +129,14 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
   }
   float s = 0.f;
 #pragma unroll
-  for (int h = 0; h < kMaxHI; ++h)
+  for (int h = 0; h < HMAX; ++h)
     if (h < a.HI) s = fmaf(w[h], fmaxf(acc[h], 0.f), s);
   return s;
 }
 
+// HMAX: the head count rounded up to 8, 16, 32 or 64; the head loops are
+// unrolled to HMAX, so a few heads do not pay for sixty-four.
+template <int HMAX>
 __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   IndexSmem& sm = *reinterpret_cast<IndexSmem*>(smem_raw);
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
     int64_t e = pool ? (int64_t)pool[i] : first + i;
     uint32_t key = 0u;
     if (e >= 0 && e < ncomp) {
-      const float s = score_simt(a, b, e, sm.q, sm.w);
+      const float s = score_simt<HMAX>(a, b, e, sm.q, sm.w);
       key = score_key(s);
       if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + e] = s;
       ++mine;
@@ -182,14 +186,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
 size_t index_smem_bytes() { return sizeof(IndexSmem); }
 
 cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(index_topk_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(IndexSmem));
-    if (e != cudaSuccess) return e;
-    attr = true;
+  using KernelFn = void (*)(IndexArgs);
+  const KernelFn ks[4] = {index_topk_simt_kernel<8>, index_topk_simt_kernel<16>,
+                          index_topk_simt_kernel<32>, index_topk_simt_kernel<64>};
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    for (KernelFn k : ks) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)sizeof(IndexSmem));
+      if (e != cudaSuccess) return e;
+    }
+    attr_dev = dev;
   }
+  static_assert(kMaxHI <= 64, "the widest instance covers every head count");
+  const KernelFn kern = a.HI <= 8 ? ks[0] : a.HI <= 16 ? ks[1] : a.HI <= 32 ? ks[2] : ks[3];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.B);
   cfg.blockDim = dim3(kIdxThreads);
@@ -198,7 +210,7 @@ cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream) {
   cudaLaunchAttribute at[1] = {pdl_attribute()};
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_topk_simt_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace ckv
