@@ -198,6 +198,17 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   const int kk = min(a.K_sel, (int)sm.n_real);
   const int32_t* pool = a.pool ? a.pool + (int64_t)b * a.pool_len + first_entry : nullptr;
   const bool tr = a.trace && b == 0 && chunk == 0 && threadIdx.x == 0;
+  if (a.n_chunks == 1 && a.pool_out == 0) {
+    // one chunk holds the whole sequence: its top-k is the answer
+    int32_t* oi = a.out_idx + (int64_t)b * a.topk;
+    const int kt = min(a.topk, (int)sm.n_real);
+    block_select_ordered<NT>(
+        n_elem, kt, [&](int i) { return keys[i]; },
+        [&](int pos, int i) { oi[pos] = pool ? pool[i] : (int32_t)(first_entry + i); }, sm.sel);
+    for (int i = kt + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
+    pdl_launch_dependents();
+    return;
+  }
   const long long t0 = clock64();
   long long marks[2] = {0, 0};
   block_select_ordered<NT>(
