@@ -482,8 +482,7 @@ def workload_config(wl):
     return {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "context_tokens": wl.T,
             "compressed_entries": wl.n_comp, "heads": wl.H, "indexer_heads": wl.HI, "topk": wl.topk,
             "window": wl.W, "main_kv": wl.main_fmt, "indexer_keys": wl.idx_fmt or None,
-            "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step",
-            "launch": "CUDA graph of the step's library calls" if TIMING.get("graph") else "eager calls"}
+            "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step"}
 
 
 def main():
@@ -520,7 +519,9 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4/fp8/bf16 in, f32 accumulate",
-            "data": "synthetic", "config": workload_config(wl),
+            "data": "synthetic",
+            "config": dict(workload_config(wl), launch="CUDA graph of the step's library calls"
+                           if TIMING.get("graph") else "eager calls"),
             "roofline": {"bound": "hbm", "kernel": dom_tag, "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": profiled_traffic(dom_tag + ":" + wl.name),
