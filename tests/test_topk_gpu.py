@@ -51,6 +51,9 @@ def _gpu_selection_of(dbg_row, n, k):
     ("fp4", 64, [300, 9000], 512),                 # n_comp < k: -1 padding
     ("fp4", 16, [20000], 1024),                    # several chunks, k = 1024
     ("bf16", 8, [5000, 17], 64),
+    ("bf16", 16, [2000], 256),                     # CUDA-core scorer sized for 16 heads
+    ("bf16", 32, [1500, 900], 128),                # ... for 32 heads
+    ("bf16", 64, [800], 512),                      # ... for 64 heads, one chunk
 ])
 def test_index_topk_matches_oracle(fmt, HI, n_list, topk):
     b = ckv()
