@@ -20,7 +20,11 @@
  *     state between calls (apart from the per-device launch attributes it
  *     sets once).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
- *     NULL = the legacy default stream) and return after enqueueing.
+ *     NULL = the legacy default stream) and return after enqueueing.  The
+ *     kernels are launched with programmatic stream serialisation: one may
+ *     begin launching while the previous work in the stream finishes, but it
+ *     touches no global memory (inputs, outputs, workspace) before that work
+ *     is complete, so stream order holds as usual.
  *   - Arguments are validated on the host first.  A host-detected error
  *     returns CKV_ERR_INVALID / CKV_ERR_UNSUPPORTED / CKV_ERR_WORKSPACE and
  *     enqueues nothing.  A failed launch returns CKV_ERR_CUDA.
