@@ -302,16 +302,24 @@ __device__ __forceinline__ void store_chunk(const AttnArgs& a, uint32_t tile, in
       st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), raw.v);
     }
   } else {  // FP4: 32 channels
-    const float s0 = e4m3_value((uint8_t)(raw.s & 0xFF)), s1 = e4m3_value((uint8_t)(raw.s >> 8));
+    // Hardware conversions: two E2M1 codes -> f16x2, the E4M3 scale -> f16;
+    // a code times a scale has at most 6 significant bits and stays within
+    // f16's range, so the f16 product and its BF16 rounding are exact.
+    const __half2 s0 = __half2half2(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(raw.s & 0xFF), __NV_E4M3)));
+    const __half2 s1 = __half2half2(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(raw.s >> 8), __NV_E4M3)));
     const uint32_t w[4] = {raw.v.x, raw.v.y, raw.v.z, raw.v.w};
     uint32_t o[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float sc = i < 2 ? s0 : s1;
+      const __half2 sc = i < 2 ? s0 : s1;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t byte = (w[i] >> (8 * k)) & 0xFF;
-        o[4 * i + k] = pack_bf16(e2m1_value(byte & 0xF) * sc, e2m1_value(byte >> 4) * sc);
+        // low nibble = even channel = .x
+        const __half2 hv = __hmul2(__half2(__nv_cvt_fp4x2_to_halfraw2(
+                                       (__nv_fp4x2_storage_t)((w[i] >> (8 * k)) & 0xFF), __NV_E2M1)),
+                                   sc);
+        const float2 f = __half22float2(hv);
+        o[4 * i + k] = pack_bf16(f.x, f.y);
       }
     }
     const int d0 = q * 32;
