@@ -96,11 +96,19 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
     if (blk + 1 < 8) fetch(blk + 1, n0, n1, ns);
     float kv[16];
     if (fp4) {
+      // hardware E2M1 decode, two codes (low nibble first) per byte; the
+      // f16 values are exact, the f32 products too
       const float s = e4m3_value((uint8_t)xs);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        kv[i] = e2m1_value((x0.x >> (4 * i)) & 0xF) * s;
-        kv[8 + i] = e2m1_value((x0.y >> (4 * i)) & 0xF) * s;
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(
+            (__nv_fp4x2_storage_t)((x0.x >> (8 * i)) & 0xFF), __NV_E2M1)));
+        const float2 hi = __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(
+            (__nv_fp4x2_storage_t)((x0.y >> (8 * i)) & 0xFF), __NV_E2M1)));
+        kv[2 * i] = lo.x * s;
+        kv[2 * i + 1] = lo.y * s;
+        kv[8 + 2 * i] = hi.x * s;
+        kv[8 + 2 * i + 1] = hi.y * s;
       }
     } else {
       const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
