@@ -29,6 +29,7 @@ struct IndexSmem {
   float q[kMaxHI * kIdxDim];       // dequantised indexer query
   float w[kMaxHI];
   uint32_t keys[kMaxChunk];        // scores of this chunk as order keys
+  float part[kIdxThreads];         // half-head partial scores (two threads per key)
   MergeSmem<kIdxThreads> m;
 };
 
@@ -67,7 +68,8 @@ __device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
 // exposed rather than one per block.
 template <int HMAX>
 __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t entry,
-                                            const float* q, const float* w) {
+                                            const float* q, const float* w, int h0 = 0) {
+  // heads h0 .. h0 + HMAX - 1 (those below HI)
   float acc[HMAX];
 #pragma unroll
   for (int h = 0; h < HMAX; ++h) acc[h] = 0.f;
@@ -120,8 +122,8 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
     }
 #pragma unroll
     for (int h = 0; h < HMAX; ++h) {
-      if (h < a.HI) {
-        const float4* qq = reinterpret_cast<const float4*>(q + h * kIdxDim + blk * 16);
+      if (h0 + h < a.HI) {
+        const float4* qq = reinterpret_cast<const float4*>(q + (h0 + h) * kIdxDim + blk * 16);
         float r = acc[h];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -138,7 +140,7 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
   float s = 0.f;
 #pragma unroll
   for (int h = 0; h < HMAX; ++h)
-    if (h < a.HI) s = fmaf(w[h], fmaxf(acc[h], 0.f), s);
+    if (h0 + h < a.HI) s = fmaf(w[h0 + h], fmaxf(acc[h], 0.f), s);
   return s;
 }
 
@@ -171,7 +173,35 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
     n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)ncomp - first));
   }
   uint32_t mine = 0;
-  for (int i = threadIdx.x; i < n_elem; i += kIdxThreads) {
+  bool split = false;
+  if constexpr (HMAX == 64) {
+    split = n_elem <= kIdxThreads / 2 && a.HI > 32;
+    if (split) {
+      // few keys (a Reindex chunk): two threads per key, 32 heads each
+      const int k = threadIdx.x & (kIdxThreads / 2 - 1), hh = threadIdx.x / (kIdxThreads / 2);
+      float part = 0.f;
+      int64_t e = -1;
+      if (k < n_elem) {
+        e = pool ? (int64_t)pool[k] : first + k;
+        if (e >= 0 && e < ncomp) part = score_simt<32>(a, b, e, sm.q, sm.w, 32 * hh);
+      }
+      sm.part[threadIdx.x] = part;
+      __syncthreads();
+      if (hh == 0 && k < n_elem) {
+        uint32_t key = 0u;
+        if (e >= 0 && e < ncomp) {
+          const float sc = sm.part[k] + sm.part[k + kIdxThreads / 2];
+          key = score_key(sc);
+          if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + e] = sc;
+          ++mine;
+        } else if (e >= ncomp && pool) {
+          report(a.st, CKV_ERR_DEVICE_BOUNDS, (int)e);
+        }
+        sm.keys[k] = key;
+      }
+    }
+  }
+  for (int i = threadIdx.x; !split && i < n_elem; i += kIdxThreads) {
     int64_t e = pool ? (int64_t)pool[i] : first + i;
     uint32_t key = 0u;
     if (e >= 0 && e < ncomp) {

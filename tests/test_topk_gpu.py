@@ -104,23 +104,31 @@ def test_index_topk_exact_ties_go_to_lower_index():
     assert np.array_equal(idx, _gpu_selection_of(d, n, 512))
 
 
-def test_index_pool_and_reindex():
-    """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool."""
+@pytest.mark.parametrize("HI2", [64, 40])
+def test_index_pool_and_reindex(HI2):
+    """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool; the
+    Reindex pass scores its short chunks two threads per key (heads split at
+    32), so a head count that is not a multiple of 32 is covered too."""
     b = ckv()
     n = 12000
     keys, qi, w, plane = _case(2, [n, n - 999], 64, "fp4", seed=5)
     n_comp = torch.tensor([n, n - 999], dtype=torch.int32, device="cuda")
     idx, pool = b.csa_index_topk(plane, n_comp, n, qi, w, 512, pool_out=2048)
-    qi2 = torch.stack([wl.rms_rows((64, 128), 4242 + s, "cuda") for s in range(2)])
-    w2 = torch.stack([wl.head_weights((64,), 99 + s, "cuda") for s in range(2)])
-    idx2 = b.csa_index_topk(plane, n_comp, n, qi2, w2, 512, pool=pool)
+    qi2 = torch.stack([wl.rms_rows((HI2, 128), 4242 + s, "cuda") for s in range(2)])
+    w2 = torch.stack([wl.head_weights((HI2,), 99 + s, "cuda") for s in range(2)])
+    dbg = torch.full((2, n), float("nan"), device="cuda")
+    idx2 = b.csa_index_topk(plane, n_comp, n, qi2, w2, 512, pool=pool, dbg_scores=dbg)
     torch.cuda.synchronize()
     idx, pool, idx2 = idx.cpu().numpy(), pool.cpu().numpy(), idx2.cpu().numpy()
+    dbg = dbg.cpu().numpy()
     for s in range(2):
         sc, eps = _oracle_scores(keys[s], qi[s], w[s], "fp4")
         assert check_topk(pool[s], sc, eps, 2048, where="pool") == 0
         assert check_topk(idx[s], sc, eps, 512, where="full") == 0
         sc2, eps2 = _oracle_scores(keys[s], qi2[s], w2[s], "fp4")
+        cand = pool[s][pool[s] >= 0]
+        err = np.abs(dbg[s, cand] - sc2[cand])
+        assert np.all(err <= eps2[cand] + 1e-30), "reindex score error above the bound"
         assert check_topk(idx2[s], sc2, eps2, 512, candidates=pool[s], where="reindex") == 0
         assert set(idx2[s]) <= set(pool[s])
 
