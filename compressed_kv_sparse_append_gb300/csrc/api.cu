@@ -176,9 +176,12 @@ size_t attn_part_bytes(int B, int layers) {
 size_t attn_ws_bytes(int B, int layers) {
   return attn_part_bytes(B, layers) + align_up((size_t)layers * B * 2 * sizeof(uint32_t), 256);
 }
-void attn_set_ws(AttnArgs& a, uint8_t* region, int B, int layers) {
-  a.part = reinterpret_cast<float*>(region);
-  a.tickets = reinterpret_cast<uint32_t*>(region + attn_part_bytes(B, layers));
+// Layers [l0, ...) of a region sized for `layers`: their partials and
+// counters follow those of layers 0 .. l0 - 1 (inside, a launch indexes them
+// by its own grid z).
+void attn_set_ws(AttnArgs& a, uint8_t* region, int B, int layers, int l0 = 0) {
+  a.part = reinterpret_cast<float*>(region) + (size_t)l0 * B * 2 * kMaxPairs * kPartFloats;
+  a.tickets = reinterpret_cast<uint32_t*>(region + attn_part_bytes(B, layers)) + (size_t)l0 * B * 2;
 }
 
 // Picks the number of CTA pairs per sequence and the cluster shape.  Every
@@ -432,25 +435,33 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
     }
     if (s) return s;
   }
-  // every layer's attention in one launch (grid z = layer)
+  // the layers' attention in as few launches as the parameter block allows
+  // (grid z = layer within a launch), split evenly: 6 layers -> 3 + 3
   AttnArgs la[CKV_CSA2_MAX_LAYERS];
-  // one shape for the whole launch: the tightest layer decides
-  int rows_max = 0;
-  for (int l = 0; l < L; ++l) {
-    const int r = topk + (int)g->win[g->kv_src[l]].cap;
-    rows_max = rows_max > r ? rows_max : r;
+  const int n_launch = (L + kLayersPerLaunch - 1) / kLayersPerLaunch;
+  for (int gi = 0, l0 = 0; gi < n_launch; ++gi) {
+    const int n_g = (L - l0) / (n_launch - gi);
+    // one shape per launch: its tightest layer decides
+    int rows_max = 0;
+    for (int l = l0; l < l0 + n_g; ++l) {
+      const int r = topk + (int)g->win[g->kv_src[l]].cap;
+      rows_max = rows_max > r ? rows_max : r;
+    }
+    const PairChoice pc = choose_pairs(B * n_g, rows_max);
+    for (int l = l0; l < l0 + n_g; ++l) {
+      const int k = g->kv_src[l];
+      la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
+      la[l].idx = layer_idx[l];
+      la[l].topk = topk;
+      la[l].G = pc.G;
+      la[l].cluster_all = pc.cluster_all;
+      attn_set_ws(la[l], attn_region, B, CKV_CSA2_MAX_LAYERS, l0);
+    }
+    s = cuda_status(launch_attention_layers(la + l0, n_g, B, st));
+    if (s) return s;
+    l0 += n_g;
   }
-  const PairChoice pc = choose_pairs(B * L, rows_max);
-  for (int l = 0; l < L; ++l) {
-    const int k = g->kv_src[l];
-    la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
-    la[l].idx = layer_idx[l];
-    la[l].topk = topk;
-    la[l].G = pc.G;
-    la[l].cluster_all = pc.cluster_all;
-    attn_set_ws(la[l], attn_region, B, CKV_CSA2_MAX_LAYERS);   // indexed by layer inside
-  }
-  return cuda_status(launch_attention_layers(la, L, B, st));
+  return CKV_OK;
 }
 
 ckv_status ckv_read_device_status(void* ws, void* stream) {

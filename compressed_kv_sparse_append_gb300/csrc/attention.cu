@@ -356,6 +356,12 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     attn_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_win,
                 const __grid_constant__ AttnBatch batch) {
   const AttnArgs& a = batch.layer[blockIdx.z];
+  if (a.tag != (kArgsTag ^ (int)blockIdx.z)) {
+    // a damaged argument block: touch none of its pointers (every CTA of
+    // the cluster takes this branch, so none waits on the others)
+    if (threadIdx.x == 0) report(batch.layer[0].st, CKV_ERR_INVALID, (int)blockIdx.z);
+    return;
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -1129,7 +1135,7 @@ static AttnKernelFn attn_kernel_for(int fmt) {
 }
 
 cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream) {
-  if (n < 1 || n > kMaxLayers) return cudaErrorInvalidValue;
+  if (n < 1 || n > kLayersPerLaunch) return cudaErrorInvalidValue;
   const AttnArgs& a0 = layers[0];
   for (int l = 1; l < n; ++l)
     if (layers[l].fmt != a0.fmt || layers[l].G != a0.G || layers[l].cluster_all != a0.cluster_all)
@@ -1141,6 +1147,7 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   for (int l = 0; l < n; ++l) {
     batch.layer[l] = layers[l];
     batch.layer[l].use_tma = 0;
+    batch.layer[l].tag = kArgsTag ^ l;
   }
   CUtensorMap mk, mw;
   memset(&mk, 0, sizeof(mk));

@@ -37,19 +37,27 @@ struct AttnArgs {
   uint32_t* tickets;      // workspace: [layer][B][2] finished-CTA counters (start at 0)
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   int progress;           // debugging: count pipeline events in the status block
+  int tag;                // set by the launcher: kArgsTag ^ layer (checked on entry)
   DevStatus* st;
   CUtensorMap gmap[4];    // set by the launcher: row-gather maps (main, window)
 };
 
-constexpr int kMaxLayers = 8;
 constexpr int kMaxPairs = 8;      // CTA pairs per sequence
+// Layers per launch: the kernel's whole parameter block (two tensor maps and
+// the batch) stays within 4 KB, the classic limit, so a launch captured into
+// a CUDA graph carries it whole; more layers take more launches.
+constexpr int kLayersPerLaunch = 4;
+constexpr int kArgsTag = 0x434B5641;
 struct AttnBatch {
-  AttnArgs layer[kMaxLayers];  // one launch runs every layer (grid z = layer)
+  AttnArgs layer[kLayersPerLaunch];  // one launch runs these layers (grid z = layer)
 };
+static_assert(2 * sizeof(CUtensorMap) + sizeof(AttnBatch) <= 4096,
+              "attention parameter block above 4 KB");
 
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream);
 int attn_max_active_clusters(int cluster_size);
-// All `n` layers share B, G and the row format; layer l uses grid z = l.
+// All `n` (<= kLayersPerLaunch) layers share B, G and the row format; layer
+// l uses grid z = l.
 cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaStream_t stream);
 
 }  // namespace ckv

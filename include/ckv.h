@@ -217,7 +217,12 @@ ckv_status ckv_hca_attn(const ckv_plane *kv, const int32_t *n_comp,
  *   REUSE   takes the indices of layer idx_src[l] unchanged.
  * Every layer then attends (as ckv_csa_sparse_attn) to the main KV and
  * window of layer kv_src[l].  Before the layers run, the call appends
- * n_append rows to `append_dst` (as ckv_kv_append_quant). */
+ * n_append rows to `append_dst` (as ckv_kv_append_quant).  The layers'
+ * attention runs in launches of at most four layers each (six layers: two
+ * launches of three), so that every launch's parameter block stays within
+ * the classic 4 KB.  Do not capture this call into a CUDA graph: replaying
+ * such a graph faulted (illegal address) on GB300, cause not yet found;
+ * eager calls are not affected. */
 #define CKV_CSA2_FULL    0
 #define CKV_CSA2_REINDEX 1
 #define CKV_CSA2_REUSE   2
@@ -248,7 +253,9 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group *g, const int32_t *n_comp,
                                  void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronises `stream`, returns the sticky device status recorded in `ws`
- * (CKV_OK, CKV_ERR_DEVICE_BOUNDS or CKV_ERR_TIMEOUT) and clears it. */
+ * (CKV_OK, CKV_ERR_DEVICE_BOUNDS or CKV_ERR_TIMEOUT; CKV_ERR_INVALID if an
+ * attention launch found its argument block damaged and skipped the layer)
+ * and clears it. */
 ckv_status ckv_read_device_status(void *ws, void *stream);
 
 /* Human-readable name of a status code (static string). */

@@ -16,10 +16,14 @@ pytestmark = pytest.mark.gpu
 TAU = 1.0 / math.sqrt(512)
 
 
-@pytest.mark.parametrize("pool_len,wiring", [(256, "bench"), (64, "pages"), (64, "degenerate")])
-def test_csa2_group_matches_oracle(pool_len, wiring):
+# L = 6 runs its attention as two launches of three layers, 8 as 4 + 4,
+# 5 as 3 + 2, 3 as one launch.
+@pytest.mark.parametrize("pool_len,wiring,L", [(256, "bench", 6), (64, "pages", 6),
+                                                (64, "degenerate", 6), (64, "pages", 8),
+                                                (64, "pages", 5), (64, "pages", 3)])
+def test_csa2_group_matches_oracle(pool_len, wiring, L):
     b = ckv()
-    B, n, H, HI, topk, W, L = 2, 2500, 64, 64, 64, 128, 6
+    B, n, H, HI, topk, W = 2, 2500, 64, 64, 64, 128
     if wiring == "degenerate":
         pool_len = topk
     cap = n + 16
@@ -35,11 +39,11 @@ def test_csa2_group_matches_oracle(pool_len, wiring):
     out = [torch.empty_like(q[0]) for _ in range(L)]
     lse = [torch.empty((B, H), device="cuda") for _ in range(L)]
     idx_out = [torch.empty((B, topk), dtype=torch.int32, device="cuda") for _ in range(L)]
-    roles = [oc.FULL, oc.REINDEX] + [oc.REUSE] * 4
+    roles = [oc.FULL, oc.REINDEX] + [oc.REUSE] * (L - 2)
     if wiring == "bench":
-        kv_src, idx_src = [0, 0, 2, 3, 4, 5], [0, 0, 0, 0, 0, 0]
+        kv_src, idx_src = [0, 0] + list(range(2, L)), [0] * L
     else:   # the pages' reading: previous layer's indices, one shared KV
-        kv_src, idx_src = [0] * 6, [0, 0, 1, 2, 3, 4]
+        kv_src, idx_src = [0] * L, [0, 0] + list(range(1, L - 1))
     g = b.make_group(roles, kv_src, idx_src, kvp, wp, kplane, q, qi, w, out, lse=lse, idx_out=idx_out,
                      pool_len=pool_len)
     # 16 appended rows (8 per sequence) into layer 0's main KV at [n, n + 8)
