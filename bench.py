@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attn layer-steps/s at 128k/1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "layer-steps/s"
 KERNEL_SOURCES = ["append.cu", "indexer.cu", "indexer_umma.cu", "attention.cu", "api.cu",
-                  "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh"]
+                  "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh",
+                  "tmap.cuh"]
 
 
 def parse():
@@ -171,6 +172,23 @@ def setup_csa(wl, dev, ckv, wlmod):
     return kv, win, keys, cap
 
 
+def packed(tensors, dev):
+    """The same tensors as views of one device buffer (256-byte aligned
+    offsets), so that a step's inputs or outputs move in one copy."""
+    import torch
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(tensors, offs):
+        v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 def make_step(wl, dev, ckv, wlmod):
     """Returns (step_fn(timer), dominant-kernel tag, algorithmic bytes of the
     dominant kernel per launch, launches per step, layer-steps per step,
@@ -186,6 +204,7 @@ def make_step(wl, dev, ckv, wlmod):
         kv, win, keys, cap = setup_csa(wl, dev, ckv, wlmod)
         new_kv = wlmod.append_rows(wl, B, 512, 0, dev)
         new_key = wlmod.append_rows(wl, B, 128, 1, dev)
+        in_buf, (q, qi, w, new_kv, new_key) = packed((q, qi, w, new_kv, new_key), dev)
         slot = torch.arange(B, dtype=torch.int64, device=dev) * cap + n
         idx = torch.empty((B, wl.topk), dtype=torch.int32, device=dev)
         out = torch.empty_like(q)
@@ -207,7 +226,7 @@ def make_step(wl, dev, ckv, wlmod):
             ckv.csa_sparse_attn(kv, win, win_len, idx, q, tau, out=out, lse=lse, ws=ws)
             return out
 
-        host = {"inputs": (q, qi, w, new_kv, new_key), "outputs": (out,)}
+        host = {"inputs": in_buf, "outputs": out}
         return step, "csa_index_topk", dom_bytes, 4, 1, host, ws
     if wl.kind == "hca":
         cap = n + 8
@@ -219,6 +238,7 @@ def make_step(wl, dev, ckv, wlmod):
             ckv.kv_append_quant(kv, kvr, torch.arange(n, dtype=torch.int64, device=dev) + b * cap, ws=ws)
             ckv.kv_append_quant(win, wr, torch.arange(wl.W, dtype=torch.int64, device=dev) + b * wl.W, ws=ws)
         new_kv = wlmod.append_rows(wl, B, 512, 0, dev)
+        in_buf, (q, new_kv) = packed((q, new_kv), dev)
         slot = torch.arange(B, dtype=torch.int64, device=dev) * cap + n
         out = torch.empty_like(q)
         lse = torch.empty((B, wl.H), device=dev)
@@ -233,7 +253,7 @@ def make_step(wl, dev, ckv, wlmod):
                 timer[1].record()
             return out
 
-        host = {"inputs": (q, new_kv), "outputs": (out,)}
+        host = {"inputs": in_buf, "outputs": out}
         return step, "hca_attn", dom_bytes, 2, 1, host, ws
     # csa2 group
     L = wl.n_layers
@@ -256,11 +276,14 @@ def make_step(wl, dev, ckv, wlmod):
         qs.append(ql)
         qis.append(qil if l < 2 else None)
         ws_.append(wl_ if l < 2 else None)
-    outs = [torch.empty_like(qs[0]) for _ in range(L)]
+    app = wlmod.append_rows(wl, wl.n_append, 512, 0, dev)
+    # the step's inputs in one buffer, its L outputs in another
+    in_buf, views = packed(qs + qis[:2] + ws_[:2] + [app], dev)
+    qs, qis[:2], ws_[:2], app = views[:L], views[L:L + 2], views[L + 2:L + 4], views[L + 4]
+    out_buf, outs = packed([torch.empty_like(qs[0]) for _ in range(L)], dev)
     roles = [ckv.CSA2_FULL, ckv.CSA2_REINDEX] + [ckv.CSA2_REUSE] * (L - 2)
     g = ckv.make_group(roles, [0, 0] + list(range(2, L)), [0, 0] + [0] * (L - 2), kvs, wins, keys, qs,
                        qis, ws_, outs, pool_len=wl.pool_len)
-    app = wlmod.append_rows(wl, wl.n_append, 512, 0, dev)
     per = wl.n_append // B
     app_slot = (torch.arange(B, device=dev)[:, None] * cap + n + torch.arange(per, device=dev)[None]).flatten().to(torch.int64)
     ws = ckv.new_workspace(ckv.workspace_bytes(ckv.OP_CSA2, B, wl.H, wl.HI, n, wl.topk, wl.pool_len), dev)
@@ -276,10 +299,10 @@ def make_step(wl, dev, ckv, wlmod):
             timer[1].record()
         return outs[0]
 
-    host = {"inputs": tuple(qs) + tuple(t for t in qis + ws_ if t is not None) + (app,),
-            "outputs": tuple(outs)}
-    # launches: append + Full index + Reindex index + L attention
-    return step, "csa2_group_decode", dom_bytes, 3 + L, L, host, ws
+    host = {"inputs": in_buf, "outputs": out_buf}
+    # launches: append + Full index + Reindex index + the attention, four
+    # layers at most per launch
+    return step, "csa2_group_decode", dom_bytes, 3 + (L + 3) // 4, L, host, ws
 
 
 # ------------------------------------------------------------------ timing --
@@ -348,19 +371,19 @@ def time_e2e(step, host, K, W, dev):
     """Same steps through the public API, with every step's inputs (queries,
     indexer queries, head weights, new rows) copied from pinned host memory
     into the device tensors the step reads, and the outputs copied back to
-    pinned host memory, inside the timed region."""
+    pinned host memory, inside the timed region.  The step's inputs are views
+    of one device buffer and its outputs of another, so each direction is a
+    single copy."""
     import torch
-    d_in = list(host["inputs"])
-    h_in = [t.cpu().pin_memory() for t in d_in]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in host["outputs"]]
+    d_in, d_out = host["inputs"], host["outputs"]
+    h_in = d_in.cpu().pin_memory()
+    h_out = torch.empty(d_out.shape, dtype=d_out.dtype).pin_memory()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def one():
-        for hsrc, ddst in zip(h_in, d_in):
-            ddst.copy_(hsrc, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         step()
-        for dsrc, hdst in zip(host["outputs"], h_out):
-            hdst.copy_(dsrc, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(W):
@@ -376,8 +399,8 @@ def time_e2e(step, host, K, W, dev):
         e1.record()
         torch.cuda.synchronize()
         tot += e0.elapsed_time(e1)
-    bi = sum(t.numel() * t.element_size() for t in h_in)
-    bo = sum(t.numel() * t.element_size() for t in h_out)
+    bi = h_in.numel() * h_in.element_size()
+    bo = h_out.numel() * h_out.element_size()
     return tot / K, bi, bo
 
 

@@ -74,14 +74,22 @@ def _check(code, where):
         raise CkvError(code, where)
 
 
+# Pointers and streams go to ctypes as plain ints (the argtypes convert them):
+# a decode step makes a handful of these calls, and on the host each object
+# built per argument costs about as much as a kernel launch's own overhead.
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def entry_bytes(fmt: str, dim: int) -> int:
@@ -101,6 +109,7 @@ class Plane:
     memory (data [batch, cap, entry_bytes] uint8, scale per format)."""
 
     def __init__(self, fmt, dim, batch, cap, device="cuda", nope_block=448, data=None, scale=None):
+        self._c = None
         self.fmt, self.dim, self.batch, self.cap, self.nope_block = fmt, dim, batch, cap, nope_block
         eb = entry_bytes(fmt, dim)
         self.data = data if data is not None else torch.zeros((batch, cap, eb), dtype=torch.uint8,
@@ -111,9 +120,18 @@ class Plane:
         else:
             self.scale = torch.zeros((batch, cap) + shp, dtype=dt, device=device)
 
+    def __setattr__(self, name, value):
+        # any change of the plane's fields drops the cached C descriptor
+        object.__setattr__(self, name, value)
+        if name != "_c":
+            object.__setattr__(self, "_c", None)
+
     def c(self) -> CPlane:
-        return CPlane(FMT[self.fmt], self.dim, self.nope_block, self.batch, self.cap,
-                      self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr())
+        """The C descriptor (built once, rebuilt after a field is reassigned)."""
+        if self._c is None:
+            self._c = CPlane(FMT[self.fmt], self.dim, self.nope_block, self.batch, self.cap,
+                             self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr())
+        return self._c
 
 
 def workspace_bytes(op, B, H=0, HI=0, n_comp_max=0, topk=0, pool_len=0) -> int:
@@ -129,7 +147,7 @@ def kv_append_quant(plane: Plane, src, slot, ws=None, stream=None):
     n = 0 if src is None else src.shape[0]
     ws = ws if ws is not None else new_workspace(workspace_bytes(OP_APPEND, 1), plane.data.device)
     c = plane.c()
-    _check(lib.ckv_kv_append_quant(ctypes.byref(c), _ptr(src), _ptr(slot), n, _ptr(ws), ws.numel(),
+    _check(lib.ckv_kv_append_quant(c, _ptr(src), _ptr(slot), n, _ptr(ws), ws.numel(),
                                    _stream(stream)), "kv_append_quant")
     return ws
 
@@ -146,7 +164,7 @@ def csa_index_topk(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, p
         ws = new_workspace(workspace_bytes(OP_INDEX_TOPK, B, 0, HI, n_comp_max, topk, pool_out), dev)
     pool_len = 0 if pool is None else pool.shape[1]
     c = keys.c()
-    _check(lib.ckv_csa_index_topk(ctypes.byref(c), _ptr(n_comp), B, n_comp_max, _ptr(q_idx), _ptr(w),
+    _check(lib.ckv_csa_index_topk(c, _ptr(n_comp), B, n_comp_max, _ptr(q_idx), _ptr(w),
                                   HI, topk, _ptr(pool), pool_len, _ptr(out_idx), _ptr(out_pool),
                                   pool_out if out_pool is not None else 0, _ptr(dbg_scores),
                                   _ptr(ws), ws.numel(), _stream(stream)), "csa_index_topk")
@@ -165,7 +183,7 @@ def csa_index_topk_static(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=
         out_pool = torch.empty((B, pool_out), dtype=torch.int32, device=dev)
     pool_len = 0 if pool is None else pool.shape[1]
     c = keys.c()
-    _check(lib.ckv_csa_index_topk_static(ctypes.byref(c), _ptr(n_comp), B, n_comp_max, _ptr(q_idx),
+    _check(lib.ckv_csa_index_topk_static(c, _ptr(n_comp), B, n_comp_max, _ptr(q_idx),
                                          _ptr(w), HI, topk, _ptr(pool), pool_len, _ptr(out_idx),
                                          _ptr(out_pool), pool_out if out_pool is not None else 0,
                                          _ptr(dbg_scores), _stream(stream)), "csa_index_topk_static")
@@ -179,7 +197,7 @@ def csa_sparse_attn(kv: Plane, win: Plane, win_len, idx, q, sm_scale, out=None, 
         out = torch.empty_like(q)
     ws = ws if ws is not None else new_workspace(workspace_bytes(OP_SPARSE_ATTN, B), q.device)
     ck, cw = kv.c(), win.c()
-    _check(lib.ckv_csa_sparse_attn(ctypes.byref(ck), ctypes.byref(cw), _ptr(win_len), _ptr(idx), B,
+    _check(lib.ckv_csa_sparse_attn(ck, cw, _ptr(win_len), _ptr(idx), B,
                                    idx.shape[1], _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
                                    ws.numel(), _stream(stream)), "csa_sparse_attn")
     return out
@@ -192,7 +210,7 @@ def hca_attn(kv: Plane, n_comp, n_comp_max, win: Plane, win_len, q, sm_scale, ou
         out = torch.empty_like(q)
     ws = ws if ws is not None else new_workspace(workspace_bytes(OP_HCA_ATTN, B), q.device)
     ck, cw = kv.c(), win.c()
-    _check(lib.ckv_hca_attn(ctypes.byref(ck), _ptr(n_comp), n_comp_max, ctypes.byref(cw),
+    _check(lib.ckv_hca_attn(ck, _ptr(n_comp), n_comp_max, cw,
                             _ptr(win_len), B, _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
                             ws.numel(), _stream(stream)), "hca_attn")
     return out

@@ -95,6 +95,17 @@ bool use_umma_indexer() {
   return v == 1;
 }
 
+// CKV_DEBUG_PROGRESS (1, 2 or 3; read once per process) turns on the
+// kernels' debugging records in the status block.
+int debug_progress() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CKV_DEBUG_PROGRESS");
+    v = (e && e[0] >= '1' && e[0] <= '3') ? e[0] - '0' : 0;
+  }
+  return v;
+}
+
 ckv_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return CKV_OK;
   (void)cudaGetLastError();
@@ -134,8 +145,7 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.out_pool = out_pool;
   a.dbg = dbg;
   a.st = st;
-  const char* pe = getenv("CKV_DEBUG_PROGRESS");
-  a.trace = (pe && pe[0] == '2') ? 1 : 0;
+  a.trace = debug_progress() == 2 ? 1 : 0;
   const int64_t rows = (int64_t)keys->batch * keys->cap;
   if (use_umma_indexer() && index_umma_supported(a, rows))
     return cuda_status(launch_index_umma(a, rows, stream));
@@ -247,8 +257,7 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.tickets = nullptr;
   a.st = st;
   a.use_tma = 0;
-  const char* pe = getenv("CKV_DEBUG_PROGRESS");
-  a.progress = (pe && pe[0] >= '1' && pe[0] <= '3') ? pe[0] - '0' : 0;
+  a.progress = debug_progress();
   return a;
 }
 

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "attention.cuh"
+#include "tmap.cuh"
 
 namespace ckv {
 
@@ -1039,44 +1040,20 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_attn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 2-D map over a BF16 plane viewed as [rows][512] bf16, box 64 x 64, 128B swizzle.
 bool encode_bf16_rows(CUtensorMap* m, const void* data, int64_t rows) {
-  auto enc = encode_fn_attn();
-  if (!enc || rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
-  cuuint64_t dims[2] = {512, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {1024};
-  cuuint32_t box[2] = {64, 64};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(data), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, data, 512, (uint64_t)rows, 1024, 64, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 2-D map of one-row boxes over a plane's rows (`rows` rows of `row_elems`
 // elements of `dt`, contiguous) for TMA gathers of `box_elems` elements.
 bool encode_gather_rows(CUtensorMap* m, const void* data, CUtensorMapDataType dt, int elem_bytes,
                         int64_t rows, int row_elems, int box_elems, CUtensorMapSwizzle sw) {
-  auto enc = encode_fn_attn();
-  if (!enc || !data || rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem_bytes};
-  cuuint32_t box[2] = {(cuuint32_t)box_elems, 1};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(data), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (!data || rows <= 0 || rows >= ((int64_t)1 << 31)) return false;
+  return encode_tmap_2d(m, dt, data, (uint64_t)row_elems, (uint64_t)rows,
+                        (uint64_t)row_elems * elem_bytes, (uint32_t)box_elems, 1, sw);
 }
 
 // The gather maps of one layer: [0, 1] main plane, [2, 3] window plane.

@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "tmap.cuh"
 #include "topk_merge.cuh"
 
 namespace ckv {
@@ -284,28 +285,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
                                     (int)(kOffMerge / 8), msm);
 }
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-}  // namespace
-
 bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
   // FP4 keys, no pool, 64 heads max, scale rows pair up (even cap), the
   // 2-D maps' row counts fit in int32.
   return a.fmt == CKV_FMT_FP4 && a.pool == nullptr && a.HI <= 64 && (a.cap % 2) == 0 &&
-         batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && encode_fn() != nullptr;
+         batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && tmap_encode_fn() != nullptr;
 }
 
 cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream_t stream) {
@@ -318,28 +302,12 @@ cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
-  auto enc = encode_fn();
   CUtensorMap md, ms;
-  {
-    cuuint64_t dims[2] = {64, (cuuint64_t)batch_rows};
-    cuuint64_t strides[1] = {64};
-    cuuint32_t box[2] = {64, (cuuint32_t)kUTile};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.kdata), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[2] = {16, (cuuint64_t)(batch_rows / 2)};
-    cuuint64_t strides[1] = {16};
-    cuuint32_t box[2] = {16, (cuuint32_t)(kUTile / 2)};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.kscale), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (!encode_tmap_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kdata, 64, (uint64_t)batch_rows, 64, 64,
+                      (uint32_t)kUTile, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kscale, 16, (uint64_t)(batch_rows / 2), 16,
+                      16, (uint32_t)(kUTile / 2), CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   UmmaIndexArgs ua;
   ua.a = a;
   ua.row_limit = batch_rows;
