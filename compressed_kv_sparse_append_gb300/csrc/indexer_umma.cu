@@ -54,6 +54,7 @@ constexpr uint32_t kTmemU = 256;
 constexpr uint32_t kColD = 0;          // two 64-column accumulators
 constexpr uint32_t kColSFA = 128;      // 8 columns per stage
 constexpr uint32_t kColSFB = 192;      // 8 columns
+static_assert(kColSFA + 8 * kUStages <= kColSFB, "scale columns of every stage below SFB");
 constexpr uint32_t kIdescNvf4 = idesc_nvf4(128, 64);
 
 enum { BU_FULL = 0, BU_EMPTY = kUStages, BU_SFA = 2 * kUStages, BU_DFULL = 3 * kUStages,
