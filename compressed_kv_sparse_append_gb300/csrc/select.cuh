@@ -104,7 +104,8 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
   __syncthreads();
   lo = sm.bcast[2];
   hi = sm.bcast[3];
-  __syncthreads();
+  // (no barrier here: bcast[2..3] and warp_a/b are not written again before
+  // the barriers below)
   if (lo == hi) {   // every key equal
     T = lo;
     need = (uint32_t)K;
@@ -112,11 +113,14 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
   }
   int top = 32 - __clz(lo ^ hi);   // bits [top, 32) are the same in every key
   uint32_t prefix = top == 32 ? 0u : (lo & (0xFFFFFFFFu << top)), remaining = (uint32_t)K;
+  // Two barriers per pass: warp 0 clears the bins as it scans them, and the
+  // digit it publishes is read before any thread can reach the next pass's
+  // publication (which follows that pass's first barrier).
+  for (int i = threadIdx.x; i < 256; i += NT) sm.hist[i] = 0;
+  __syncthreads();
 #pragma unroll 1
   while (top > 0) {
     const int width = top < 8 ? top : 8, shift = top - width;
-    for (int i = threadIdx.x; i < 256; i += NT) sm.hist[i] = 0;
-    __syncthreads();
     const uint32_t mask = top == 32 ? 0u : (0xFFFFFFFFu << top);   // settled bits
     const uint32_t dmask = (1u << width) - 1u;
     for (int i = threadIdx.x; i < n; i += NT) {
@@ -130,6 +134,7 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         c[j] = sm.hist[255 - 8 * lane - j];
+        sm.hist[255 - 8 * lane - j] = 0;
         t += c[j];
       }
       uint32_t incl = t;
@@ -156,8 +161,9 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
     prefix |= sm.bcast[0] << shift;
     remaining = sm.bcast[1];
     top = shift;
-    __syncthreads();
   }
+  // the caller may reuse sm once everyone has read the last digit
+  __syncthreads();
   T = prefix;
   need = remaining;
 }
