@@ -7,9 +7,9 @@ A step is one decode step of one layer for the whole batch on a synthetic
 workload (see compressed_kv_sparse_append_gb300/workloads.py):
   * CSA workloads (default: csa_128k = batch 8, 131072-token context, 32768
     compressed entries, 128 heads, 64 indexer heads, top-512, mixed
-    FP8-nope/BF16-rope main KV, FP4 indexer keys): kv_append_quant of the
-    step's new compressed entry and indexer key, csa_index_topk,
-    csa_sparse_attn;
+    FP8-nope/BF16-rope main KV, FP4 indexer keys): kv_append_quant_multi of
+    the step's new compressed entry and indexer key (one launch for both
+    planes), csa_index_topk, csa_sparse_attn;
   * hca_1m: kv_append_quant + hca_attn;
   * csa2_group: one csa2_group_decode call (six layer-steps).
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
@@ -216,8 +216,8 @@ def make_step(wl, dev, ckv, wlmod):
         dom_bytes = B * n * ent + qi.numel() * 2 + w.numel() * 4 + idx.numel() * 4
 
         def step(timer=None):
-            ckv.kv_append_quant(kv, new_kv, slot, ws=ws)
-            ckv.kv_append_quant(keys, new_key, slot, ws=ws)
+            # the new main-KV and indexer-key rows, one launch for both planes
+            ckv.kv_append_quant_multi([kv, keys], [new_kv, new_key], [slot, slot], ws=ws)
             if timer:
                 timer[0].record()
             ckv.csa_index_topk(keys, n_comp, n, qi, w, wl.topk, out_idx=idx, ws=ws)
@@ -227,7 +227,7 @@ def make_step(wl, dev, ckv, wlmod):
             return out
 
         host = {"inputs": in_buf, "outputs": out}
-        return step, "csa_index_topk", dom_bytes, 4, 1, host, ws
+        return step, "csa_index_topk", dom_bytes, 3, 1, host, ws
     if wl.kind == "hca":
         cap = n + 8
         kv = ckv.Plane("bf16", 512, B, cap, dev)

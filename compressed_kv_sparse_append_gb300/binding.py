@@ -43,6 +43,9 @@ lib.ckv_workspace_bytes.restype = _sz
 lib.ckv_workspace_bytes.argtypes = [_i32] * 7
 lib.ckv_kv_append_quant.restype = _i32
 lib.ckv_kv_append_quant.argtypes = [_P, _vp, _vp, _i32, _vp, _sz, _vp]
+lib.ckv_kv_append_quant_multi.restype = _i32
+lib.ckv_kv_append_quant_multi.argtypes = [_P, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                          ctypes.POINTER(_i32), _i32, _vp, _sz, _vp]
 lib.ckv_csa_index_topk.restype = _i32
 lib.ckv_csa_index_topk.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp,
                                    _i32, _vp, _vp, _sz, _vp]
@@ -149,6 +152,24 @@ def kv_append_quant(plane: Plane, src, slot, ws=None, stream=None):
     c = plane.c()
     _check(lib.ckv_kv_append_quant(c, _ptr(src), _ptr(slot), n, _ptr(ws), ws.numel(),
                                    _stream(stream)), "kv_append_quant")
+    return ws
+
+
+APPEND_MAX_PLANES = 4
+
+
+def kv_append_quant_multi(planes, srcs, slots, ws=None, stream=None):
+    """kv_append_quant into several planes (distinct data) in one launch."""
+    k = len(planes)
+    if not 1 <= k <= APPEND_MAX_PLANES or len(srcs) != k or len(slots) != k:
+        raise ValueError("kv_append_quant_multi: 1..%d planes, one src and slot each" % APPEND_MAX_PLANES)
+    ws = ws if ws is not None else new_workspace(workspace_bytes(OP_APPEND, 1), planes[0].data.device)
+    cp = (CPlane * k)(*[p.c() for p in planes])
+    sp = (_vp * k)(*[_ptr(t) for t in srcs])
+    lp = (_vp * k)(*[_ptr(t) for t in slots])
+    nn = (_i32 * k)(*[0 if t is None else t.shape[0] for t in srcs])
+    _check(lib.ckv_kv_append_quant_multi(cp, sp, lp, nn, k, _ptr(ws), ws.numel(), _stream(stream)),
+           "kv_append_quant_multi")
     return ws
 
 

@@ -13,6 +13,8 @@
 namespace ckv {
 cudaError_t launch_append(const ckv_plane& p, const void* src, const int64_t* slot, int32_t n,
                           DevStatus* st, cudaStream_t stream);
+cudaError_t launch_append_multi(const ckv_plane* p, const void* const* src, const int64_t* const* slot,
+                                const int32_t* n, int n_planes, DevStatus* st, cudaStream_t stream);
 }
 
 using namespace ckv;
@@ -304,6 +306,27 @@ ckv_status ckv_kv_append_quant(const ckv_plane* dst, const void* src_bf16, const
   if (s) return s;
   return cuda_status(launch_append(*dst, src_bf16, slot, n, static_cast<DevStatus*>(ws),
                                    static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_kv_append_quant_multi(const ckv_plane* dst, const void* const* src_bf16,
+                                     const int64_t* const* slot, const int32_t* n, int32_t n_planes,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (!dst || !src_bf16 || !slot || !n || n_planes < 1 || n_planes > CKV_APPEND_MAX_PLANES)
+    return CKV_ERR_INVALID;
+  for (int k = 0; k < n_planes; ++k) {
+    if (n[k] < 0) return CKV_ERR_INVALID;
+    ckv_status s = check_plane(&dst[k], dst[k].dim, 1);
+    if (s) return s;
+    if (dst[k].dim != 512 && dst[k].dim != 128) return CKV_ERR_UNSUPPORTED;
+    if (n[k] > 0 && (!src_bf16[k] || !slot[k] || !aligned16(src_bf16[k]))) return CKV_ERR_INVALID;
+    // the planes' entry bytes must not overlap (rows land in no set order)
+    for (int j = 0; j < k; ++j)
+      if (dst[j].data == dst[k].data) return CKV_ERR_INVALID;
+  }
+  ckv_status s = check_ws(ws, ws_bytes, kStatusBytes);
+  if (s) return s;
+  return cuda_status(launch_append_multi(dst, src_bf16, slot, n, n_planes, static_cast<DevStatus*>(ws),
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 ckv_status ckv_csa_index_topk(const ckv_plane* idx_keys, const int32_t* n_comp, int32_t B,

@@ -12,6 +12,8 @@
 // are 8- to 32-byte vectors; the whole call is a few microseconds of launch
 // latency for the row counts of a decode step.
 
+#include <cstring>
+
 #include "common.cuh"
 
 namespace ckv {
@@ -38,11 +40,17 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* p, float (&v)[
   }
 }
 
-__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
+// Up to kMaxAppendPlanes appends in one launch: plane k takes blocks
+// [block0[k], block0[k + 1]), four rows per block.
+constexpr int kMaxAppendPlanes = CKV_APPEND_MAX_PLANES;
+struct AppendBatch {
+  AppendArgs p[kMaxAppendPlanes];
+  int32_t block0[kMaxAppendPlanes + 1];
+  int32_t n_planes;
+};
+
+// Row `row` of append `a`, by one warp.
+__device__ __forceinline__ void append_row(const AppendArgs& a, int row, int lane) {
   if (row >= a.n) return;
   const int64_t slot = a.slot[row];
   if (slot < 0) return;
@@ -134,28 +142,52 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   }
 }
 
-cudaError_t launch_append(const ckv_plane& p, const void* src, const int64_t* slot, int32_t n,
-                          DevStatus* st, cudaStream_t stream) {
-  if (n == 0) return cudaSuccess;
-  AppendArgs a;
-  a.data = static_cast<uint8_t*>(p.data);
-  a.scale = p.scale;
-  a.src = static_cast<const __nv_bfloat16*>(src);
-  a.slot = slot;
-  a.n_slots = (int64_t)p.batch * p.cap;
-  a.n = n;
-  a.fmt = p.fmt;
-  a.dim = p.dim;
-  a.nope_block = p.nope_block;
-  a.st = st;
+__global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendBatch b) {
+  pdl_wait();
+  pdl_launch_dependents();
+  int k = 0;
+  while (k + 1 < b.n_planes && (int)blockIdx.x >= b.block0[k + 1]) ++k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  append_row(b.p[k], ((int)blockIdx.x - b.block0[k]) * 4 + warp, lane);
+}
+
+cudaError_t launch_append_multi(const ckv_plane* p, const void* const* src, const int64_t* const* slot,
+                                const int32_t* n, int n_planes, DevStatus* st, cudaStream_t stream) {
+  if (n_planes < 1 || n_planes > kMaxAppendPlanes) return cudaErrorInvalidValue;
+  AppendBatch b;
+  memset(&b, 0, sizeof(b));
+  int blocks = 0;
+  for (int k = 0; k < n_planes; ++k) {
+    AppendArgs& a = b.p[k];
+    a.data = static_cast<uint8_t*>(p[k].data);
+    a.scale = p[k].scale;
+    a.src = static_cast<const __nv_bfloat16*>(src[k]);
+    a.slot = slot[k];
+    a.n_slots = (int64_t)p[k].batch * p[k].cap;
+    a.n = n[k];
+    a.fmt = p[k].fmt;
+    a.dim = p[k].dim;
+    a.nope_block = p[k].nope_block;
+    a.st = st;
+    b.block0[k] = blocks;
+    blocks += (n[k] + 3) / 4;
+  }
+  b.block0[n_planes] = blocks;
+  b.n_planes = n_planes;
+  if (blocks == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n + 3) / 4);
+  cfg.gridDim = dim3(blocks);
   cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cudaLaunchAttribute at[1] = {pdl_attribute()};
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, append_kernel, a);
+  return cudaLaunchKernelEx(&cfg, append_kernel, b);
+}
+
+cudaError_t launch_append(const ckv_plane& p, const void* src, const int64_t* slot, int32_t n,
+                          DevStatus* st, cudaStream_t stream) {
+  return launch_append_multi(&p, &src, &slot, &n, 1, st, stream);
 }
 
 }  // namespace ckv

@@ -124,6 +124,23 @@ ckv_status ckv_kv_append_quant(const ckv_plane *dst, const void *src_bf16,
                                const int64_t *slot, int32_t n,
                                void *ws, size_t ws_bytes, void *stream);
 
+/* Several appends in one launch (the same passages as ckv_kv_append_quant):
+ * plane k receives n[k] rows src_bf16[k] at slot[k], stored bit-exactly as
+ * ckv_kv_append_quant(&dst[k], src_bf16[k], slot[k], n[k], ...) stores them.
+ * A decode step appends to several planes (the main KV and the indexer
+ * keys); one launch instead of one per plane shortens the step's chain of
+ * dependent launches.
+ *   dst      [host] n_planes plane descriptors, 1 <= n_planes <=
+ *            CKV_APPEND_MAX_PLANES, with distinct data arrays.
+ *   src_bf16 [host] n_planes device pointers, each [n[k]][dst[k].dim] bf16.
+ *   slot     [host] n_planes device pointers, each [n[k]] int64 (as above).
+ *   n        [host] n_planes row counts (>= 0).
+ * Validation, workspace and device status as ckv_kv_append_quant. */
+#define CKV_APPEND_MAX_PLANES 4
+ckv_status ckv_kv_append_quant_multi(const ckv_plane *dst, const void *const *src_bf16,
+                                     const int64_t *const *slot, const int32_t *n,
+                                     int32_t n_planes, void *ws, size_t ws_bytes, void *stream);
+
 /* Lightning-indexer score + exact top-k ([KVC] §四; score definition
  * s_j = sum_h w_h * ReLU(q_h . k_j) on the dequantised values; for FP4 keys
  * the query is first quantised with the same E2M1 + E4M3/16 block

@@ -81,3 +81,34 @@ def test_host_validation_rejects_before_launch(lib):
     args[7] = 128
     args[12] = ctypes.c_size_t(16)
     assert lib.ckv_csa_sparse_attn(*args) == -4
+
+
+def test_append_multi_host_validation(lib):
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    f = lib.ckv_kv_append_quant_multi
+    f.restype = ctypes.c_int32
+    vp = ctypes.c_void_p
+    planes = (CPlane * 2)(CPlane(2, 512, 448, 1, 8, 0x10000, 0x20000),
+                          CPlane(2, 128, 448, 1, 8, 0x30000, 0x40000))
+    src = (vp * 2)(0x50000, 0x60000)
+    slot = (vp * 2)(0x70000, 0x80000)
+    n = (ctypes.c_int32 * 2)(1, 1)
+    ws = vp(0x90000)
+    # no planes, too many planes, null arrays
+    assert f(planes, src, slot, n, 0, ws, ctypes.c_size_t(256), None) == -1
+    assert f(planes, src, slot, n, 5, ws, ctypes.c_size_t(256), None) == -1
+    assert f(None, src, slot, n, 2, ws, ctypes.c_size_t(256), None) == -1
+    assert f(planes, None, slot, n, 2, ws, ctypes.c_size_t(256), None) == -1
+    # missing workspace
+    assert f(planes, src, slot, n, 2, None, ctypes.c_size_t(0), None) == -4
+    # a negative row count; a misaligned source of the second plane
+    n_bad = (ctypes.c_int32 * 2)(1, -1)
+    assert f(planes, src, slot, n_bad, 2, ws, ctypes.c_size_t(256), None) == -1
+    src_bad = (vp * 2)(0x50000, 0x60008)
+    assert f(planes, src_bad, slot, n, 2, ws, ctypes.c_size_t(256), None) == -1
+    # the same plane twice (rows would race)
+    same = (CPlane * 2)(planes[0], planes[0])
+    assert f(same, src, slot, n, 2, ws, ctypes.c_size_t(256), None) == -1
+    # an unsupported dim in the second plane
+    odd = (CPlane * 2)(planes[0], CPlane(2, 256, 448, 1, 8, 0x30000, 0x40000))
+    assert f(odd, src, slot, n, 2, ws, ctypes.c_size_t(256), None) in (-1, -2)
