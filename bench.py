@@ -33,9 +33,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn layer-steps/s at 128k/1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "layer-steps/s"
-KERNEL_SOURCES = ["append.cu", "indexer.cu", "indexer_umma.cu", "attention.cu", "api.cu",
-                  "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh",
-                  "tmap.cuh"]
+ALL_SOURCES = ["append.cu", "indexer.cu", "indexer_umma.cu", "attention.cu", "api.cu",
+               "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh",
+               "tmap.cuh"]
+# The sources that decide each dominant kernel's DRAM traffic (its code, the
+# headers it includes, and the host code that sizes its launch).
+KERNEL_SOURCES = {
+    "csa_index_topk": ["indexer_umma.cu", "indexer.cu", "topk_merge.cuh", "select.cuh",
+                       "indexer.cuh", "common.cuh", "tmap.cuh", "api.cu"],
+    "hca_attn": ["attention.cu", "attention.cuh", "common.cuh", "tmap.cuh", "api.cu"],
+}
 
 
 def parse():
@@ -52,9 +59,9 @@ def parse():
     return p.parse_args()
 
 
-def source_hash():
+def source_hash(kernel=None):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES.get(kernel, ALL_SOURCES):
         with open(os.path.join(ROOT, "compressed_kv_sparse_append_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -66,7 +73,7 @@ def profiled_traffic(kernel_tag):
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    cur = source_hash()
+    cur = source_hash(kernel_tag.split(":")[0])
     for line in open(path, encoding="utf-8"):
         parts = line.strip().strip("|").split("|")
         parts = [p.strip() for p in parts]
