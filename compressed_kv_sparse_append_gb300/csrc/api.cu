@@ -53,6 +53,17 @@ struct IndexLayout {
 // Candidate rows hold K_sel slots, a multiple of 4 (16-byte rows).
 int pad4(int k) { return (k + 3) & ~3; }
 
+// Between-call state of the single-op calls, at fixed offsets after the
+// status block, so that index/top-k and attention calls with the same B may
+// share one workspace: every op's scratch starts after all of it.
+//   [0, index_zero_bytes)   index: per-sequence merge tickets, then the
+//                           per-sequence 4096-bin key histograms
+//   [.., + attn_zero_bytes) attention: per-sequence, per-half merge counters
+// Each op leaves its own part zero when it finishes.
+size_t index_zero_bytes(int B) { return align_up((size_t)B * 4, 256) + (size_t)B * 4096 * 4; }
+size_t attn_zero_bytes(int B) { return align_up((size_t)B * 2 * sizeof(uint32_t), 256); }
+size_t shared_zero_bytes(int B) { return index_zero_bytes(B) + attn_zero_bytes(B); }
+
 IndexLayout index_layout(int B, int n_comp_max, int K_sel_in, bool pool_mode, int pool_len) {
   IndexLayout L;
   const int K_sel = pad4(K_sel_in);
@@ -73,7 +84,7 @@ IndexLayout index_layout(int B, int n_comp_max, int K_sel_in, bool pool_mode, in
   }
   L.counters_off = 0;
   L.hist_off = align_up((size_t)B * 4, 256);
-  L.key_off = L.hist_off + (size_t)B * 4096 * 4;
+  L.key_off = shared_zero_bytes(B);   // candidates after the attention's counters too
   const size_t cand = (size_t)B * L.n_chunks * K_sel * 4;
   L.idx_off = L.key_off + align_up(cand, 256);
   L.bytes = L.idx_off + align_up(cand, 256);
@@ -89,22 +100,20 @@ ckv_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 // FP4 keys are scored on the block-scaled tensor cores; CKV_INDEXER=simt in
 // the environment selects the CUDA-core scorer (used to cross-check them).
 bool use_umma_indexer() {
-  static int v = -1;
-  if (v < 0) {
+  static const bool v = [] {
     const char* e = getenv("CKV_INDEXER");
-    v = (e && strcmp(e, "simt") == 0) ? 0 : 1;
-  }
-  return v == 1;
+    return !(e && strcmp(e, "simt") == 0);
+  }();
+  return v;
 }
 
 // CKV_DEBUG_PROGRESS (1, 2 or 3; read once per process) turns on the
 // kernels' debugging records in the status block.
 int debug_progress() {
-  static int v = -1;
-  if (v < 0) {
+  static const int v = [] {
     const char* e = getenv("CKV_DEBUG_PROGRESS");
-    v = (e && e[0] >= '1' && e[0] <= '3') ? e[0] - '0' : 0;
-  }
+    return (e && e[0] >= '1' && e[0] <= '3') ? e[0] - '0' : 0;
+  }();
   return v;
 }
 
@@ -194,6 +203,13 @@ size_t attn_ws_bytes(int B, int layers) {
 void attn_set_ws(AttnArgs& a, uint8_t* region, int B, int layers, int l0 = 0) {
   a.part = reinterpret_cast<float*>(region) + (size_t)l0 * B * 2 * kMaxPairs * kPartFloats;
   a.tickets = reinterpret_cast<uint32_t*>(region + attn_part_bytes(B, layers)) + (size_t)l0 * B * 2;
+}
+// The single-op attention calls: counters in their fixed slot of the shared
+// layout, partials after it.
+size_t attn_single_ws_bytes(int B) { return shared_zero_bytes(B) + attn_part_bytes(B, 1); }
+void attn_set_ws_single(AttnArgs& a, uint8_t* region, int B) {
+  a.tickets = reinterpret_cast<uint32_t*>(region + index_zero_bytes(B));
+  a.part = reinterpret_cast<float*>(region + shared_zero_bytes(B));
 }
 
 // Picks the number of CTA pairs per sequence and the cluster shape.  Every
@@ -288,7 +304,7 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t
     }
     case CKV_OP_SPARSE_ATTN:
     case CKV_OP_HCA_ATTN:
-      return kStatusBytes + attn_ws_bytes(B, 1);
+      return kStatusBytes + attn_single_ws_bytes(B);
     default:
       return kStatusBytes;
   }
@@ -356,11 +372,11 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
   if (s) return s;
   if (!idx || topk <= 0) return CKV_ERR_INVALID;
   if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
-  s = check_ws(ws, ws_bytes, kStatusBytes + attn_ws_bytes(B, 1));
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_single_ws_bytes(B));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
-  attn_set_ws(a, static_cast<uint8_t*>(ws) + kStatusBytes, B, 1);
+  attn_set_ws_single(a, static_cast<uint8_t*>(ws) + kStatusBytes, B);
   a.idx = idx;
   a.topk = topk;
   const PairChoice pc = choose_pairs(B, topk + (int)win->cap);
@@ -376,11 +392,11 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!n_comp || n_comp_max < 0 || n_comp_max > kv->cap) return CKV_ERR_INVALID;
-  s = check_ws(ws, ws_bytes, kStatusBytes + attn_ws_bytes(B, 1));
+  s = check_ws(ws, ws_bytes, kStatusBytes + attn_single_ws_bytes(B));
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
-  attn_set_ws(a, static_cast<uint8_t*>(ws) + kStatusBytes, B, 1);
+  attn_set_ws_single(a, static_cast<uint8_t*>(ws) + kStatusBytes, B);
   a.n_comp = n_comp;
   a.n_comp_max = n_comp_max;
   const PairChoice pc = choose_pairs(B, n_comp_max + (int)win->cap);
@@ -530,8 +546,7 @@ const char* ckv_status_string(ckv_status s) {
 // with cudaGetSymbolAddress once per device (the array's name is only a
 // host-side stand-in) and passes that address to the same kernels.
 static __device__ __align__(256) uint8_t g_index_scratch[CKV_STATIC_SCRATCH_BYTES];
-static constexpr int kMaxDevices = 64;
-static void* g_index_scratch_dev[kMaxDevices] = {};
+static void* g_index_scratch_dev[kOnceDevices] = {};
 
 extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const int32_t* n_comp,
                                                 int32_t B, int32_t n_comp_max,
@@ -547,14 +562,16 @@ extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const
   const int K_sel = out_pool ? pool_out : topk;
   const IndexLayout L = index_layout(B, n_comp_max, K_sel, pool_mode, pool_mode ? pool_len : 0);
   if (kStatusBytes + L.bytes > (size_t)CKV_STATIC_SCRATCH_BYTES) return CKV_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CKV_ERR_CUDA;
-  if (g_index_scratch_dev[dev] == nullptr) {
+  static DeviceOnce once;
+  int dev = -1;
+  const cudaError_t e = once_per_device(once, [](int d) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr)
-      return cuda_status(cudaErrorUnknown);
-    g_index_scratch_dev[dev] = p;
-  }
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_index_scratch);
+    g_index_scratch_dev[d] = p;
+    return r != cudaSuccess ? r : p == nullptr ? cudaErrorUnknown : cudaSuccess;
+  });
+  if (e != cudaSuccess) return cuda_status(e);
+  if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_CUDA;
   uint8_t* w8 = static_cast<uint8_t*>(g_index_scratch_dev[dev]);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // status, per-sequence tickets and key histograms must start at zero

@@ -1094,20 +1094,18 @@ using AttnKernelFn = void (*)(const CUtensorMap, const CUtensorMap, const AttnBa
 // The kernel instance for a cache format (nullptr for an unknown one), with
 // its launch attributes set once per device.
 static AttnKernelFn attn_kernel_for(int fmt) {
-  static int attr_done = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
+  static DeviceOnce once;
   const AttnKernelFn ks[3] = {attn_kernel<CKV_FMT_BF16>, attn_kernel<CKV_FMT_MIXED>,
                               attn_kernel<CKV_FMT_FP4>};
-  if (attr_done != dev) {
+  const cudaError_t e = once_per_device(once, [&](int) {
     for (AttnKernelFn k : ks) {
-      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn) !=
-              cudaSuccess ||
-          cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return nullptr;
+      cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAttn);
+      if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (r != cudaSuccess) return r;
     }
-    attr_done = dev;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return nullptr;
   return fmt == CKV_FMT_BF16 ? ks[0] : fmt == CKV_FMT_MIXED ? ks[1] : fmt == CKV_FMT_FP4 ? ks[2] : nullptr;
 }
 
@@ -1157,38 +1155,41 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
 // Clusters of `cluster_size` CTAs of attn_kernel that fit on the GPU at once
 // (cached per device and size).
 int attn_max_active_clusters(int cluster_size) {
-  static int cache_dev = -1;
-  static int cache[2 * kMaxPairs + 1] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (cache_dev != dev) {
-    for (int i = 0; i <= 2 * kMaxPairs; ++i) cache[i] = -1;
-    cache_dev = dev;
-  }
+  // every cluster size 1 .. 2 kMaxPairs, asked once per device
+  static DeviceOnce once;
+  static int cache[kOnceDevices][2 * kMaxPairs + 1];
   if (cluster_size < 1 || cluster_size > 2 * kMaxPairs) return 0;
-  if (cache[cluster_size] < 0) {
+  int dev = -1;
+  const cudaError_t e = once_per_device(once, [&](int d) {
+    dev = d;
     // every format's instance has the same resources: ask about one
     const AttnKernelFn kern = attn_kernel_for(CKV_FMT_MIXED);
-    if (!kern) return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cluster_size, 1, 1);
-    cfg.blockDim = dim3(kThreadsAttn, 1, 1);
-    cfg.dynamicSmemBytes = kSmemAttn;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster_size;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      n = 0;
+    for (int cs = 0; cs <= 2 * kMaxPairs; ++cs) {
+      int n = 0;
+      if (kern && cs >= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs, 1, 1);
+        cfg.blockDim = dim3(kThreadsAttn, 1, 1);
+        cfg.dynamicSmemBytes = kSmemAttn;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = 0;
+        }
+      }
+      cache[d][cs] = n;
     }
-    cache[cluster_size] = n;
-  }
-  return cache[cluster_size];
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return 0;
+  if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return cache[dev][cluster_size];
 }
 
 cudaError_t launch_attention(const AttnArgs& a, int B, cudaStream_t stream) {

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -13,6 +14,25 @@
 #include "../../include/ckv.h"
 
 namespace ckv {
+
+// ---- host: one-time setup per device, safe with several host threads ----
+constexpr int kOnceDevices = 64;
+struct DeviceOnce {
+  std::once_flag flag[kOnceDevices];
+  cudaError_t err[kOnceDevices] = {};
+};
+// Runs f() (returning cudaError_t) once for the current device; every later
+// call, from any thread, returns that first result.
+template <class F>
+inline cudaError_t once_per_device(DeviceOnce& o, F&& f) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kOnceDevices) return cudaErrorInvalidDevice;
+  std::call_once(o.flag[dev], [&] { o.err[dev] = f(dev); });
+  return o.err[dev];
+}
+
 
 // ------------------------------------------------------------ status ----
 // The first 256 bytes of every workspace: [0] sticky error code (the most

@@ -227,17 +227,16 @@ cudaError_t launch_index_simt(const IndexArgs& a, cudaStream_t stream) {
   using KernelFn = void (*)(IndexArgs);
   const KernelFn ks[4] = {index_topk_simt_kernel<8>, index_topk_simt_kernel<16>,
                           index_topk_simt_kernel<32>, index_topk_simt_kernel<64>};
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
+  static DeviceOnce once;
+  const cudaError_t e = once_per_device(once, [&](int) {
     for (KernelFn k : ks) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)sizeof(IndexSmem));
-      if (e != cudaSuccess) return e;
+      const cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)sizeof(IndexSmem));
+      if (r != cudaSuccess) return r;
     }
-    attr_dev = dev;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   static_assert(kMaxHI <= 64, "the widest instance covers every head count");
   const KernelFn kern = a.HI <= 8 ? ks[0] : a.HI <= 16 ? ks[1] : a.HI <= 32 ? ks[2] : ks[3];
   cudaLaunchConfig_t cfg = {};

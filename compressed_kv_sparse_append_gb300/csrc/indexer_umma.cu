@@ -294,15 +294,12 @@ bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
 }
 
 cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream_t stream) {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(index_topk_umma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemU);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  static DeviceOnce once;
+  const cudaError_t e = once_per_device(once, [](int) {
+    return cudaFuncSetAttribute(index_topk_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemU);
+  });
+  if (e != cudaSuccess) return e;
   CUtensorMap md, ms;
   if (!encode_tmap_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kdata, 64, (uint64_t)batch_rows, 64, 64,
                       (uint32_t)kUTile, CU_TENSOR_MAP_SWIZZLE_64B) ||

@@ -36,7 +36,12 @@
  *     expired record CKV_ERR_DEVICE_BOUNDS / CKV_ERR_TIMEOUT there, skip the
  *     offending access and never trap.  ckv_read_device_status() returns
  *     and clears it.  Calls that overlap on the GPU must use distinct
- *     workspaces.
+ *     workspaces.  One workspace may serve, one after another, the
+ *     ckv_csa_index_topk, ckv_csa_sparse_attn and ckv_hca_attn calls of a
+ *     step that share the batch size B (size it for the largest): the state
+ *     each keeps between calls (merge tickets, key histograms, merge
+ *     counters) sits at fixed offsets after the status word, and every
+ *     call's scratch lies beyond all of it.
  *   - Dimensions are fixed by the pages: main-KV entries are D = 512 with
  *     R = 64 RoPE dims, indexer keys are 128-d, heads H <= 128.
  */
@@ -95,7 +100,9 @@ typedef struct ckv_plane {
  * (output normalised by its own row sum, running max and sum) per CTA of a sequence in the
  * workspace for the final merge, plus one counter per sequence, layer and
  * half that elects the CTA doing the merge: about 1.1 MB per sequence and
- * layer. */
+ * layer.  The single-op calls (CKV_OP_INDEX_TOPK, CKV_OP_SPARSE_ATTN,
+ * CKV_OP_HCA_ATTN) also reserve the shared between-call state of all three
+ * for B (about 16 KB per sequence; see the workspace note above). */
 #define CKV_OP_APPEND      0
 #define CKV_OP_INDEX_TOPK  1
 #define CKV_OP_SPARSE_ATTN 2

@@ -48,11 +48,15 @@ def test_workspace_sizes(lib):
     b = f(1, 8, 128, 64, 262144, 512, 0)
     assert 256 < a < b
     assert f(1, 8, 64, 64, 65536, 512, 2048) > f(1, 8, 64, 64, 65536, 512, 0)
-    # attention: status word + the merge partials of up to 16 CTAs per
-    # sequence + one merge ticket per sequence and half (256-byte aligned)
+    # attention: status word + the shared between-call state (index tickets
+    # and 4096-bin histograms, then the attention's merge counters, each
+    # 256-byte aligned) + the merge partials of up to 16 CTAs per sequence
     part = 16 * (32 * 128 * 4 + 256) * 4
-    assert f(2, 3, 128, 0, 0, 0, 0) == 256 + 3 * part + 256
-    assert f(3, 3, 128, 0, 0, 0, 0) == 256 + 3 * part + 256
+    zero = 256 + 3 * 4096 * 4 + 256
+    assert f(2, 3, 128, 0, 0, 0, 0) == 256 + zero + 3 * part
+    assert f(3, 3, 128, 0, 0, 0, 0) == 256 + zero + 3 * part
+    # the index/top-k call reserves the same state before its candidates
+    assert f(1, 3, 128, 64, 4096, 512, 0) >= 256 + zero
     assert f(4, 8, 64, 64, 65536, 512, 2048) % 256 == 0
 
 
