@@ -60,6 +60,44 @@ __device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk
   }
 }
 
+// Of the kHistBins counts in hs (the last bin is the highest), finds the
+// bin holding the min(K, total)-th largest element.  Returns the bin; sets
+// total (all counts), keff = min(K, total) and above (the count in higher
+// bins).  Block-wide; hs is only read.
+template <int NT>
+__device__ uint32_t find_bin_desc(const uint32_t* hs, uint32_t K, MergeSmem<NT>& sm, uint32_t& total,
+                                  uint32_t& keff, uint32_t& above) {
+  constexpr int per = (kHistBins + NT - 1) / NT;   // descending bins, contiguous per thread
+  const int p0 = min(kHistBins, (int)threadIdx.x * per), p1 = min(kHistBins, p0 + per);
+  uint32_t cnt = 0;
+  for (int p = p0; p < p1; ++p) cnt += hs[kHistBins - 1 - p];
+  uint32_t before, d0, d1;
+  block_scan2<NT>(cnt, 0u, before, d0, total, d1, sm.sel);
+  keff = min(K, total);
+  if (threadIdx.x == 0) {
+    sm.bcast[0] = 0u;
+    sm.bcast[1] = 0u;
+  }
+  __syncthreads();
+  if (keff > 0 && before < keff && before + cnt >= keff) {
+    uint32_t cum = before;
+    for (int p = p0; p < p1; ++p) {
+      const uint32_t c = hs[kHistBins - 1 - p];
+      if (cum + c >= keff) {
+        sm.bcast[0] = (uint32_t)(kHistBins - 1 - p);
+        sm.bcast[1] = cum;
+        break;
+      }
+      cum += c;
+    }
+  }
+  __syncthreads();
+  const uint32_t bin = sm.bcast[0];
+  above = sm.bcast[1];
+  __syncthreads();
+  return bin;
+}
+
 // Merge of all chunks' candidates (run by the last CTA of sequence b).
 // surv_key / surv_ent: `surv_cap`-entry shared-memory scratch (>= kHistBins
 // words for surv_key).  Every global read is a coalesced 16-byte load.
@@ -96,33 +134,43 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     }
   }
   __syncthreads();
-  constexpr int per = (kHistBins + NT - 1) / NT;   // descending bins, contiguous per thread
-  const int p0 = min(kHistBins, (int)threadIdx.x * per), p1 = min(kHistBins, p0 + per);
-  uint32_t cnt = 0;
-  for (int p = p0; p < p1; ++p) cnt += hs[kHistBins - 1 - p];
-  uint32_t before, dummy, total, dummy2;
-  block_scan2<NT>(cnt, 0u, before, dummy, total, dummy2, sm.sel);
+  uint32_t total, keff, above;
+  const uint32_t tb = find_bin_desc<NT>(hs, (uint32_t)K, sm, total, keff, above);
   const int n_real = (int)total;
-  const uint32_t keff = (uint32_t)min(K, n_real);
-  if (threadIdx.x == 0) sm.bcast[0] = 0u;
-  __syncthreads();
-  if (keff > 0 && before < keff && before + cnt >= keff) {
-    uint32_t cum = before;
-    for (int p = p0; p < p1; ++p) {
-      const uint32_t c = hs[kHistBins - 1 - p];
-      if (cum + c >= keff) {
-        sm.bcast[0] = (uint32_t)(kHistBins - 1 - p);
-        break;
+  // Survivors are the candidates with key >= lo_key.  When the threshold
+  // bin is too crowded for shared memory (many exact ties at the boundary),
+  // a second histogram of the next 12 key bits over that bin's candidates
+  // narrows it first.
+  uint32_t lo_key = tb << kHistShift;
+  const uint32_t in_tb = hs[tb];
+  if (keff > 0 && above + in_tb > (uint32_t)surv_cap) {
+    __syncthreads();   // everyone has read hs[tb]
+    for (int i = threadIdx.x; i < kHistBins; i += NT) hs[i] = 0u;
+    __syncthreads();
+    constexpr int kV2 = 4;   // 16-byte loads in flight per thread
+    for (int base = 0; base < n_slots; base += 4 * kV2 * NT) {
+      uint4 k4[kV2];
+#pragma unroll
+      for (int v = 0; v < kV2; ++v) {
+        const int sv = base + 4 * (threadIdx.x + v * NT);
+        k4[v] = sv < n_slots ? __ldcg(reinterpret_cast<const uint4*>(ck + sv)) : make_uint4(0u, 0u, 0u, 0u);
       }
-      cum += c;
+#pragma unroll
+      for (int v = 0; v < kV2; ++v) {
+        const uint32_t kk[4] = {k4[v].x, k4[v].y, k4[v].z, k4[v].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (kk[e] != 0u && (kk[e] >> kHistShift) == tb) atomicAdd(&hs[(kk[e] >> 8) & 0xFFFu], 1u);
+      }
     }
+    __syncthreads();
+    uint32_t total2, keff2, above2;
+    const uint32_t tb2 = find_bin_desc<NT>(hs, keff - above, sm, total2, keff2, above2);
+    lo_key |= tb2 << 8;
   }
-  __syncthreads();
-  const uint32_t tb = sm.bcast[0];
-  __syncthreads();   // hs is reused below
   trace_at(a.st, tr, 20, t0);
 
-  // (b) survivors (key bin >= tb) in slot order, 16 slots per thread per
+  // (b) survivors (key >= lo_key) in slot order, 16 slots per thread per
   // pass; the next pass's loads are issued before this pass is compacted
   constexpr int kPer = 16;
   uint32_t n_surv = 0;
@@ -153,7 +201,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     if (base + kPer * NT < n_slots) fetch(base + kPer * NT);
     uint32_t f = 0;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) f |= (uint32_t)((kk[e] != 0u) && ((kk[e] >> kHistShift) >= tb)) << e;
+    for (int e = 0; e < kPer; ++e) f |= (uint32_t)((kk[e] != 0u) && (kk[e] >= lo_key)) << e;
     uint32_t pos, d0, tot, d1;
     block_scan2<NT>((uint32_t)__popc(f), 0u, pos, d0, tot, d1, sm.sel);
     if (n_surv + tot <= (uint32_t)surv_cap) {
