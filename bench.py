@@ -55,7 +55,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--graph", action="store_true",
-                   help="time replays of a CUDA graph of the step (off by default: see DESIGN.md)")
+                   help="time replays of a CUDA graph of the step (off by default; never taken for the CSA2 group, whose replay faulted)")
     return p.parse_args()
 
 
