@@ -1,0 +1,50 @@
+"""The bench's JSON contract, checked on the CPU through its reference arm
+(the float64 oracle timed on the host cores): one JSON line with the
+contract's keys, a positive value, and under torchrun (world size 2, gloo)
+one line from rank 0 only, every rank exiting 0."""
+
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ARGS = ["--impl", "reference", "--workload", "csa_tiny_4k", "--steps", "1", "--warmup", "0"]
+KEYS = ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+        "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"]
+
+
+def _check_line(line, n_gpus):
+    d = json.loads(line)
+    for k in KEYS:
+        assert k in d, k
+    assert d["impl"] == "reference"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["n_gpus"] == n_gpus and d["steps"] == 1 and d["warmup"] == 0
+    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["config"]["workload"] == "csa_tiny_4k"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py"] + ARGS, cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    _check_line(lines[0], 1)
+
+
+def test_reference_arm_under_torchrun_rank0_only():
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29517", "bench.py", "--gpus", "2"]
+                       + ARGS, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    _check_line(lines[0], 2)
