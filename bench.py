@@ -152,8 +152,8 @@ def setup_csa(wl, dev, ckv, wlmod):
     import torch
     B, n = wl.B, wl.n_comp
     cap = n + 8                     # room for the step's appended entry
-    kv = ckv.Plane(wl.main_fmt, 512, B, cap, dev)
-    win = ckv.Plane(wl.main_fmt, 512, B, wl.W, dev)
+    kv = ckv.Plane(wl.main_fmt, 512, B, cap, dev, nope_block=wl.nope_block)
+    win = ckv.Plane(wl.main_fmt, 512, B, wl.W, dev, nope_block=wl.nope_block)
     keys = ckv.Plane(wl.idx_fmt, 128, B, cap, dev)
     ws = ckv.new_workspace(256, dev)
     for b in range(B):
@@ -437,14 +437,15 @@ def cpu_oracle_sample(wl, budget_s):
             oa.hca_attention(f(q[0]), kd, ks, "bf16", n, wd, wsc, wl.W, wl.tau)
             layers = 1
         elif wl.kind == "csa":
-            kd, ks = ff.quantize_entries(kvf, wl.main_fmt)
-            wd, wsc = ff.quantize_entries(winf, wl.main_fmt)
+            kd, ks = ff.quantize_entries(kvf, wl.main_fmt, wl.nope_block)
+            wd, wsc = ff.quantize_entries(winf, wl.main_fmt, wl.nope_block)
             kk, kks = ff.quantize_entries(f(keys), wl.idx_fmt)
             kvals = ff.dequantize_entries(kk, kks, wl.idx_fmt)
             qv = oi.indexer_query(f(qi[0]), wl.idx_fmt == "fp4")
             sc = oi.index_scores(qv, f(w[0]).astype(np.float64), kvals)
             idx = oi.topk_set(sc, wl.topk)
-            oa.csa_sparse_attention(f(q[0]), kd, ks, wl.main_fmt, idx, wd, wsc, wl.W, wl.tau)
+            oa.csa_sparse_attention(f(q[0]), kd, ks, wl.main_fmt, idx, wd, wsc, wl.W, wl.tau,
+                                    nope_block=wl.nope_block)
             layers = 1
         else:
             kk, kks = ff.fp4_quantize(f(keys))
@@ -512,6 +513,7 @@ def workload_config(wl):
     return {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "context_tokens": wl.T,
             "compressed_entries": wl.n_comp, "heads": wl.H, "indexer_heads": wl.HI, "topk": wl.topk,
             "window": wl.W, "main_kv": wl.main_fmt, "indexer_keys": wl.idx_fmt or None,
+            "fp8_scale_block": wl.nope_block if wl.main_fmt == "mixed" else None,
             "layers_per_step": wl.n_layers, "l2": "flushed (1 GiB write) before every step"}
 
 

@@ -45,6 +45,7 @@ class Workload:
     pool_len: int = 0
     n_append: int = 0
     n_layers: int = 1
+    nope_block: int = 448  # channels per f32 scale of the MIXED format
     D: int = 512
     R: int = 64
     DI: int = 128
@@ -68,6 +69,10 @@ WORKLOADS = {
     # HCA decode, dense over 1M/128 BF16 entries.
     "hca_1m": Workload("hca_1m", "hca", B=16, T=1048576, ratio=128, H=128, HI=0, topk=0,
                        W=128, main_fmt="bf16", idx_fmt="", seed=1002),
+    # CSA decode at V4-Pro's own indexer setting: top-1024, and FP8 scales per
+    # 64 channels (the act_quant block reading), 128k context.
+    "csa_128k_pro": Workload("csa_128k_pro", "csa", B=8, T=131072, ratio=4, H=128, HI=64, topk=1024,
+                             W=128, main_fmt="mixed", idx_fmt="fp4", seed=1005, nope_block=64),
     # CSA decode at 1M context with ~5 % exact score ties.
     "csa_1m": Workload("csa_1m", "csa", B=4, T=1048576, ratio=4, H=128, HI=64, topk=512,
                        W=128, main_fmt="mixed", idx_fmt="fp4", seed=1003, ties=True),

@@ -22,13 +22,14 @@ def _fill(b, plane, rows, seq, cap):
     b.kv_append_quant(plane, rows, torch.arange(rows.shape[0], dtype=torch.int64, device="cuda") + seq * cap)
 
 
-@pytest.mark.parametrize("name,sample", [("csa_tiny_4k", [0]), ("csa_128k", [0, 5]), ("csa_1m", [2])])
+@pytest.mark.parametrize("name,sample", [("csa_tiny_4k", [0]), ("csa_128k", [0, 5]), ("csa_1m", [2]),
+                                         ("csa_128k_pro", [3])])
 def test_csa_full_size(name, sample):
     b = ckv()
     wl = wlmod.WORKLOADS[name]
     B, n, cap = wl.B, wl.n_comp, wl.n_comp + 8
-    kv = b.Plane(wl.main_fmt, 512, B, cap)
-    win = b.Plane(wl.main_fmt, 512, B, wl.W)
+    kv = b.Plane(wl.main_fmt, 512, B, cap, nope_block=wl.nope_block)
+    win = b.Plane(wl.main_fmt, 512, B, wl.W, nope_block=wl.nope_block)
     keys = b.Plane(wl.idx_fmt, 128, B, cap)
     q, qi, w = wlmod.step_queries(wl, 0, "cuda")
     rows = {}
@@ -65,10 +66,10 @@ def test_csa_full_size(name, sample):
         want = oi.topk_set(sc, wl.topk)
         ties_seen += int((sc == sc[want].min()).sum() > 1)
         sel = want[want >= 0]
-        kd, ks = ff.quantize_entries(np32(kvr)[sel], wl.main_fmt)
-        wd, wsc = ff.quantize_entries(np32(wr), wl.main_fmt)
+        kd, ks = ff.quantize_entries(np32(kvr)[sel], wl.main_fmt, wl.nope_block)
+        wd, wsc = ff.quantize_entries(np32(wr), wl.main_fmt, wl.nope_block)
         o_ref, l_ref = oa.csa_sparse_attention(np32(q[s]), kd, ks, wl.main_fmt, np.arange(len(sel)),
-                                               wd, wsc, wl.W, wl.tau)
+                                               wd, wsc, wl.W, wl.tau, nope_block=wl.nope_block)
         check_attention(out[s], lse[s], o_ref, l_ref, wl.H, where="%s seq %d" % (name, s))
     if wl.ties:
         assert ties_seen == len(sample), "tie injection must put exact ties on the boundary"
