@@ -48,7 +48,8 @@
  *     step that share the batch size B (size it for the largest): the state
  *     each keeps between calls (merge tickets, key histograms, merge
  *     counters) sits at fixed offsets after the status word, and every
- *     call's scratch lies beyond all of it.
+ *     call's scratch lies beyond all of it.  ckv_csa2_group_decode lays out
+ *     its workspace its own way: give it one of its own.
  *   - Dimensions are fixed by the pages: main-KV entries are D = 512 with
  *     R = 64 RoPE dims, indexer keys are 128-d, heads H <= 128.
  */
