@@ -4,14 +4,17 @@
 // ascending entry order in the workspace and adds them to a per-sequence
 // histogram of the top 12 key bits (global atomics).  The last CTA of the
 // sequence (atomic ticket, no spinning) then
-//   (a) finds the histogram bin holding the K-th largest key,
-//   (b) compacts, in order, the candidates in or above that bin into shared
-//       memory (one pass over the candidate lists),
+//   (a) finds the histogram bin holding the K-th largest key (and, when the
+//       candidates in or above it would not fit in shared memory, the bin of
+//       the next 12 key bits within it, from a second histogram over that
+//       bin's candidates),
+//   (b) compacts, in order, the candidates at or above that threshold into
+//       shared memory (one pass over the candidate lists),
 //   (c) runs the exact radix select on those survivors,
 // and writes the ascending top-k (and the CSA2 Full layer's pool).  Ties at
 // the threshold go to the earliest, i.e. lowest, entries ("DeepSeek-V4 KV
-// Cache 深度分析", §四: the indexer keeps the top-k blocks).  If the threshold
-// bin is too crowded for shared memory the select runs on the full lists.
+// Cache 深度分析", §四: the indexer keeps the top-k blocks).  If even that is
+// too crowded for shared memory the select runs on the full lists.
 #pragma once
 
 #include "select.cuh"
