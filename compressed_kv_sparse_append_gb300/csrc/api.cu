@@ -434,7 +434,7 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
     ckv_status s = check_attn_common(&g->kv[k], &g->win[k], win_len, B, g->q[l], H, g->out[l], sm_scale);
     if (s) return s;
     if (n_comp_max > g->kv[k].cap) return CKV_ERR_INVALID;
-    // one attention launch serves every layer: one cache format for all
+    // the group's attention launches share one kernel instance: one cache format for all
     if (g->kv[k].fmt != g->kv[g->kv_src[0]].fmt) return CKV_ERR_UNSUPPORTED;
   }
   (void)any_reindex;
