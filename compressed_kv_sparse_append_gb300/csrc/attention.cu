@@ -5,7 +5,8 @@
 // the 128-token window; §三 -- HCA attends densely to every ratio-128 entry
 // plus the window.  One softmax over the union of the rows (no sink).
 //
-// Decomposition (per sequence b, one thread-block cluster of 2G CTAs):
+// Decomposition (per sequence b, 2G CTAs: G pairs; a cluster is either all
+// 2G CTAs of the sequence or one pair, whichever lets more pairs run):
 //   * CTA (pair p, half c) owns latent dims [256c, 256c + 256).  TMEM:
 //     O_c = 128 heads x 256 f32 (columns 0..255), Q_c as the bf16 A operand
 //     (columns 256..383), two 128 x 64 f32 score buffers S (384..511); the
@@ -17,9 +18,11 @@
 //     (K = 256), swap S_c through distributed shared memory and add, so both
 //     hold the same S bit for bit and run the same online softmax; then each
 //     accumulates O_c += P . E_c (N = 256).
-//   * The G pairs merge (m, l, O) in the cluster at the end: CTA (p, c)
-//     finalises latent columns [256c + p*256/G, ...) from the G partial
-//     accumulators of half c read over DSMEM.
+//   * The G pairs merge (m, l, O) at the end through the workspace: every CTA
+//     writes its partial (O / l in fp16, (m, l) in f32; it stays in L2), the
+//     sequence's CTAs meet (the cluster barrier, or with pair clusters a
+//     bounded counter in the workspace), and CTA (p, c) finalises latent
+//     columns [256c + p*256/G, ...) from the G partials of half c.
 // Warp roles: warp 0 issues TMA for contiguous BF16 tiles (HCA); warps 1-4
 // gather + dequantise rows of the other formats (or zero the rows past the
 // end of a partial TMA tile); warp 5 owns TMEM and issues every tcgen05.mma;

@@ -15,8 +15,9 @@
 // ordered compaction resolves ties towards the lower index.
 //
 // Scoring engines:
-//   * score_simt: CUDA-core FMAs on dequantised values (BF16 keys, and the
-//     fallback for FP4 when a block-scaled tensor-core scorer is not used);
+//   * score_simt: CUDA-core FMAs on dequantised values (BF16 keys, the CSA2
+//     Reindex pass over a candidate pool, and FP4 keys when the block-scaled
+//     tensor-core scorer is not used);
 //   * the block-scaled tcgen05 scorer lives in indexer_umma.cu.
 
 #include "topk_merge.cuh"
