@@ -116,3 +116,89 @@ def test_append_multi_host_validation(lib):
     # an unsupported dim in the second plane
     odd = (CPlane * 2)(planes[0], CPlane(2, 256, 448, 1, 8, 0x30000, 0x40000))
     assert f(odd, src, slot, n, 2, ws, ctypes.c_size_t(256), None) in (-1, -2)
+
+
+def _index_args(**over):
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    vp = ctypes.c_void_p
+    keys = CPlane(2, 128, 448, 2, 64, 0x100000, 0x200000)   # FP4 indexer keys, B = 2, cap 64
+    a = dict(keys=keys, n_comp=vp(0x300000), B=2, n_comp_max=64, q=vp(0x400000), w=vp(0x500000),
+             HI=64, topk=16, pool=None, pool_len=0, out_idx=vp(0x600000), out_pool=None, pool_out=0,
+             dbg=None, ws=vp(0x700000), ws_bytes=ctypes.c_size_t(1 << 30), stream=None)
+    a.update(over)
+    return [ctypes.byref(a["keys"]), a["n_comp"], a["B"], a["n_comp_max"], a["q"], a["w"], a["HI"],
+            a["topk"], a["pool"], a["pool_len"], a["out_idx"], a["out_pool"], a["pool_out"], a["dbg"],
+            a["ws"], a["ws_bytes"], a["stream"]]
+
+
+def test_index_topk_host_validation(lib):
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    f = lib.ckv_csa_index_topk
+    f.restype = ctypes.c_int32
+    vp = ctypes.c_void_p
+    assert f(*_index_args(B=0)) == -1                          # no sequences
+    assert f(*_index_args(n_comp=None)) == -1                  # null lengths
+    assert f(*_index_args(q=vp(0x400008))) == -1               # misaligned query
+    assert f(*_index_args(HI=65)) == -2                        # more heads than supported
+    assert f(*_index_args(n_comp_max=65)) == -1                # longer than the plane
+    assert f(*_index_args(topk=4096)) == -2                    # k above 2048
+    assert f(*_index_args(topk=0)) == -2
+    # a pool both read and written; a pool smaller than k
+    assert f(*_index_args(pool=vp(0x800000), pool_len=32, out_pool=vp(0x900000), pool_out=32)) == -1
+    assert f(*_index_args(out_pool=vp(0x900000), pool_out=8)) == -1
+    # keys of the wrong width or format
+    assert f(*_index_args(keys=CPlane(2, 512, 448, 2, 64, 0x100000, 0x200000))) in (-1, -2)
+    assert f(*_index_args(keys=CPlane(1, 128, 448, 2, 64, 0x100000, 0x200000))) in (-1, -2)
+    # the workspace: missing, misaligned, too small
+    assert f(*_index_args(ws=None)) == -4
+    assert f(*_index_args(ws=vp(0x700010))) == -4
+    assert f(*_index_args(ws_bytes=ctypes.c_size_t(256))) == -4
+
+
+def _group(L=6, fmt=2):
+    from compressed_kv_sparse_append_gb300.binding import CGroup, CPlane
+    g = CGroup()
+    g.n_layers = L
+    for l in range(L):
+        g.role[l] = 0 if l == 0 else (1 if l == 1 else 2)
+        g.kv_src[l] = 0
+        g.idx_src[l] = 0 if l < 2 else l - 1
+        g.kv[l] = CPlane(fmt, 512, 448, 2, 64, 0x1000000 + l * 0x100000, 0x8000000 + l * 0x100000)
+        g.win[l] = CPlane(fmt, 512, 448, 2, 16, 0x2000000 + l * 0x100000, 0x9000000 + l * 0x100000)
+        g.q[l] = 0x3000000 + l * 0x10000
+        g.q_idx[l] = 0x4000000 + l * 0x10000 if l < 2 else None
+        g.w[l] = 0x5000000 + l * 0x10000 if l < 2 else None
+        g.out[l] = 0x6000000 + l * 0x10000
+    g.idx_keys = CPlane(2, 128, 448, 2, 64, 0x7000000, 0x7100000)
+    g.pool_len = 32
+    return g
+
+
+def test_csa2_group_host_validation(lib):
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    f = lib.ckv_csa2_group_decode
+    f.restype = ctypes.c_int32
+    vp = ctypes.c_void_p
+
+    def call(g, topk=16, ws_bytes=1 << 30):
+        return f(ctypes.byref(g), vp(0xA000000), 64, vp(0xB000000), 2, 64, 64, topk,
+                 ctypes.c_float(0.04), None, None, None, 0, vp(0xC000000), ctypes.c_size_t(ws_bytes), None)
+
+    g = _group(); g.n_layers = 0
+    assert call(g) == -1
+    g = _group(); g.n_layers = 9
+    assert call(g) == -1
+    g = _group(); g.role[0] = 1                     # the first layer must be a Full layer
+    assert call(g) == -1
+    g = _group(); g.idx_src[3] = 3                  # Reuse must name an earlier layer
+    assert call(g) == -1
+    g = _group(); g.kv_src[2] = 6                   # no such layer
+    assert call(g) == -1
+    g = _group(); g.role[4] = 7                     # no such role
+    assert call(g) == -1
+    g = _group(); g.pool_len = 8                    # pool smaller than k
+    assert call(g) == -1
+    g = _group(); g.kv_src[2] = 2; g.kv[2] = CPlane(1, 512, 448, 2, 64, 0x1200000, 0x8200000)
+    g.win[2] = CPlane(1, 512, 448, 2, 16, 0x2200000, 0x9200000)
+    assert call(g) == -2                            # one launch format across the layers
+    assert call(_group(), ws_bytes=256) == -4       # workspace too small
