@@ -109,7 +109,12 @@ def scale_shape(fmt: str, dim: int, nope_block: int = 448):
 
 class Plane:
     """A cache plane of ``batch`` sequences x ``cap`` entry slots in device
-    memory (data [batch, cap, entry_bytes] uint8, scale per format)."""
+    memory (data [batch, cap, entry_bytes] uint8, scale per format).
+
+    The C descriptor is built once and rebuilt whenever a field is
+    reassigned; replace ``data`` / ``scale`` by assignment, not by resizing
+    the tensors in place (that would move their storage behind the cached
+    pointers)."""
 
     def __init__(self, fmt, dim, batch, cap, device="cuda", nope_block=448, data=None, scale=None):
         self._c = None
