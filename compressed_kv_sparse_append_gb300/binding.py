@@ -60,6 +60,10 @@ lib.ckv_csa2_group_decode.argtypes = [ctypes.POINTER(CGroup), _vp, _i32, _vp, _i
 lib.ckv_csa_index_topk_static.restype = _i32
 lib.ckv_csa_index_topk_static.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp,
                                           _vp, _i32, _vp, _vp]
+lib.ckv_debug_wait_probe.restype = _i32
+lib.ckv_debug_wait_probe.argtypes = [_vp, _sz, _i32, ctypes.c_uint32, _vp]
+lib.ckv_read_static_status.restype = _i32
+lib.ckv_read_static_status.argtypes = [_vp]
 lib.ckv_read_device_status.restype = _i32
 lib.ckv_read_device_status.argtypes = [_vp, _vp]
 lib.ckv_status_string.restype = ctypes.c_char_p
@@ -200,7 +204,8 @@ def csa_index_topk(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, p
 def csa_index_topk_static(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=None, pool_out=0,
                           out_idx=None, out_pool=None, dbg_scores=None, stream=None):
     """csa_index_topk with the library's static device scratch instead of a
-    caller workspace (for callers that cannot allocate; see include/ckv.h)."""
+    caller workspace, for callers that cannot allocate device memory (see
+    include/ckv.h); its device status is read with read_static_status."""
     B, HI = q_idx.shape[0], q_idx.shape[1]
     dev = q_idx.device
     if out_idx is None:
@@ -275,6 +280,20 @@ def csa2_group_decode(group: CGroup, n_comp, n_comp_max, win_len, B, H, HI, topk
                                      _ptr(append_src), _ptr(append_slot), n_app, _ptr(ws), ws.numel(),
                                      _stream(stream)), "csa2_group_decode")
     return ws
+
+
+def debug_wait_probe(ws, mode, limit_us, stream=None):
+    """Runs one of the kernels' bounded waits on something nothing completes
+    (mode 0: an mbarrier phase; mode 1: a zero counter in ``ws``); the status
+    of ``ws`` then reads CKV_ERR_TIMEOUT (see include/ckv.h)."""
+    _check(lib.ckv_debug_wait_probe(_ptr(ws), ws.numel(), mode, limit_us, _stream(stream)),
+           "debug_wait_probe")
+
+
+def read_static_status(stream=None) -> int:
+    """Synchronises, returns and clears the sticky device status of the
+    static scratch used by csa_index_topk_static (current device)."""
+    return int(lib.ckv_read_static_status(_stream(stream)))
 
 
 def read_device_status(ws, stream=None) -> int:

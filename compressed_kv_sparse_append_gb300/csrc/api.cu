@@ -6,6 +6,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "indexer.cuh"
 #include "attention.cuh"
@@ -17,11 +19,47 @@ cudaError_t launch_append_multi(const ckv_plane* p, const void* const* src, cons
                                 const int32_t* n, int n_planes, DevStatus* st, cudaStream_t stream);
 }
 
+namespace ckv {
+
+// Makes one bounded wait of the kinds the kernels use run out: mode 0 an
+// mbarrier phase that nothing completes (the pipeline waits), mode 1 a
+// global counter that nothing increments (the cross-CTA merge wait).  The
+// wait records CKV_ERR_TIMEOUT in the status block after `limit_ns` and the
+// kernel returns; nothing else is touched.
+__global__ void wait_probe_kernel(DevStatus* st, const uint32_t* never_set, int mode, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (mode == 0) mbar_wait(&bar, 0, st, &abort_flag, 90, limit_ns);
+    else spin_until_geq(never_set, 1u, st, &abort_flag, 91, limit_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace ckv
+
 using namespace ckv;
 
 namespace {
 
 constexpr size_t kStatusBytes = 256;
+
+// An NVTX range named after the entry point around each call's host work
+// (validation and enqueue), so that a timeline tool shows which library call
+// issued which launches.  Without a tool attached each push/pop is a test of
+// an unset function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -312,6 +350,7 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t
 
 ckv_status ckv_kv_append_quant(const ckv_plane* dst, const void* src_bf16, const int64_t* slot,
                                int32_t n, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_kv_append_quant");
   if (n < 0) return CKV_ERR_INVALID;
   if (!dst) return CKV_ERR_INVALID;
   ckv_status s = check_plane(dst, dst->dim, 1);
@@ -327,6 +366,7 @@ ckv_status ckv_kv_append_quant(const ckv_plane* dst, const void* src_bf16, const
 ckv_status ckv_kv_append_quant_multi(const ckv_plane* dst, const void* const* src_bf16,
                                      const int64_t* const* slot, const int32_t* n, int32_t n_planes,
                                      void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_kv_append_quant_multi");
   if (!dst || !src_bf16 || !slot || !n || n_planes < 1 || n_planes > CKV_APPEND_MAX_PLANES)
     return CKV_ERR_INVALID;
   for (int k = 0; k < n_planes; ++k) {
@@ -350,6 +390,7 @@ ckv_status ckv_csa_index_topk(const ckv_plane* idx_keys, const int32_t* n_comp, 
                               int32_t HI, int32_t topk, const int32_t* pool, int32_t pool_len,
                               int32_t* out_idx, int32_t* out_pool, int32_t pool_out,
                               float* dbg_scores, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_csa_index_topk");
   ckv_status s = check_index_args(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool,
                                   pool_len, out_idx, out_pool, pool_out);
   if (s) return s;
@@ -368,6 +409,7 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
                                const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
                                int32_t H, float sm_scale, void* out_bf16, float* lse, void* ws,
                                size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_csa_sparse_attn");
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!idx || topk <= 0) return CKV_ERR_INVALID;
@@ -389,6 +431,7 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
                         const ckv_plane* win, const int32_t* win_len, int32_t B,
                         const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
                         float* lse, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_hca_attn");
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
   if (!n_comp || n_comp_max < 0 || n_comp_max > kv->cap) return CKV_ERR_INVALID;
@@ -411,6 +454,7 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
                                  const ckv_plane* append_dst, const void* append_src_bf16,
                                  const int64_t* append_slot, int32_t n_append, void* ws,
                                  size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_range("ckv_csa2_group_decode");
   if (!g || g->n_layers < 1 || g->n_layers > CKV_CSA2_MAX_LAYERS) return CKV_ERR_INVALID;
   const int L = g->n_layers;
   if (g->role[0] != CKV_CSA2_FULL) return CKV_ERR_INVALID;
@@ -448,6 +492,20 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   const size_t need = ckv_workspace_bytes(CKV_OP_CSA2, B, H, HI, n_comp_max, topk, pool_len);
   ckv_status s = check_ws(ws, ws_bytes, need);
   if (s) return s;
+  {
+    // Replaying a captured group call has faulted on GB300 with no cause
+    // found: refuse to be captured, before anything is enqueued.  A capture
+    // in global mode on another stream makes the legacy default stream's
+    // query fail with cudaErrorStreamCaptureImplicit: refused as well.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs);
+    if (ce == cudaErrorStreamCaptureImplicit) {
+      (void)cudaGetLastError();
+      return CKV_ERR_UNSUPPORTED;
+    }
+    if (ce != cudaSuccess) return cuda_status(ce);
+    if (cs != cudaStreamCaptureStatusNone) return CKV_ERR_UNSUPPORTED;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -512,6 +570,22 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   return CKV_OK;
 }
 
+ckv_status ckv_debug_wait_probe(void* ws, size_t ws_bytes, int32_t mode, uint32_t limit_us,
+                                void* stream) {
+  NvtxRange nvtx_range("ckv_debug_wait_probe");
+  if (mode != 0 && mode != 1) return CKV_ERR_INVALID;
+  if (limit_us < 1 || limit_us > 2000000u) return CKV_ERR_INVALID;
+  // mode 1 spins on the first word after the status block, which the
+  // caller keeps zero
+  ckv_status s = check_ws(ws, ws_bytes, kStatusBytes + (mode == 1 ? 256 : 0));
+  if (s) return s;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<DevStatus*>(w8), reinterpret_cast<const uint32_t*>(w8 + kStatusBytes), mode,
+      (uint64_t)limit_us * 1000ull);
+  return cuda_status(cudaGetLastError());
+}
+
 ckv_status ckv_read_device_status(void* ws, void* stream) {
   if (!ws) return CKV_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -548,6 +622,24 @@ const char* ckv_status_string(ckv_status s) {
 static __device__ __align__(256) uint8_t g_index_scratch[CKV_STATIC_SCRATCH_BYTES];
 static void* g_index_scratch_dev[kOnceDevices] = {};
 
+// Device address of the static scratch on the current device, looked up
+// once per device with that device current.
+static cudaError_t static_scratch(uint8_t** out) {
+  static DeviceOnce once;
+  const cudaError_t e = once_per_device(once, [](int d) {
+    void* p = nullptr;
+    const cudaError_t r = cudaGetSymbolAddress(&p, g_index_scratch);
+    g_index_scratch_dev[d] = p;
+    return r != cudaSuccess ? r : p == nullptr ? cudaErrorUnknown : cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  int dev = -1;
+  const cudaError_t g = cudaGetDevice(&dev);
+  if (g != cudaSuccess) return g;
+  *out = static_cast<uint8_t*>(g_index_scratch_dev[dev]);
+  return cudaSuccess;
+}
+
 extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const int32_t* n_comp,
                                                 int32_t B, int32_t n_comp_max,
                                                 const void* q_idx_bf16, const float* w,
@@ -555,6 +647,7 @@ extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const
                                                 int32_t pool_len, int32_t* out_idx,
                                                 int32_t* out_pool, int32_t pool_out,
                                                 float* dbg_scores, void* stream) {
+  NvtxRange nvtx_range("ckv_csa_index_topk_static");
   ckv_status s = check_index_args(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool,
                                   pool_len, out_idx, out_pool, pool_out);
   if (s) return s;
@@ -562,22 +655,30 @@ extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const
   const int K_sel = out_pool ? pool_out : topk;
   const IndexLayout L = index_layout(B, n_comp_max, K_sel, pool_mode, pool_mode ? pool_len : 0);
   if (kStatusBytes + L.bytes > (size_t)CKV_STATIC_SCRATCH_BYTES) return CKV_ERR_WORKSPACE;
-  static DeviceOnce once;
-  int dev = -1;
-  const cudaError_t e = once_per_device(once, [](int d) {
-    void* p = nullptr;
-    const cudaError_t r = cudaGetSymbolAddress(&p, g_index_scratch);
-    g_index_scratch_dev[d] = p;
-    return r != cudaSuccess ? r : p == nullptr ? cudaErrorUnknown : cudaSuccess;
-  });
-  if (e != cudaSuccess) return cuda_status(e);
-  if (cudaGetDevice(&dev) != cudaSuccess) return CKV_ERR_CUDA;
-  uint8_t* w8 = static_cast<uint8_t*>(g_index_scratch_dev[dev]);
+  uint8_t* w8 = nullptr;
+  s = cuda_status(static_scratch(&w8));
+  if (s) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // status, per-sequence tickets and key histograms must start at zero
-  s = cuda_status(cudaMemsetAsync(w8, 0, kStatusBytes + L.key_off, st));
+  // The per-sequence tickets and histograms must start at zero (a call
+  // that ran with other sizes may have left its own layout's state behind).
+  // The status word is not cleared: it is sticky until
+  // ckv_read_static_status reads it.
+  s = cuda_status(cudaMemsetAsync(w8 + kStatusBytes, 0, L.key_off, st));
   if (s) return s;
   return run_index(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool, pool_len,
                    out_idx, out_pool, pool_out, dbg_scores, reinterpret_cast<DevStatus*>(w8),
                    w8 + kStatusBytes, st);
+}
+
+extern "C" ckv_status ckv_read_static_status(void* stream) {
+  NvtxRange nvtx_range("ckv_read_static_status");
+  uint8_t* w8 = nullptr;
+  ckv_status s = cuda_status(static_scratch(&w8));
+  if (s) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  int32_t code = 0;
+  if (cudaMemcpy(&code, w8, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return CKV_ERR_CUDA;
+  if (code != 0 && cudaMemset(w8, 0, kStatusBytes) != cudaSuccess) return CKV_ERR_CUDA;
+  return code;
 }

@@ -362,7 +362,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const AttnArgs& a = batch.layer[blockIdx.z];
   if (a.tag != (kArgsTag ^ (int)blockIdx.z)) {
     // a damaged argument block: touch none of its pointers (every CTA of
-    // the cluster takes this branch, so none waits on the others)
+    // the cluster takes this branch, so none waits on the others).  The CTA
+    // still waits for the previous grid before it leaves: a grid whose CTAs
+    // all left without waiting could complete before its predecessor and
+    // release the next launch of the stream too early.
+    pdl_wait();
     if (threadIdx.x == 0) report(batch.layer[0].st, CKV_ERR_INVALID, (int)blockIdx.z);
     return;
   }
@@ -969,18 +973,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   if (tid == 0 && !a.cluster_all) {
     __threadfence();
     atomicAdd(cnt, 1u);
-    const uint64_t g0 = globaltimer();
-    for (uint32_t it = 0;; ++it) {
-      uint32_t v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-      if (v >= (uint32_t)(2 * G)) break;
-      if (*abort_p || it >= kWaitLimitIters || globaltimer() - g0 > kWaitLimitNs) {
-        report(a.st, CKV_ERR_TIMEOUT, 31);
-        *abort_p = 1;
-        break;
-      }
-      __nanosleep(64);
-    }
+    spin_until_geq(cnt, (uint32_t)(2 * G), a.st, abort_p, 31);
   }
   __syncthreads();
   if (tid == 0) stamp3(2);

@@ -122,7 +122,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // Bounded polling wait (non-suspending test_wait) for barriers whose
 // arrivals come from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, DevStatus* st,
-                                               volatile int* abort, int where) {
+                                               volatile int* abort, int where,
+                                               uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer();
   const long long c0 = clock64();
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, D
     if ((it & 255u) == 255u) {
       if (*abort) return false;
       if (it >= 16u * kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
-          globaltimer() - t0 > kWaitLimitNs) {
+          globaltimer() - t0 > limit_ns) {
         report(st, CKV_ERR_TIMEOUT, where);
         *abort = 1;
         return false;
@@ -144,7 +145,8 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, D
 // it records CKV_ERR_TIMEOUT (detail = `where`), raises *abort and returns
 // false; once *abort is set every later wait returns false at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevStatus* st,
-                                          volatile int* abort, int where) {
+                                          volatile int* abort, int where,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -154,12 +156,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevSta
     if ((it & 63u) == 0) {
       if (*abort) return false;
       if (it >= kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
-          globaltimer() - t0 > kWaitLimitNs) {
+          globaltimer() - t0 > limit_ns) {
         report(st, CKV_ERR_TIMEOUT, where);
         *abort = 1;
         return false;
       }
     }
+  }
+}
+
+// Bounded spin of one thread until the global counter *cnt reaches
+// `target` (acquire at GPU scope, so the writes released before each
+// increment are visible once it returns true).  On expiry it records
+// CKV_ERR_TIMEOUT (detail = `where`), raises *abort and returns false.
+__device__ __forceinline__ bool spin_until_geq(const uint32_t* cnt, uint32_t target, DevStatus* st,
+                                               volatile int* abort, int where,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const uint64_t g0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) return true;
+    if (*abort || it >= kWaitLimitIters || globaltimer() - g0 > limit_ns) {
+      if (!*abort) report(st, CKV_ERR_TIMEOUT, where);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
   }
 }
 

@@ -188,23 +188,24 @@ ckv_status ckv_csa_index_topk(const ckv_plane *idx_keys, const int32_t *n_comp,
 
 /* csa_index_topk for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment convenience.  Some callers cannot
- * call cudaMalloc at all -- code running inside a CUDA graph being captured,
- * plug-ins of serving engines that own every allocation, or embedded
- * runtimes with a fixed memory plan -- and so cannot provide the workspace
- * of ckv_csa_index_topk.  This entry point computes exactly the same outputs
- * with its scratch in a statically sized device array inside libckv
- * (CKV_STATIC_SCRATCH_BYTES, held on every GPU that loads the library until
- * the process exits); it allocates nothing.
+ * call cudaMalloc at all -- plug-ins of serving engines that own every device
+ * allocation, or embedded runtimes whose memory plan is fixed before they
+ * start -- and so cannot provide the workspace of ckv_csa_index_topk.  This
+ * entry point computes exactly the same outputs with its scratch in a
+ * statically sized device array inside libckv (CKV_STATIC_SCRATCH_BYTES, held
+ * on every GPU that loads the library until the process exits); it calls no
+ * allocating routine.
  *   Arguments as ckv_csa_index_topk, without ws / ws_bytes.
  *   Returns CKV_ERR_WORKSPACE when the call needs more scratch than
  *   CKV_STATIC_SCRATCH_BYTES (see ckv_workspace_bytes(CKV_OP_INDEX_TOPK, ...)).
  *   The first call on a device looks the array up (cudaGetSymbolAddress)
  *   with that device current: make that first call before any stream
- *   capture.  Every call clears the scratch's counters on `stream` first.
- *   All calls share the one array: calls that overlap on the GPU (different
- *   streams, or graphs replayed concurrently) race and must be serialised by
- *   the caller.  Device-side range errors are recorded in the array's status
- *   word, which this entry point does not report. */
+ *   capture.  Every call first clears the scratch's counters on `stream`.
+ *   All calls share the one array, which keeps the last call's contents:
+ *   calls that overlap on the GPU (different streams) race and must be
+ *   serialised by the caller.  Device-side range errors (a pool entry at or
+ *   beyond n_comp) are recorded in the array's own sticky status word; read
+ *   it with ckv_read_static_status. */
 #define CKV_STATIC_SCRATCH_BYTES (8u << 20)
 ckv_status ckv_csa_index_topk_static(const ckv_plane *idx_keys, const int32_t *n_comp,
                                      int32_t B, int32_t n_comp_max,
@@ -212,6 +213,12 @@ ckv_status ckv_csa_index_topk_static(const ckv_plane *idx_keys, const int32_t *n
                                      int32_t topk, const int32_t *pool, int32_t pool_len,
                                      int32_t *out_idx, int32_t *out_pool, int32_t pool_out,
                                      float *dbg_scores, void *stream);
+
+/* Synchronises `stream`, returns the sticky device status of the static
+ * scratch of ckv_csa_index_topk_static on the current device (CKV_OK,
+ * CKV_ERR_DEVICE_BOUNDS or CKV_ERR_TIMEOUT) and clears it.  The pages have no
+ * counterpart. */
+ckv_status ckv_read_static_status(void *stream);
 
 /* CSA sparse attention ([KVC] §十一 flow chart: attention over the selected
  * entries followed by the sliding window; §五: each entry is both key and
@@ -252,9 +259,10 @@ ckv_status ckv_hca_attn(const ckv_plane *kv, const int32_t *n_comp,
  * n_append rows to `append_dst` (as ckv_kv_append_quant).  The layers'
  * attention runs in launches of at most four layers each (six layers: two
  * launches of three), so that every launch's parameter block stays within
- * the classic 4 KB.  Do not capture this call into a CUDA graph: replaying
- * such a graph faulted (illegal address) on GB300, cause not yet found;
- * eager calls are not affected. */
+ * the classic 4 KB.  The call refuses to be captured into a CUDA graph: on
+ * a capturing stream it returns CKV_ERR_UNSUPPORTED and enqueues nothing
+ * (replaying a captured group call faulted on GB300, cause not found; eager
+ * calls are not affected). */
 #define CKV_CSA2_FULL    0
 #define CKV_CSA2_REINDEX 1
 #define CKV_CSA2_REUSE   2
@@ -283,6 +291,20 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group *g, const int32_t *n_comp,
                                  const void *append_src_bf16,
                                  const int64_t *append_slot, int32_t n_append,
                                  void *ws, size_t ws_bytes, void *stream);
+
+/* Failure-path check of the bounded waits (the pages have no counterpart).
+ * Every spin-wait in the kernels gives up after a limit (2 s), records
+ * CKV_ERR_TIMEOUT in the workspace status word and lets the kernel return,
+ * so that a lost arrival never hangs the GPU.  This call launches one small
+ * kernel that runs the same wait code on something nothing will complete:
+ *   mode 0  an mbarrier phase (as the pipelines' producer/consumer waits);
+ *   mode 1  the first 32-bit word after the status block, which must be
+ *           zero (as the cross-CTA merge counters); needs ws_bytes >= 512.
+ * The wait gives up after limit_us (1 .. 2,000,000) microseconds; the
+ * status then reads CKV_ERR_TIMEOUT (ckv_read_device_status) and the GPU
+ * context stays usable.  Asynchronous on `stream`. */
+ckv_status ckv_debug_wait_probe(void *ws, size_t ws_bytes, int32_t mode, uint32_t limit_us,
+                                void *stream);
 
 /* Synchronises `stream`, returns the sticky device status recorded in `ws`
  * (CKV_OK, CKV_ERR_DEVICE_BOUNDS or CKV_ERR_TIMEOUT; CKV_ERR_INVALID if an

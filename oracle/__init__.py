@@ -21,9 +21,9 @@ Sources (titles of the pages, with the section each function follows):
     Reuse, hierarchical indexer pool, FP4 main KV).
   * "DeepSeek V4 의 정확한 KV 캐시 사용량 분석" -- per-token byte arithmetic.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-except ``v41_flash_bytes_per_token`` (the 890 B/token figure cannot be
-derived from the pages: parity unpinned).
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``.
+The pages' 890 B/token figure for V4.1-Flash cannot be derived from what they
+print, so no function computes it.
 """
 
 from . import fp_formats, sizes, indexer, attention, csa2  # noqa: F401

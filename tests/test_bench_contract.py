@@ -9,7 +9,8 @@ import subprocess
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-ARGS = ["--impl", "reference", "--workload", "csa_tiny_4k", "--steps", "1", "--warmup", "0"]
+ARGS = ["--impl", "reference", "--workload", "csa_tiny_4k", "--steps", "1", "--warmup", "0",
+        "--ref-seconds", "2"]
 KEYS = ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
         "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"]
 

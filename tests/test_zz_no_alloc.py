@@ -1,11 +1,14 @@
 """The allocation-free index/top-k entry point.
 
-Some callers cannot allocate device memory (code inside a CUDA graph being
-captured, serving-engine plug-ins whose memory plan is fixed); for them
+Some callers cannot allocate device memory (serving-engine plug-ins that own
+every allocation, embedded runtimes whose memory plan is fixed); for them
 ckv_csa_index_topk_static keeps its scratch in a static device array inside
-libckv.  This test calls it through the C ABI twice in a row and checks that
+libckv.  These tests call it through the C ABI twice in a row and check that
 both calls give exactly what the workspace entry point gives on the same
-inputs.  It lives in a file pytest collects last."""
+inputs, and that a device-side range error stays readable through
+ckv_read_static_status.  They live in a file pytest collects last."""
+
+import numpy as np
 
 import pytest
 import torch
@@ -50,3 +53,27 @@ def test_static_scratch_rejects_oversized_calls():
     with pytest.raises(b.CkvError) as e:
         b.csa_index_topk_static(plane, n_comp, 1 << 20, qi, w, 2048)
     assert e.value.code == -4
+
+
+def test_static_scratch_reports_out_of_range_pool_entry():
+    """A pool entry at or beyond n_comp is skipped and recorded; the record
+    survives the next call's clearing of the counters and reads once."""
+    from oracle import fp_formats as ff
+    from oracle import indexer as oi
+    b = ckv()
+    keys = [wl.rms_rows((100, 128), 4300, "cuda")]
+    plane = gpu_plane("fp4", 128, keys, 100)
+    qi = wl.rms_rows((1, 8, 128), 4301, "cuda")
+    w = wl.head_weights((1, 8), 4302, "cuda")
+    n_comp = torch.tensor([100], dtype=torch.int32, device="cuda")
+    pool = torch.tensor([[5, 7, 250, -1, 9]], dtype=torch.int32, device="cuda")
+    assert b.read_static_status() in (0, -6)        # whatever earlier tests left
+    idx = b.csa_index_topk_static(plane, n_comp, 100, qi, w, 2, pool=pool)
+    good = torch.tensor([[5, 7, 9]], dtype=torch.int32, device="cuda")
+    b.csa_index_topk_static(plane, n_comp, 100, qi, w, 2, pool=good)
+    assert b.read_static_status() == -6
+    assert b.read_static_status() == 0
+    kd, ks = ff.fp4_quantize(keys[0].float().cpu().numpy())
+    sc = oi.index_scores(oi.indexer_query(qi[0].float().cpu().numpy(), True),
+                         w[0].cpu().numpy().astype(np.float64), ff.fp4_dequantize(kd, ks))
+    assert list(idx.cpu().numpy()[0]) == list(oi.topk_set(sc, 2, candidates=[5, 7, 9]))
