@@ -84,28 +84,29 @@ ckv_status check_plane(const ckv_plane* p, int dim, int B) {
 }
 
 struct IndexLayout {
-  int chunk, n_chunks, K_sel;
-  size_t counters_off, hist_off, key_off, idx_off, bytes;  // relative to the index region
+  int chunk, n_chunks;
+  size_t seq_off, hist_off, count_off, key_off, idx_off, bytes;  // relative to the index region
 };
-
-// Candidate rows hold K_sel slots, a multiple of 4 (16-byte rows).
-int pad4(int k) { return (k + 3) & ~3; }
 
 // Between-call state of the single-op calls, at fixed offsets after the
 // status block, so that index/top-k and attention calls with the same B may
 // share one workspace: every op's scratch starts after all of it.
-//   [0, index_zero_bytes)   index: per-sequence merge tickets, then the
-//                           per-sequence 4096-bin key histograms
+//   [0, index_zero_bytes)   index: per-sequence state (merge ticket, the
+//                           range of histogram bins in use), then the
+//                           per-sequence 8192-bin key histograms
 //   [.., + attn_zero_bytes) attention: per-sequence, per-half merge counters
 // Each op leaves its own part zero when it finishes.
-size_t index_zero_bytes(int B) { return align_up((size_t)B * 4, 256) + (size_t)B * 4096 * 4; }
+size_t index_zero_bytes(int B) {
+  return align_up((size_t)B * kSeqWords * 4, 256) + (size_t)B * kBins * 4;
+}
 size_t attn_zero_bytes(int B) { return align_up((size_t)B * 2 * sizeof(uint32_t), 256); }
 size_t shared_zero_bytes(int B) { return index_zero_bytes(B) + attn_zero_bytes(B); }
 
-IndexLayout index_layout(int B, int n_comp_max, int K_sel_in, bool pool_mode, int pool_len) {
+// Chunking of one index pass and the scratch after the shared state: per
+// chunk its candidate count and real-key count, then candidate keys and
+// entries (one slot per entry of the chunk, the most a chunk can keep).
+IndexLayout index_layout(int B, int n_comp_max, bool pool_mode, int pool_len) {
   IndexLayout L;
-  const int K_sel = pad4(K_sel_in);
-  L.K_sel = K_sel;
   if (pool_mode) {
     L.chunk = 256;
     L.n_chunks = (pool_len + 255) / 256;
@@ -120,10 +121,11 @@ IndexLayout index_layout(int B, int n_comp_max, int K_sel_in, bool pool_mode, in
     L.n_chunks = (n_comp_max + c - 1) / c;
     if (L.n_chunks < 1) L.n_chunks = 1;
   }
-  L.counters_off = 0;
-  L.hist_off = align_up((size_t)B * 4, 256);
-  L.key_off = shared_zero_bytes(B);   // candidates after the attention's counters too
-  const size_t cand = (size_t)B * L.n_chunks * K_sel * 4;
+  L.seq_off = 0;
+  L.hist_off = align_up((size_t)B * kSeqWords * 4, 256);
+  L.count_off = shared_zero_bytes(B);   // scratch after the attention's counters too
+  const size_t cand = (size_t)B * L.n_chunks * L.chunk * 4;
+  L.key_off = L.count_off + align_up((size_t)B * L.n_chunks * 8, 256);
   L.idx_off = L.key_off + align_up(cand, 256);
   L.bytes = L.idx_off + align_up(cand, 256);
   return L;
@@ -166,8 +168,7 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
                      const void* q_idx, const float* w, int HI, int topk, const int32_t* pool,
                      int pool_len, int32_t* out_idx, int32_t* out_pool, int pool_out, float* dbg,
                      DevStatus* st, uint8_t* region, cudaStream_t stream) {
-  const int K_sel = pad4(out_pool ? pool_out : topk);
-  IndexLayout L = index_layout(B, n_comp_max, K_sel, pool != nullptr, pool_len);
+  IndexLayout L = index_layout(B, n_comp_max, pool != nullptr, pool_len);
   IndexArgs a;
   a.kdata = static_cast<const uint8_t*>(keys->data);
   a.kscale = static_cast<const uint8_t*>(keys->scale);
@@ -183,11 +184,11 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.pool_len = pool_len;
   a.topk = topk;
   a.pool_out = out_pool ? pool_out : 0;
-  a.K_sel = K_sel;
   a.chunk = L.chunk;
   a.n_chunks = L.n_chunks;
-  a.counters = reinterpret_cast<uint32_t*>(region + L.counters_off);
+  a.seq_state = reinterpret_cast<uint32_t*>(region + L.seq_off);
   a.ghist = reinterpret_cast<uint32_t*>(region + L.hist_off);
+  a.ccount = reinterpret_cast<uint32_t*>(region + L.count_off);
   a.cand_key = reinterpret_cast<uint32_t*>(region + L.key_off);
   a.cand_idx = reinterpret_cast<int32_t*>(region + L.idx_off);
   a.out_idx = out_idx;
@@ -213,6 +214,8 @@ ckv_status check_index_args(const ckv_plane* keys, const int32_t* n_comp, int B,
   if (HI <= 0 || HI > kMaxHI) return CKV_ERR_UNSUPPORTED;
   if (n_comp_max < 0 || n_comp_max > keys->cap) return CKV_ERR_INVALID;
   if (topk <= 0 || topk > kMaxPool) return CKV_ERR_UNSUPPORTED;
+  if (index_layout(B, n_comp_max, pool != nullptr, pool_len).n_chunks > kMaxChunksPerSeq)
+    return CKV_ERR_UNSUPPORTED;
   if (pool) {
     if (out_pool || pool_len <= 0 || pool_len > kMaxChunk) return CKV_ERR_INVALID;
   }
@@ -220,10 +223,9 @@ ckv_status check_index_args(const ckv_plane* keys, const int32_t* n_comp, int B,
   return CKV_OK;
 }
 
-// Scratch of one index pass: K_sel candidates per chunk (pool_out for a
-// CSA2 Full layer, else topk); a pool-mode pass is one chunk of pool_len.
-size_t index_ws_bytes(int B, int n_comp_max, int K_sel, bool pool_mode, int pool_len) {
-  return index_layout(B, n_comp_max, K_sel, pool_mode, pool_len).bytes;
+// Scratch of one index pass; a pool-mode pass chunks the pool.
+size_t index_ws_bytes(int B, int n_comp_max, bool pool_mode, int pool_len) {
+  return index_layout(B, n_comp_max, pool_mode, pool_len).bytes;
 }
 
 // The attention's split-KV merge state: the partials of up to 2 * kMaxPairs
@@ -331,10 +333,10 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI, int32_t
       // pool_len here: the pool_out of a CSA2 Full pass (0 for none); a
       // pool-mode (Reindex) pass never needs more than a full pass.
       return kStatusBytes +
-             index_ws_bytes(B, n_comp_max, pool_len > topk ? pool_len : topk, false, 0);
+             index_ws_bytes(B, n_comp_max, false, 0);
     case CKV_OP_CSA2: {
-      size_t full = index_ws_bytes(B, n_comp_max, pool_len, false, 0);
-      size_t re = index_ws_bytes(B, n_comp_max, topk, true, pool_len);
+      size_t full = index_ws_bytes(B, n_comp_max, false, 0);
+      size_t re = index_ws_bytes(B, n_comp_max, true, pool_len);
       size_t idx_region = align_up(full > re ? full : re, 256);
       size_t pool = align_up((size_t)B * (pool_len > 0 ? pool_len : 1) * 4, 256);
       size_t idxbuf = align_up((size_t)CKV_CSA2_MAX_LAYERS * B * topk * 4, 256);
@@ -395,8 +397,7 @@ ckv_status ckv_csa_index_topk(const ckv_plane* idx_keys, const int32_t* n_comp, 
                                   pool_len, out_idx, out_pool, pool_out);
   if (s) return s;
   const bool pool_mode = pool != nullptr;
-  const size_t need = kStatusBytes + index_ws_bytes(B, n_comp_max, out_pool ? pool_out : topk,
-                                                    pool_mode, pool_mode ? pool_len : 0);
+  const size_t need = kStatusBytes + index_ws_bytes(B, n_comp_max, pool_mode, pool_mode ? pool_len : 0);
   s = check_ws(ws, ws_bytes, need);
   if (s) return s;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -510,8 +511,8 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   DevStatus* dst = reinterpret_cast<DevStatus*>(w8);
-  const size_t full = index_ws_bytes(B, n_comp_max, pool_len, false, 0);
-  const size_t re = index_ws_bytes(B, n_comp_max, topk, true, pool_len);
+  const size_t full = index_ws_bytes(B, n_comp_max, false, 0);
+  const size_t re = index_ws_bytes(B, n_comp_max, true, pool_len);
   uint8_t* idx_region = w8 + kStatusBytes;
   int32_t* pool_buf = reinterpret_cast<int32_t*>(idx_region + align_up(full > re ? full : re, 256));
   int32_t* idxbuf = pool_buf + align_up((size_t)B * pool_len * 4, 256) / 4;
@@ -652,8 +653,7 @@ extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const
                                   pool_len, out_idx, out_pool, pool_out);
   if (s) return s;
   const bool pool_mode = pool != nullptr;
-  const int K_sel = out_pool ? pool_out : topk;
-  const IndexLayout L = index_layout(B, n_comp_max, K_sel, pool_mode, pool_mode ? pool_len : 0);
+  const IndexLayout L = index_layout(B, n_comp_max, pool_mode, pool_mode ? pool_len : 0);
   if (kStatusBytes + L.bytes > (size_t)CKV_STATIC_SCRATCH_BYTES) return CKV_ERR_WORKSPACE;
   uint8_t* w8 = nullptr;
   s = cuda_status(static_scratch(&w8));
@@ -663,7 +663,7 @@ extern "C" ckv_status ckv_csa_index_topk_static(const ckv_plane* idx_keys, const
   // that ran with other sizes may have left its own layout's state behind).
   // The status word is not cleared: it is sticky until
   // ckv_read_static_status reads it.
-  s = cuda_status(cudaMemsetAsync(w8 + kStatusBytes, 0, L.key_off, st));
+  s = cuda_status(cudaMemsetAsync(w8 + kStatusBytes, 0, index_zero_bytes(B), st));
   if (s) return s;
   return run_index(idx_keys, n_comp, B, n_comp_max, q_idx_bf16, w, HI, topk, pool, pool_len,
                    out_idx, out_pool, pool_out, dbg_scores, reinterpret_cast<DevStatus*>(w8),

@@ -6,19 +6,22 @@
 // Score (workload definition): s_j = sum_h w_h * ReLU(q_h . k_j) on the
 // dequantised values; for FP4 keys the query is block-quantised first.
 //
-// Grid (chunk, sequence).  Each CTA scores one chunk of entries, keeps the
-// chunk's top-K candidates (K = max(topk, pool_out)) with the radix select of
-// select.cuh and writes them to the workspace; the last CTA of a sequence to
-// finish (atomic ticket, no spinning) merges the candidate lists into the
-// exact top-K, and for a CSA2 Full layer also the top-k of that pool.
-// Candidate lists are stored in ascending entry order, so the merge's
-// ordered compaction resolves ties towards the lower index.
+// Grid (chunk, sequence).  Each CTA scores one chunk of entries, histograms
+// their keys, and writes the keys above a lower bound on the sequence's
+// threshold (from the sequence histogram in the workspace) as its
+// candidates; the last CTA of a sequence to finish (atomic ticket, no
+// spinning) merges them into the exact top-K, and for a CSA2 Full layer also
+// the top-k of that pool (topk_merge.cuh).  Candidate lists are in ascending
+// entry order, so the merge's ordered compaction resolves ties towards the
+// lower index.
 //
 // Scoring engines:
 //   * score_simt: CUDA-core FMAs on dequantised values (BF16 keys, the CSA2
 //     Reindex pass over a candidate pool, and FP4 keys when the block-scaled
 //     tensor-core scorer is not used);
 //   * the block-scaled tcgen05 scorer lives in indexer_umma.cu.
+
+#include <cstddef>
 
 #include "topk_merge.cuh"
 
@@ -29,10 +32,13 @@ constexpr int kIdxThreads = 512;
 struct IndexSmem {
   float q[kMaxHI * kIdxDim];       // dequantised indexer query
   float w[kMaxHI];
-  uint32_t keys[kMaxChunk];        // scores of this chunk as order keys
+  uint32_t keys[kMaxChunk];        // scores of this chunk as order keys (0 = no entry)
+  uint32_t hist[kBins];            // their histogram (top kBinBits bits)
   float part[kIdxThreads];         // half-head partial scores (two threads per key)
   MergeSmem<kIdxThreads> m;
 };
+static_assert(offsetof(IndexSmem, hist) == offsetof(IndexSmem, keys) + kMaxChunk * 4,
+              "keys and hist are one block of merge scratch");
 
 // Dequantised indexer query into shared memory: FP4 keys -> the query is
 // quantised with the E2M1 + E4M3/16 block quantiser (the same arithmetic as
@@ -157,7 +163,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
   const long long t0 = clock64();
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
   load_query(a, b, sm.q, sm.w);
-  if (threadIdx.x == 0) sm.m.n_real = 0;
+  merge_smem_init<kIdxThreads>(sm.m);
+  for (int i = threadIdx.x; i < kBins / 4; i += kIdxThreads)
+    reinterpret_cast<uint4*>(sm.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   trace_at(a.st, tr, 0, t0);
 
@@ -217,9 +225,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_topk_simt_kernel(IndexAr
   }
   atomicAdd(&sm.m.n_real, mine);
   __syncthreads();
+  // histogram and range of the real keys
+  {
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+    for (int i = threadIdx.x; i < n_elem; i += kIdxThreads) {
+      const uint32_t u = sm.keys[i];
+      if (u != 0u) {
+        atomicAdd(&sm.hist[key_bin(u)], 1u);
+        kmin = min(kmin, u);
+        kmax = max(kmax, u);
+      }
+    }
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    if ((threadIdx.x & 31) == 0) {
+      atomicMin(&sm.m.kmin, kmin);
+      atomicMax(&sm.m.kmax, kmax);
+    }
+  }
+  __syncthreads();
   trace_at(a.st, tr, 9, t0);
-  chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.keys, kMaxChunk / 2,
-                                      sm.m);
+  chunk_select_and_merge<kIdxThreads>(a, b, chunk, n_elem, first, sm.keys, sm.hist, sm.keys,
+                                      kMaxChunk + kBins, sm.m);
 }
 
 size_t index_smem_bytes() { return sizeof(IndexSmem); }

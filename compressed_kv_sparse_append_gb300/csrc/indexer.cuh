@@ -9,6 +9,13 @@ constexpr int kIdxDim = 128;      // indexer head dim ("DeepSeek-V4 KV Cache 深
 constexpr int kMaxHI = 64;        // indexer heads supported
 constexpr int kMaxChunk = 8192;   // entries scored per CTA
 constexpr int kMaxPool = 2048;    // largest pool / top-k kept by the merge
+// Key histograms: the top kBinBits bits of the order-preserving key (for
+// positive scores: the exponent and 4 mantissa bits, bins of 1/16 octave).
+constexpr int kBinBits = 13;
+constexpr int kBinShift = 32 - kBinBits;
+constexpr int kBins = 1 << kBinBits;
+constexpr int kMaxChunksPerSeq = 1024;
+constexpr int kSeqWords = 4;      // per sequence: ticket, top bin + 1, kBins - low bin, spare
 
 struct IndexArgs {
   const uint8_t* kdata;           // indexer-key plane data
@@ -22,12 +29,13 @@ struct IndexArgs {
   int HI;
   const int32_t* pool;            // Reindex: candidate entries, or null
   int pool_len;
-  int topk, pool_out, K_sel;
+  int topk, pool_out;
   int chunk, n_chunks;
-  uint32_t* cand_key;             // workspace [B][n_chunks][K_sel]
-  int32_t* cand_idx;
-  uint32_t* counters;             // workspace [B], zero between calls
-  uint32_t* ghist;                // workspace [B][4096] key histogram, zero between calls
+  uint32_t* cand_key;             // workspace [B][n_chunks][chunk] candidate keys
+  int32_t* cand_idx;              // workspace [B][n_chunks][chunk] their entries
+  uint32_t* ccount;               // workspace [B][n_chunks][2]: candidates, real keys
+  uint32_t* seq_state;            // workspace [B][4]: ticket, bin range; zero between calls
+  uint32_t* ghist;                // workspace [B][8192] key histogram, zero between calls
   int32_t* out_idx;
   int32_t* out_pool;
   float* dbg;

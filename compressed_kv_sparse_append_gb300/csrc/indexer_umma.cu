@@ -10,15 +10,18 @@
 //
 // Per CTA: one chunk of C keys of one sequence.
 //   warp 0   TMA producer: 128-key tiles of packed codes (SWIZZLE_64B) and
-//            their scale bytes into a kStages-deep shared-memory ring;
+//            their scale bytes into a kUStages-deep shared-memory ring,
+//            starting as soon as the previous kernel is done (the other
+//            warps quantise the query meanwhile);
 //   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, two
 //            buffers) = keys (A, M = 128) x query (B, N = 64), K = 128 in two
 //            block-scaled steps;
 //   warps 6-9 move each tile's key scales into TMEM (lane = key), running
 //            ahead of the MMA by up to the ring depth;
-//   warps 2-5 epilogue: read D back (one key per thread) and form
-//            s = sum_h w_h ReLU(d_h) in f32.
-// The scores stay in shared memory; the chunk's top-K and the cross-chunk
+//   warps 2-5 epilogue: read D back (one key per thread), form
+//            s = sum_h w_h ReLU(d_h) in f32, and count its key in the
+//            chunk's shared-memory histogram.
+// The scores stay in shared memory; the candidate bound and the cross-chunk
 // merge are those of topk_merge.cuh.
 
 #include <cuda.h>
@@ -31,8 +34,10 @@ namespace ckv {
 
 namespace {
 
-constexpr int kUThreads = 320;   // TMA, MMA, 4 epilogue warps, 4 scale-mover warps
-constexpr int kUStages = 6;
+// warp 0 TMA, warp 1 MMA, warps 2-5 and 10-13 epilogue (even / odd tiles),
+// warps 6-9 scale movers
+constexpr int kUThreads = 448;
+constexpr int kUStages = 14;
 constexpr int kUTile = 128;
 constexpr uint32_t kDataBytes = kUTile * 64;                 // 8 KB
 constexpr uint32_t kScaleBytes = kUTile * 8;                 // 1 KB
@@ -42,19 +47,22 @@ constexpr uint32_t kOffQ = kOffScale + kUStages * kScaleBytes;     // 64 rows x 
 constexpr uint32_t kOffQs = kOffQ + 64 * 64;                       // 64 x 8 scale bytes
 constexpr uint32_t kOffW = kOffQs + 64 * 8;                        // 64 f32
 constexpr uint32_t kOffKeys = kOffW + 64 * 4;                      // u32 [kMaxChunk]
-constexpr uint32_t kOffMerge = kOffKeys + kMaxChunk * 4;
+constexpr uint32_t kOffHist = kOffKeys + kMaxChunk * 4;            // u32 [kBins]
+constexpr uint32_t kOffMerge = kOffHist + kBins * 4;
 constexpr uint32_t kOffBar = (kOffMerge + sizeof(MergeSmem<kUThreads>) + 7) & ~7u;
 constexpr int kNumBarU = 3 * kUStages + 4;
 constexpr uint32_t kOffSlotU = kOffBar + kNumBarU * 8;
 constexpr uint32_t kSmemU = kOffSlotU + 16 + 1024;
 static_assert(kOffQ % 1024 == 0, "operand tiles 1024-aligned");
 static_assert(kSmemU <= 232448, "fits in shared memory");
+// The merge's shared-memory scratch: the pipeline ring (dead by then).
+constexpr int kMergeScratchWords = (int)(kOffQ / 4);
 
 constexpr uint32_t kTmemU = 256;
 constexpr uint32_t kColD = 0;          // two 64-column accumulators
 constexpr uint32_t kColSFA = 128;      // 8 columns per stage
-constexpr uint32_t kColSFB = 192;      // 8 columns
-static_assert(kColSFA + 8 * kUStages <= kColSFB, "scale columns of every stage below SFB");
+constexpr uint32_t kColSFB = kColSFA + 8 * kUStages;   // 8 columns
+static_assert(kColSFB + 8 <= kTmemU, "scale columns of every stage and the query's fit");
 constexpr uint32_t kIdescNvf4 = idesc_nvf4(128, 64);
 
 enum { BU_FULL = 0, BU_EMPTY = kUStages, BU_SFA = 2 * kUStages, BU_DFULL = 3 * kUStages,
@@ -90,6 +98,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(g + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(g + kOffSlotU);
   uint32_t* keys = reinterpret_cast<uint32_t*>(g + kOffKeys);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(g + kOffHist);
   float* wsm = reinterpret_cast<float*>(g + kOffW);
   MergeSmem<kUThreads>& msm = *reinterpret_cast<MergeSmem<kUThreads>*>(g + kOffMerge);
   __shared__ int abort_flag;
@@ -111,6 +120,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tslot, kTmemU);
+  merge_smem_init<kUThreads>(msm);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
   pdl_wait();
   const int b = blockIdx.y, chunk = blockIdx.x;
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
@@ -118,16 +132,53 @@ __global__ void __launch_bounds__(kUThreads, 1)
   const int n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)ncomp - c0));
   const int T = (n_elem + kUTile - 1) / kUTile;
   const int64_t row0 = (int64_t)b * a.cap + c0;
+  volatile int* abort_p = &abort_flag;
+  const bool tr = a.trace && b == 0 && chunk == 0;
+  const long long tr0 = clock64();
 
-  // ---- setup: FP4 query (B operand) + its scales, head weights, barriers
-  {
-    for (int j = tid; j < 64 * 8; j += kUThreads) {
-      const int h = j >> 3, blk = j & 7;
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA ----
+    // The key stream does not depend on the query: it starts at once, while
+    // the other warps prepare the query.
+    if (lane == 0) {
+      for (int t = 0; t < T; ++t) {
+        const int s = t % kUStages;
+        if (t >= kUStages &&
+            !mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11))
+          break;
+        mbar_expect_tx(&bars[BU_FULL + s], kDataBytes + kScaleBytes);
+        const int64_t row = row0 + (int64_t)t * kUTile;
+        tma_load_2d(base + kOffData + s * kDataBytes, &map_data, 0, (int)row, &bars[BU_FULL + s]);
+        tma_load_2d(base + kOffScale + s * kScaleBytes, &map_scale, 0, (int)(row >> 1),
+                    &bars[BU_FULL + s]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- warps 1-9: FP4 query (B operand) + its scales, head weights, an
+    // empty histogram
+    const int t9 = tid - 32;
+    constexpr int kQItems = (64 * 8 + kUThreads - 33) / (kUThreads - 32);   // 16-channel blocks per thread
+    uint4 qraw[kQItems][2];
+#pragma unroll
+    for (int k = 0; k < kQItems; ++k) {
+      const int j = t9 + k * (kUThreads - 32), h = j >> 3, blk = j & 7;
+      qraw[k][0] = qraw[k][1] = make_uint4(0u, 0u, 0u, 0u);
+      if (j < 64 * 8 && h < a.HI) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16);
+        qraw[k][0] = s4[0];
+        qraw[k][1] = s4[1];
+      }
+    }
+    const float wv = (t9 < 64 && t9 < a.HI) ? a.w[(int64_t)b * a.HI + t9] : 0.f;
+#pragma unroll
+    for (int k = 0; k < kQItems; ++k) {
+      const int j = t9 + k * (kUThreads - 32), h = j >> 3, blk = j & 7;
+      if (j >= 64 * 8) break;
       uint32_t lo = 0, hi = 0;
       uint8_t sc = 0;
       if (h < a.HI) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16);
-        const uint4 x0 = s4[0], x1 = s4[1];
+        const uint4 x0 = qraw[k][0], x1 = qraw[k][1];
         const uint32_t wd[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         float v[16];
         float amax = 0.f;
@@ -153,120 +204,123 @@ __global__ void __launch_bounds__(kUThreads, 1)
       *reinterpret_cast<uint2*>(g + kOffQ + sw64(h, blk >> 1) + (blk & 1) * 8) = make_uint2(lo, hi);
       g[kOffQs + h * 8 + blk] = sc;
     }
-  }
-  if (tid < 64) wsm[tid] = tid < a.HI ? a.w[(int64_t)b * a.HI + tid] : 0.f;
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  volatile int* abort_p = &abort_flag;
-  const bool tr = a.trace && b == 0 && chunk == 0;
-  const long long tr0 = clock64();
-
-  if (warp >= 2 && warp < 6) {
-    // query scales -> TMEM (B operand scales): lane 32q + r, column j holds
-    // the four block scales (one 32-bit word per K step) of query row 32j + r.
-    const int qd = warp & 3;
-    const int m = qd * 32 + lane;
-    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+    if (t9 < 64) wsm[t9] = wv;
+    for (int i = t9; i < kBins / 4; i += kUThreads - 32)
+      reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 1, %0;" ::"r"(kUThreads - 32) : "memory");
+    if (warp >= 2 && warp < 6) {
+      // query scales -> TMEM (B operand scales): lane 32q + r, column j holds
+      // the four block scales (one 32-bit word per K step) of query row 32j + r.
+      const int qd = warp & 3;
+      const int m = qd * 32 + lane;
+      const uint32_t lb = (uint32_t)(qd * 32) << 16;
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint32_t v[4];
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = 32 * j + (m & 31);
-        v[j] = row < 64 ? *reinterpret_cast<const uint32_t*>(g + kOffQs + row * 8 + ks * 4) : 0u;
+        for (int j = 0; j < 4; ++j) {
+          const int row = 32 * j + (m & 31);
+          v[j] = row < 64 ? *reinterpret_cast<const uint32_t*>(g + kOffQs + row * 8 + ks * 4) : 0u;
+        }
+        tmem_st4(tmem + lb + kColSFB + 4 * ks, v[0], v[1], v[2], v[3]);
       }
-      tmem_st4(tmem + lb + kColSFB + 4 * ks, v[0], v[1], v[2], v[3]);
+      tmem_wait_st();
     }
-    tmem_wait_st();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) trace_at(a.st, tr, 0, tr0);
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"r"(kUThreads - 32) : "memory");
+    tc_fence_after();
+    if (tid == 32) trace_at(a.st, tr, 0, tr0);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA ----
-    if (lane == 0) {
+    if (warp == 1) {
+      // ------------------------------------------------------------ MMA ----
+      if (lane == 0) {
+        for (int t = 0; t < T; ++t) {
+          const int s = t % kUStages, d = t & 1;
+          if (!mbar_wait(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
+          if (t >= 2 && !mbar_wait(&bars[BU_DEMPTY + d], ((t >> 1) + 1) & 1, a.st, abort_p, 13)) break;
+          tc_fence_after();
+          if (t < 8) trace_at(a.st, tr, 32 + t, tr0);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
+            const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
+            umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
+                      tmem + kColSFB + 4 * ks, ks > 0);
+          }
+          umma_commit(&bars[BU_DFULL + d]);
+          umma_commit(&bars[BU_EMPTY + s]);
+          if (t < 4) trace_at(a.st, tr, 13 + t, tr0);
+        }
+      }
+      __syncwarp();
+    } else if (warp >= 6 && warp < 10) {
+      // --------------------------------------------------- scale movers ----
+      const int qd = warp & 3;
+      const int m = qd * 32 + lane;
+      const uint32_t lb = (uint32_t)(qd * 32) << 16;
       for (int t = 0; t < T; ++t) {
         const int s = t % kUStages;
-        if (t >= kUStages &&
-            !mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11))
-          break;
-        mbar_expect_tx(&bars[BU_FULL + s], kDataBytes + kScaleBytes);
-        const int64_t row = row0 + (int64_t)t * kUTile;
-        tma_load_2d(base + kOffData + s * kDataBytes, &map_data, 0, (int)row, &bars[BU_FULL + s]);
-        tma_load_2d(base + kOffScale + s * kScaleBytes, &map_scale, 0, (int)(row >> 1),
-                    &bars[BU_FULL + s]);
+        if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) break;
+        const uint2 sc = *reinterpret_cast<const uint2*>(g + kOffScale + s * kScaleBytes + m * 8);
+        tmem_st4(tmem + lb + kColSFA + 8 * s, sc.x, sc.x, sc.x, sc.x);
+        tmem_st4(tmem + lb + kColSFA + 8 * s + 4, sc.y, sc.y, sc.y, sc.y);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[BU_SFA + s]);
+        if (m == 0 && t < 8) trace_at(a.st, tr, 40 + t, tr0);
       }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA ----
-    if (lane == 0) {
-      for (int t = 0; t < T; ++t) {
-        const int s = t % kUStages, d = t & 1;
-        if (!mbar_wait(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
-        if (t >= 2 && !mbar_wait(&bars[BU_DEMPTY + d], ((t >> 1) + 1) & 1, a.st, abort_p, 13)) break;
+    } else {
+      // ------------------------------------------------------- epilogue ----
+      // group 0 (warps 2-5) takes the even tiles (accumulator 0), group 1
+      // (warps 10-13) the odd ones (accumulator 1): two warps per SM
+      // sub-partition, so one's TMEM loads and FMAs overlap the other's
+      const int qd = warp & 3;
+      const int grp = warp >= 10 ? 1 : 0;
+      const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
+      const uint32_t lb = (uint32_t)(qd * 32) << 16;
+      uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+      for (int t = grp; t < T; t += 2) {
+        const int d = t & 1;
+        if (!mbar_wait(&bars[BU_DFULL + d], (t >> 1) & 1, a.st, abort_p, 15)) break;
         tc_fence_after();
+        if (m == 0 && t < 8) trace_at(a.st, tr, 48 + t, tr0);
+        uint32_t r[64];
+        tmem_ld32(tmem + lb + kColD + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tmem + lb + kColD + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars[BU_DEMPTY + d]);
+        // eight independent partial sums (one f32 FMA chain of 64 would
+        // leave the single epilogue warp of each SM sub-partition waiting
+        // on FMA latency), added in a fixed order
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
-          const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
-          umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
-                    tmem + kColSFB + 4 * ks, ks > 0);
+        for (int h4 = 0; h4 < 16; ++h4) {
+          const float4 wv = reinterpret_cast<const float4*>(wsm)[h4];
+          const int j = (h4 & 1) * 4;
+          acc[j] = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), acc[j]);
+          acc[j + 1] = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), acc[j + 1]);
+          acc[j + 2] = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), acc[j + 2]);
+          acc[j + 3] = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), acc[j + 3]);
         }
-        umma_commit(&bars[BU_DFULL + d]);
-        umma_commit(&bars[BU_EMPTY + s]);
+        const float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        if (m == 0 && t < 8) trace_at(a.st, tr, 1 + t, tr0);
+        const int i = t * kUTile + m;
+        if (i < n_elem) {
+          const uint32_t key = score_key(sc);
+          keys[i] = key;
+          atomicAdd(&hist[key_bin(key)], 1u);
+          kmin = min(kmin, key);
+          kmax = max(kmax, key);
+          if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = sc;
+        }
       }
-    }
-    __syncwarp();
-  } else if (warp >= 6) {
-    // --------------------------------------------------- scale movers ----
-    const int qd = warp & 3;
-    const int m = qd * 32 + lane;
-    const uint32_t lb = (uint32_t)(qd * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % kUStages;
-      if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) break;
-      const uint2 sc = *reinterpret_cast<const uint2*>(g + kOffScale + s * kScaleBytes + m * 8);
-      tmem_st4(tmem + lb + kColSFA + 8 * s, sc.x, sc.x, sc.x, sc.x);
-      tmem_st4(tmem + lb + kColSFA + 8 * s + 4, sc.y, sc.y, sc.y, sc.y);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars[BU_SFA + s]);
-    }
-  } else {
-    // ------------------------------------------------------- epilogue ----
-    const int qd = warp & 3;
-    const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
-    const uint32_t lb = (uint32_t)(qd * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      const int d = t & 1;
-      if (!mbar_wait(&bars[BU_DFULL + d], (t >> 1) & 1, a.st, abort_p, 15)) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(tmem + lb + kColD + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-      tmem_ld32(tmem + lb + kColD + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars[BU_DEMPTY + d]);
-      float sc = 0.f;
-#pragma unroll
-      for (int h4 = 0; h4 < 16; ++h4) {
-        const float4 wv = reinterpret_cast<const float4*>(wsm)[h4];
-        sc = fmaf(wv.x, fmaxf(__uint_as_float(r[4 * h4]), 0.f), sc);
-        sc = fmaf(wv.y, fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f), sc);
-        sc = fmaf(wv.z, fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f), sc);
-        sc = fmaf(wv.w, fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f), sc);
-      }
-      if (m == 0 && t < 8) trace_at(a.st, tr, 1 + t, tr0);
-      const int i = t * kUTile + m;
-      if (i < n_elem) {
-        keys[i] = score_key(sc);
-        if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = sc;
+      kmin = __reduce_min_sync(0xffffffffu, kmin);
+      kmax = __reduce_max_sync(0xffffffffu, kmax);
+      if (lane == 0) {
+        atomicMin(&msm.kmin, kmin);
+        atomicMax(&msm.kmax, kmax);
       }
     }
   }
@@ -280,10 +334,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (tid == 0) trace_at(a.st, tr, 9, tr0);
   if (tr && tid == 0) a.st->pad[24] = T;
   __syncthreads();
-  // The merge's survivors may use everything below the merge state: the
-  // pipeline ring, the query tiles and the chunk's scores are all dead here.
-  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, reinterpret_cast<uint32_t*>(g),
-                                    (int)(kOffMerge / 8), msm);
+  // The merge's survivors use the pipeline ring, dead by then.
+  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, hist, reinterpret_cast<uint32_t*>(g),
+                                    kMergeScratchWords, msm);
 }
 
 bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {

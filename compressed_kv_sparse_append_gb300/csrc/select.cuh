@@ -1,13 +1,18 @@
 // Block-wide exact top-K selection on order-preserving u32 keys.
 //
 // The top-K (largest keys; among equal keys the earliest elements) of n
-// elements is found with an 8-bit radix select of the K-th largest key T
-// (over the bits the keys do not all share), then an order-preserving
-// compaction that keeps every key > T and the
-// first `need` keys == T.  Elements are visited in array order, so when the
-// array is in ascending entry order the output is the ascending index set and
-// a tie at T goes to the lower entry index ("DeepSeek-V4 KV Cache 深度分析",
-// §四: the indexer keeps the top-k blocks; equal scores resolved by index).
+// elements is found with a radix select of the K-th largest key T (8 bits per
+// pass over the bits the candidate keys do not all share), then an
+// order-preserving compaction that keeps every key > T and the first `need`
+// keys == T.  Elements are visited in array order, so when the array is in
+// ascending entry order the output is the ascending index set and a tie at T
+// goes to the lower entry index ("DeepSeek-V4 KV Cache 深度分析", §四: the
+// indexer keeps the top-k blocks; equal scores resolved by index).
+//
+// This code runs once per CTA (the chunk's candidates) or once per sequence
+// (the merge), so it executes with a cold instruction cache: it takes its keys
+// from a run-time source, its loops are not unrolled, and each kernel calls it
+// from one place, so that little code has to be fetched.
 #pragma once
 
 #include "common.cuh"
@@ -68,19 +73,59 @@ __device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ea
   __syncthreads();
 }
 
+// Where the elements of a selection come from: element i's key and entry.
+//   key != null: key[i] (shared memory); entry ent[i], or, with ent == null,
+//                pool[i] (pool != null) or first + i.
+//   key == null: the merge's candidate lists in global memory, element i
+//                being slot i of their concatenation in chunk order (chunk c
+//                holds slots cprefix[c] .. cprefix[c + 1] - 1, stored from
+//                c * stride on).
+struct SelSrc {
+  const uint32_t* key;
+  const int32_t* ent;
+  const int32_t* pool;
+  int64_t first;
+  const uint32_t* gk;
+  const int32_t* gi;
+  const uint32_t* cprefix;
+  int n_chunks;
+  int64_t stride;
+
+  __device__ int64_t slot(int v) const {
+    int lo = 0, hi = n_chunks;   // last c with cprefix[c] <= v
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((int)cprefix[mid] <= v) lo = mid;
+      else hi = mid;
+    }
+    return (int64_t)lo * stride + (v - (int)cprefix[lo]);
+  }
+  __device__ uint32_t k(int i) const { return key ? key[i] : __ldcg(gk + slot(i)); }
+  __device__ int32_t e(int i) const {
+    if (key) return ent ? ent[i] : pool ? pool[i] : (int32_t)(first + i);
+    return __ldcg(gi + slot(i));
+  }
+};
+
 // Finds T (the K-th largest key among n, K <= n) and need = how many
-// elements equal to T belong to the top-K.  get(i) returns element i's key.
-// The bits every key shares (the common prefix of the smallest and largest
-// key) are settled first; the rest is resolved 8 bits per pass, so scores of
-// similar magnitude (which share their exponent bits) spread over the bins
-// instead of piling onto one.
-template <int NT, class Get>
-__device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm, uint32_t& T,
-                                      uint32_t& need) {
+// elements equal to T belong to the top-K.  The bits every key shares (the
+// common prefix of the smallest and largest key) are settled first; the rest
+// is resolved 8 bits per pass.
+//
+// Hint: when the caller already knows that the K-th largest key has its top
+// (32 - top0) bits equal to those of prefix0, and that `above` keys are
+// larger than every key with that prefix, it passes top0 < 32, prefix0 and
+// K - above as K: only the keys with that prefix take part.
+template <int NT>
+__device__ __forceinline__ void block_radix_threshold(const SelSrc src, int n, int K, SelectSmem<NT>& sm, uint32_t& T,
+                                      uint32_t& need, uint32_t prefix0, int top0) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t mask0 = top0 >= 32 ? 0u : (0xFFFFFFFFu << top0);
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll 1
   for (int i = threadIdx.x; i < n; i += NT) {
-    const uint32_t u = get(i);
+    const uint32_t u = src.k(i);
+    if (((u ^ prefix0) & mask0) != 0u) continue;
     lo = min(lo, u);
     hi = max(hi, u);
   }
@@ -123,9 +168,18 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
     const int width = top < 8 ? top : 8, shift = top - width;
     const uint32_t mask = top == 32 ? 0u : (0xFFFFFFFFu << top);   // settled bits
     const uint32_t dmask = (1u << width) - 1u;
-    for (int i = threadIdx.x; i < n; i += NT) {
-      const uint32_t u = get(i);
-      if (((u ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u >> shift) & dmask], 1u);
+    // one shared atomic per distinct digit per warp: keys that tie exactly
+    // (or share the digit) would otherwise serialise on one counter
+#pragma unroll 1
+    for (int base = warp * 32; base < n; base += NT) {
+      const int i = base + lane;
+      uint32_t d = 0xFFFFFFFFu;
+      if (i < n) {
+        const uint32_t u = src.k(i);
+        if (((u ^ prefix) & mask) == 0) d = (u >> shift) & dmask;
+      }
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[d], (uint32_t)__popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
@@ -147,6 +201,7 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
       const bool here = before < remaining && incl >= remaining;
       if (here) {
         uint32_t cum = before;
+#pragma unroll 1
         for (int j = 0; j < 8; ++j) {
           if (cum + c[j] >= remaining) {
             sm.bcast[0] = (uint32_t)(255 - 8 * lane - j);
@@ -168,22 +223,26 @@ __device__ void block_radix_threshold(int n, int K, Get get, SelectSmem<NT>& sm,
   need = remaining;
 }
 
-// Writes the top-K of n elements (or all n if n <= K) in array order via
-// emit(out_pos, i).  Returns the number emitted.
-template <int NT, class Get, class Emit>
-__device__ int block_select_ordered(int n, int K, Get get, Emit emit, SelectSmem<NT>& sm,
-                                    long long* marks = nullptr) {
+// Writes the top-K of the n elements of `src` (or all n if n <= K) in array
+// order: output position p receives the element's entry in out_ent[p] and,
+// when out_key is not null, its key in out_key[p].  Hint (prefix0, top0,
+// above) as for block_radix_threshold (top0 = 32: none).  Returns the number
+// written.  Block-wide.
+template <int NT>
+__device__ __forceinline__ int select_ordered(const SelSrc src, int n, int K, uint32_t prefix0, int top0,
+                                           int above, int32_t* out_ent, uint32_t* out_key,
+                                           SelectSmem<NT>& sm) {
   if (n <= 0 || K <= 0) return 0;
   const bool all = n <= K;
   uint32_t T = 0, need = 0;
-  if (!all) block_radix_threshold<NT>(n, K, get, sm, T, need);
-  if (marks && threadIdx.x == 0) marks[0] = clock64();
+  if (!all) block_radix_threshold<NT>(src, n, K - above, sm, T, need, prefix0, top0);
   const int per = (n + NT - 1) / NT;
   const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
   uint32_t gt = 0, eq = 0;
   if (!all) {
+#pragma unroll 1
     for (int i = i0; i < i1; ++i) {
-      const uint32_t u = get(i);
+      const uint32_t u = src.k(i);
       gt += u > T;
       eq += u == T;
     }
@@ -192,20 +251,25 @@ __device__ int block_select_ordered(int n, int K, Get get, Emit emit, SelectSmem
   }
   uint32_t gt_before, eq_before, gt_tot, eq_tot;
   block_scan2<NT>(gt, eq, gt_before, eq_before, gt_tot, eq_tot, sm);
-  if (marks && threadIdx.x == 0) marks[1] = clock64();
   uint32_t pos = gt_before + min(eq_before, need);
   uint32_t eq_rank = eq_before;
+#pragma unroll 1
   for (int i = i0; i < i1; ++i) {
     bool take = all;
+    uint32_t u = 0;
+    if (!all || out_key) u = src.k(i);
     if (!all) {
-      const uint32_t u = get(i);
       if (u > T) take = true;
       else if (u == T && eq_rank < need) {
         take = true;
         ++eq_rank;
       }
     }
-    if (take) emit((int)pos++, i);
+    if (take) {
+      out_ent[pos] = src.e(i);
+      if (out_key) out_key[pos] = u;
+      ++pos;
+    }
   }
   __syncthreads();
   return all ? n : K;

@@ -1,20 +1,25 @@
-// Candidate stage of csa_index_topk shared by the scorers.
+// Candidate stage and cross-chunk merge of csa_index_topk, shared by the
+// scorers ("DeepSeek-V4 KV Cache 深度分析", §四: the indexer keeps the top-k
+// compressed blocks of the whole context).
 //
-// Each CTA keeps its chunk's top-K candidates (K = max(topk, pool_out)) in
-// ascending entry order in the workspace and adds them to a per-sequence
-// histogram of the top 12 key bits (global atomics).  The last CTA of the
-// sequence (atomic ticket, no spinning) then
-//   (a) finds the histogram bin holding the K-th largest key (and, when the
-//       candidates in or above it would not fit in shared memory, the bin of
-//       the next 12 key bits within it, from a second histogram over that
-//       bin's candidates),
-//   (b) compacts, in order, the candidates at or above that threshold into
-//       shared memory (one pass over the candidate lists),
-//   (c) runs the exact radix select on those survivors,
-// and writes the ascending top-k (and the CSA2 Full layer's pool).  Ties at
-// the threshold go to the earliest, i.e. lowest, entries ("DeepSeek-V4 KV
-// Cache 深度分析", §四: the indexer keeps the top-k blocks).  If even that is
-// too crowded for shared memory the select runs on the full lists.
+// Every CTA scores one chunk of a sequence and builds, in shared memory, a
+// histogram of its keys' top kBinBits bits while it scores.  Then:
+//   1. it adds that histogram to the sequence's histogram in the workspace;
+//   2. it reads the sequence histogram back.  Whatever other chunks have
+//      added by then, if at least K keys lie in bins >= v, the sequence's
+//      K-th largest key lies in a bin >= v: the highest such v is a lower
+//      bound on the threshold bin.  (Counts read while others still add are
+//      each at most the final count, so the bound holds for any snapshot.)
+//   3. it writes its keys in bins >= that bound, in entry order, as its
+//      candidates, with their count;
+//   4. it takes a ticket; the last CTA of the sequence merges: the complete
+//      histogram gives the threshold bin T and the count above it; the
+//      candidates in bins >= T are exactly the sequence's keys there (every
+//      chunk's bound is <= T); they are compacted in entry order, and an
+//      exact radix select restricted to bin T picks the top K.
+// Equal keys go to the earliest, i.e. lowest, entries.  When more survivors
+// reach the merge than its shared memory holds (a huge exact tie at the
+// boundary), the select runs on the candidate lists in global memory.
 #pragma once
 
 #include "select.cuh"
@@ -22,286 +27,538 @@
 
 namespace ckv {
 
-constexpr int kHistShift = 20;                 // 12-bit histogram of the key
-constexpr int kHistBins = 1 << (32 - kHistShift);
+__device__ __forceinline__ uint32_t key_bin(uint32_t key) { return key >> kBinShift; }
 
 template <int NT>
 struct MergeSmem {
-  uint32_t pool_key[kMaxPool];
-  int32_t pool_ent[kMaxPool];
   SelectSmem<NT> sel;
+  uint32_t cprefix[kMaxChunksPerSeq + 1];   // merge: candidate offsets of the chunks
+  uint32_t sprefix[kMaxChunksPerSeq + 1];   // merge: survivor offsets of the chunks
+  uint32_t wcnt[NT / 32];                   // per-warp counts of an ordered compaction
+  uint32_t sub[256];                        // merge: next 8 key bits within the threshold bin
   int ticket;
-  uint32_t n_real;
-  uint32_t bcast[2];
+  uint32_t n_real;                          // real keys of this chunk
+  uint32_t kmin, kmax;                      // smallest / largest real key of this chunk
+  uint32_t bcast[4];
 };
 
-// Final outputs from an ordered candidate source of n elements.
-template <int NT, class GK, class GE>
-__device__ void emit_outputs(const IndexArgs& a, int b, int n, int n_real, GK gk, GE ge,
-                             MergeSmem<NT>& sm) {
-  int32_t* oi = a.out_idx + (int64_t)b * a.topk;
-  if (a.pool_out > 0) {
-    const int kp = min(a.pool_out, n_real);
-    block_select_ordered<NT>(
-        n, kp, gk,
-        [&](int pos, int i) {
-          sm.pool_key[pos] = gk(i);
-          sm.pool_ent[pos] = ge(i);
-        },
-        sm.sel);
-    int32_t* op = a.out_pool + (int64_t)b * a.pool_out;
-    for (int i = threadIdx.x; i < a.pool_out; i += NT) op[i] = i < kp ? sm.pool_ent[i] : -1;
-    const int kk = min(a.topk, kp);
-    block_select_ordered<NT>(
-        kp, kk, [&](int i) { return sm.pool_key[i]; },
-        [&](int pos, int i) { oi[pos] = sm.pool_ent[i]; }, sm.sel);
-    for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
-  } else {
-    const int kk = min(a.topk, n_real);
-    block_select_ordered<NT>(n, kk, gk, [&](int pos, int i) { oi[pos] = ge(i); }, sm.sel);
-    for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
+// Sets n_real / kmin / kmax before the scorer's keys are written.
+template <int NT>
+__device__ __forceinline__ void merge_smem_init(MergeSmem<NT>& sm) {
+  if (threadIdx.x == 0) {
+    sm.n_real = 0u;
+    sm.kmin = 0xFFFFFFFFu;
+    sm.kmax = 0u;
   }
 }
 
-// Of the kHistBins counts in hs (the last bin is the highest), finds the
-// bin holding the min(K, total)-th largest element.  Returns the bin; sets
-// total (all counts), keff = min(K, total) and above (the count in higher
-// bins).  Block-wide; hs is only read.
+// Descending scan of the histogram `gh` (global, read through L2) from bin
+// top - 1 down: returns the highest bin v with (count of bins >= v) >= K, or
+// 0 if the whole histogram holds fewer.  `above` = count in bins > v.
+// Block-wide; NT bins per round, one load each.
 template <int NT>
-__device__ uint32_t find_bin_desc(const uint32_t* hs, uint32_t K, MergeSmem<NT>& sm, uint32_t& total,
-                                  uint32_t& keff, uint32_t& above) {
-  constexpr int per = (kHistBins + NT - 1) / NT;   // descending bins, contiguous per thread
-  const int p0 = min(kHistBins, (int)threadIdx.x * per), p1 = min(kHistBins, p0 + per);
-  uint32_t cnt = 0;
-  for (int p = p0; p < p1; ++p) cnt += hs[kHistBins - 1 - p];
-  uint32_t before, d0, d1;
-  block_scan2<NT>(cnt, 0u, before, d0, total, d1, sm.sel);
-  keff = min(K, total);
+__device__ uint32_t hist_bin_from_top(const uint32_t* gh, int top, uint32_t K, MergeSmem<NT>& sm,
+                                      uint32_t& above) {
+  uint32_t carry = 0;
+  for (int hi = top; hi > 0; hi -= NT) {
+    const int bin = hi - 1 - (int)threadIdx.x;
+    const uint32_t v = bin >= 0 ? __ldcg(gh + bin) : 0u;
+    uint32_t before, tot, d0, d1;
+    block_scan2<NT>(v, 0u, before, d0, tot, d1, sm.sel);
+    if (threadIdx.x == 0) sm.bcast[0] = 0xFFFFFFFFu;
+    __syncthreads();
+    if (v > 0 && carry + before < K && carry + before + v >= K) {
+      sm.bcast[0] = (uint32_t)bin;
+      sm.bcast[1] = carry + before;
+    }
+    __syncthreads();
+    const uint32_t found = sm.bcast[0];
+    if (found != 0xFFFFFFFFu) {
+      above = sm.bcast[1];
+      __syncthreads();
+      return found;
+    }
+    carry += tot;
+  }
+  above = carry;
+  return 0u;
+}
+
+// The chunk's lower bound on its sequence's threshold bin: one descending
+// scan from bin top - 1 over two histograms at once -- the sequence's (global,
+// a snapshot while other chunks still add to it; this chunk's own additions
+// may or may not be visible yet) and this chunk's own (shared memory).  The
+// highest bin at which either reaches K keys from the top is a valid bound
+// (each count is at most the sequence's true count).  0 if neither does.
+template <int NT>
+__device__ uint32_t chunk_bound(const uint32_t* gh, const uint32_t* lh, int top, uint32_t K,
+                                MergeSmem<NT>& sm) {
+  uint32_t cg = 0, cl = 0;
+  uint32_t found_g = 0xFFFFFFFFu, found_l = 0xFFFFFFFFu;
+  for (int hi = top; hi > 0; hi -= NT) {
+    const int bin = hi - 1 - (int)threadIdx.x;
+    const uint32_t vg = bin >= 0 ? __ldcg(gh + bin) : 0u;
+    const uint32_t vl = bin >= 0 ? lh[bin] : 0u;
+    uint32_t bg, bl, tg, tl;
+    block_scan2<NT>(vg, vl, bg, bl, tg, tl, sm.sel);
+    if (threadIdx.x == 0) {
+      sm.bcast[0] = 0xFFFFFFFFu;
+      sm.bcast[1] = 0xFFFFFFFFu;
+    }
+    __syncthreads();
+    if (found_g == 0xFFFFFFFFu && vg > 0 && cg + bg < K && cg + bg + vg >= K) sm.bcast[0] = (uint32_t)bin;
+    if (found_l == 0xFFFFFFFFu && vl > 0 && cl + bl < K && cl + bl + vl >= K) sm.bcast[1] = (uint32_t)bin;
+    __syncthreads();
+    if (sm.bcast[0] != 0xFFFFFFFFu) found_g = sm.bcast[0];
+    if (sm.bcast[1] != 0xFFFFFFFFu) found_l = sm.bcast[1];
+    cg += tg;
+    cl += tl;
+    __syncthreads();
+    // the local bound is never above the global one once both are found;
+    // either alone already bounds, and the scan stops at the first found
+    if (found_g != 0xFFFFFFFFu || found_l != 0xFFFFFFFFu) break;
+  }
+  const uint32_t g = found_g == 0xFFFFFFFFu ? 0u : found_g;
+  const uint32_t l = found_l == 0xFFFFFFFFu ? 0u : found_l;
+  return g > l ? g : l;
+}
+
+// Final outputs from an ordered source of n elements (n_real real keys in
+// the sequence).  Hint (prefix0, top0, above): the K-th largest key has
+// prefix0's top (32 - top0) bits and `above` keys lie above all such keys
+// (top0 = 32: none).  A CSA2 Full layer keeps its pool (key and entry in
+// shared memory) and then takes its top-k from the pool: two selections run
+// through one call site.
+template <int NT>
+__device__ void emit_outputs(const IndexArgs& a, int b, SelSrc src, int n, int n_real,
+                             uint32_t* pool_key, int32_t* pool_ent, MergeSmem<NT>& sm,
+                             uint32_t prefix0, int top0, int above) {
+  int32_t* oi = a.out_idx + (int64_t)b * a.topk;
+  const bool pooled = a.pool_out > 0;
+  int kk = min(a.topk, n_real);
+  int K = pooled ? min(a.pool_out, n_real) : kk;
+#pragma unroll 1
+  for (int job = 0; job < (pooled ? 2 : 1); ++job) {
+    const bool to_pool = pooled && job == 0;
+    select_ordered<NT>(src, n, K, prefix0, top0, above, to_pool ? pool_ent : oi,
+                       to_pool ? pool_key : nullptr, sm.sel);
+    if (to_pool) {
+      int32_t* op = a.out_pool + (int64_t)b * a.pool_out;
+#pragma unroll 1
+      for (int i = threadIdx.x; i < a.pool_out; i += NT) op[i] = i < K ? pool_ent[i] : -1;
+      // second job: the top-k of the pool, no hint
+      src = SelSrc{};
+      src.key = pool_key;
+      src.ent = pool_ent;
+      n = K;
+      kk = min(a.topk, K);
+      K = kk;
+      prefix0 = 0u;
+      top0 = 32;
+      above = 0;
+    }
+  }
+#pragma unroll 1
+  for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
+}
+
+// Merge of the sequence's candidates, run by its last CTA.  `scratch`
+// (scratch_words 32-bit words of shared memory, dead otherwise) holds the
+// survivors and, for a CSA2 Full layer, the pool.
+template <int NT>
+__device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* scratch,
+                               int scratch_words, uint32_t own_bound) {
+  const bool tr = a.trace && b == 0 && threadIdx.x == 0;
+  const long long t0 = clock64();
+  const int K = a.pool_out > 0 ? a.pool_out : a.topk;
+  const int nch = a.n_chunks;
+  uint32_t* seq = a.seq_state + (int64_t)b * kSeqWords;
+  uint32_t* gh = a.ghist + (int64_t)b * kBins;
+  const uint2* cc = reinterpret_cast<const uint2*>(a.ccount) + (int64_t)b * nch;
+
+  // One round trip for: the chunks' counts, the top bin in use, and the
+  // histogram window [own_bound, own_bound + NT) (this CTA's bound is a
+  // lower bound on the threshold bin, so when no key lies above the window
+  // the window alone gives the threshold bin).
+  const int wbin = (int)own_bound + (int)threadIdx.x;
+  const uint32_t wv = (own_bound > 0 && wbin < kBins) ? __ldcg(gh + wbin) : 0u;
+  const int top = (int)__ldcg(seq + 1);
+  // chunk candidate counts -> offsets; real keys in total
+  uint32_t n_total = 0;
+  {
+    constexpr int kPer = (kMaxChunksPerSeq + NT - 1) / NT;
+    const int c0 = min(nch, (int)threadIdx.x * kPer), c1 = min(nch, c0 + kPer);
+    uint32_t cnt[kPer], real = 0, mine = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      cnt[k] = 0u;
+      if (c0 + k < c1) {
+        const uint2 v = __ldcg(cc + c0 + k);
+        cnt[k] = v.x;
+        real += v.y;
+        mine += v.x;
+      }
+    }
+    uint32_t before, rb, tot, rt;
+    block_scan2<NT>(mine, real, before, rb, tot, rt, sm.sel);
+    n_total = rt;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (c0 + k < c1) {
+        sm.cprefix[c0 + k] = before;
+        before += cnt[k];
+      }
+    if (threadIdx.x == 0) sm.cprefix[nch] = tot;
+    __syncthreads();
+  }
+  const int n_cand = (int)sm.cprefix[nch];
+  const int keff = min(K, (int)n_total);
+  // threshold bin and the count above it (every key is a survivor when the
+  // sequence has at most K)
+  uint32_t tb = 0, above = 0;
+  if (keff > 0 && (int)n_total > K) {
+    bool done = false;
+    if (own_bound > 0 && top <= (int)own_bound + NT) {
+      uint32_t before, d0, tot, d1;
+      block_scan2<NT>(wv, 0u, before, d0, tot, d1, sm.sel);
+      if (threadIdx.x == 0) sm.bcast[0] = 0xFFFFFFFFu;
+      __syncthreads();
+      const uint32_t hi_cnt = tot - before - wv;   // keys in window bins above this one
+      if (wv > 0 && hi_cnt < (uint32_t)keff && hi_cnt + wv >= (uint32_t)keff) {
+        sm.bcast[0] = (uint32_t)wbin;
+        sm.bcast[1] = hi_cnt;
+      }
+      __syncthreads();
+      if (sm.bcast[0] != 0xFFFFFFFFu) {
+        tb = sm.bcast[0];
+        above = sm.bcast[1];
+        done = true;
+      }
+      __syncthreads();
+    }
+    if (!done) tb = hist_bin_from_top<NT>(gh, top, (uint32_t)keff, sm, above);
+  }
+  const uint32_t lo_key = tb << kBinShift;
+  trace_at(a.st, tr, 20, t0);
+
+  // survivors (real keys >= lo_key) in entry order.  Rounds of kU virtual
+  // slots per lane: warp w reads 32 * kU consecutive slots of the chunks'
+  // concatenated lists (coalesced, every load of a round in flight at once),
+  // counts them per warp, meets the other warps once, writes in order.  The
+  // keys of the threshold bin are also counted by their next 8 bits.
+  const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
+  const int surv_cap = (scratch_words - pool_words) / 2;
+  uint32_t* surv_key = scratch;
+  int32_t* surv_ent = reinterpret_cast<int32_t*>(scratch + surv_cap);
+  uint32_t* pool_key = scratch + 2 * surv_cap;
+  int32_t* pool_ent = reinterpret_cast<int32_t*>(pool_key + kMaxPool);
+  SelSrc cl{};   // the candidate lists in global memory
+  cl.gk = a.cand_key + (int64_t)b * nch * a.chunk;
+  cl.gi = a.cand_idx + (int64_t)b * nch * a.chunk;
+  cl.cprefix = sm.cprefix;
+  cl.n_chunks = nch;
+  cl.stride = a.chunk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = NT / 32;
+  constexpr int kU = 8;
+  const bool hint = (int)n_total > K && keff > 0;
+  for (int i = threadIdx.x; i < 256; i += NT) sm.sub[i] = 0u;
   if (threadIdx.x == 0) {
-    sm.bcast[0] = 0u;
+    sm.bcast[0] = 0u;   // sub-bin search defaults
     sm.bcast[1] = 0u;
   }
   __syncthreads();
-  if (keff > 0 && before < keff && before + cnt >= keff) {
-    uint32_t cum = before;
-    for (int p = p0; p < p1; ++p) {
-      const uint32_t c = hs[kHistBins - 1 - p];
-      if (cum + c >= keff) {
-        sm.bcast[0] = (uint32_t)(kHistBins - 1 - p);
-        sm.bcast[1] = cum;
-        break;
-      }
-      cum += c;
-    }
-  }
-  __syncthreads();
-  const uint32_t bin = sm.bcast[0];
-  above = sm.bcast[1];
-  __syncthreads();
-  return bin;
-}
-
-// Merge of all chunks' candidates (run by the last CTA of sequence b).
-// surv_key / surv_ent: `surv_cap`-entry shared-memory scratch (>= kHistBins
-// words for surv_key).  Every global read is a coalesced 16-byte load.
-template <int NT>
-__device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* surv_key,
-                               int32_t* surv_ent, int surv_cap) {
-  const bool tr = a.trace && b == 0 && threadIdx.x == 0;
-  const long long t0 = clock64();
-  const int n_slots = a.n_chunks * a.K_sel;   // K_sel is a multiple of 4
-  const uint32_t* ck = a.cand_key + (int64_t)b * n_slots;
-  const int32_t* ci = a.cand_idx + (int64_t)b * n_slots;
-  uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
-  const int K = a.pool_out > 0 ? a.pool_out : a.topk;
-
-  // (a) the histogram into shared memory (and zeroed for the next call)
-  uint32_t* hs = surv_key;
-  {
-    // every load in flight before any store (the zeroing stores would
-    // otherwise order each load after the previous one)
-    constexpr int kV = kHistBins / 4, kPerT = (kV + NT - 1) / NT;
-    uint4 hv[kPerT];
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) {
-      const int v = threadIdx.x + k * NT;
-      hv[k] = v < kV ? __ldcg(reinterpret_cast<const uint4*>(hist) + v) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int k = 0; k < kPerT; ++k) {
-      const int v = threadIdx.x + k * NT;
-      if (v < kV) {
-        reinterpret_cast<uint4*>(hs)[v] = hv[k];
-        reinterpret_cast<uint4*>(hist)[v] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-  }
-  __syncthreads();
-  uint32_t total, keff, above;
-  const uint32_t tb = find_bin_desc<NT>(hs, (uint32_t)K, sm, total, keff, above);
-  const int n_real = (int)total;
-  // Survivors are the candidates with key >= lo_key.  When the threshold
-  // bin is too crowded for shared memory (many exact ties at the boundary),
-  // a second histogram of the next 12 key bits over that bin's candidates
-  // narrows it first.
-  uint32_t lo_key = tb << kHistShift;
-  const uint32_t in_tb = hs[tb];
-  if (keff > 0 && above + in_tb > (uint32_t)surv_cap) {
-    __syncthreads();   // everyone has read hs[tb]
-    for (int i = threadIdx.x; i < kHistBins; i += NT) hs[i] = 0u;
-    __syncthreads();
-    constexpr int kV2 = 4;   // 16-byte loads in flight per thread
-    for (int base = 0; base < n_slots; base += 4 * kV2 * NT) {
-      uint4 k4[kV2];
-#pragma unroll
-      for (int v = 0; v < kV2; ++v) {
-        const int sv = base + 4 * (threadIdx.x + v * NT);
-        k4[v] = sv < n_slots ? __ldcg(reinterpret_cast<const uint4*>(ck + sv)) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int v = 0; v < kV2; ++v) {
-        const uint32_t kk[4] = {k4[v].x, k4[v].y, k4[v].z, k4[v].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (kk[e] != 0u && (kk[e] >> kHistShift) == tb) atomicAdd(&hs[(kk[e] >> 8) & 0xFFFu], 1u);
-      }
-    }
-    __syncthreads();
-    uint32_t total2, keff2, above2;
-    const uint32_t tb2 = find_bin_desc<NT>(hs, keff - above, sm, total2, keff2, above2);
-    lo_key |= tb2 << 8;
-  }
-  trace_at(a.st, tr, 20, t0);
-
-  // (b) survivors (key >= lo_key) in slot order, 16 slots per thread per
-  // pass; the next pass's loads are issued before this pass is compacted
-  constexpr int kPer = 16;
   uint32_t n_surv = 0;
-  uint4 nk[kPer / 4];
-  int4 ni[kPer / 4];
-  auto fetch = [&](int base) {
-    const int s0 = base + kPer * (int)threadIdx.x;
+#pragma unroll 1
+  for (int base = 0; base < n_cand; base += NT * kU) {
+    const int wbase = base + warp * 32 * kU;
+    uint32_t u[kU];
+    int32_t x[kU];
+    {
+      int v = wbase + lane;
+      int c = 0;
+      if (v < n_cand) {
+        int lo = 0, hi = nch;   // last c with cprefix[c] <= v
+#pragma unroll 1
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if ((int)sm.cprefix[mid] <= v) lo = mid;
+          else hi = mid;
+        }
+        c = lo;
+      }
 #pragma unroll
-    for (int v = 0; v < kPer / 4; ++v) {
-      const int sv = s0 + 4 * v;
-      nk[v] = make_uint4(0u, 0u, 0u, 0u);
-      ni[v] = make_int4(-1, -1, -1, -1);
-      if (sv < n_slots) {
-        nk[v] = __ldcg(reinterpret_cast<const uint4*>(ck + sv));
-        ni[v] = __ldcg(reinterpret_cast<const int4*>(ci + sv));
+      for (int k = 0; k < kU; ++k, v += 32) {
+        u[k] = 0u;
+        x[k] = -1;
+        if (v < n_cand) {
+          while ((int)sm.cprefix[c + 1] <= v) ++c;
+          const int64_t sl = (int64_t)c * a.chunk + (v - (int)sm.cprefix[c]);
+          u[k] = __ldcg(cl.gk + sl);
+          x[k] = __ldcg(cl.gi + sl);
+        }
       }
     }
-  };
-  fetch(0);
-  for (int base = 0; base < n_slots; base += kPer * NT) {
-    uint32_t kk[kPer];
-    int32_t ii[kPer];
+    if (tr && base == 0) a.st->pad[17] = (int32_t)(clock64() - t0);
+    uint32_t bal[kU], cnt = 0;
 #pragma unroll
-    for (int v = 0; v < kPer / 4; ++v) {
-      kk[4 * v] = nk[v].x; kk[4 * v + 1] = nk[v].y; kk[4 * v + 2] = nk[v].z; kk[4 * v + 3] = nk[v].w;
-      ii[4 * v] = ni[v].x; ii[4 * v + 1] = ni[v].y; ii[4 * v + 2] = ni[v].z; ii[4 * v + 3] = ni[v].w;
+    for (int k = 0; k < kU; ++k) {
+      const bool f = u[k] != 0u && u[k] >= lo_key;
+      bal[k] = __ballot_sync(0xffffffffu, f);
+      if (tr && base == 0 && k == 0) a.st->pad[18] = (int32_t)(clock64() - t0);
+      cnt += __popc(bal[k]);
+      if (hint) {
+        const uint32_t d = (f && key_bin(u[k]) == tb) ? ((u[k] >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.sub[d], (uint32_t)__popc(peers));
+      }
     }
-    if (base + kPer * NT < n_slots) fetch(base + kPer * NT);
-    uint32_t f = 0;
+    if (tr && base == 0) a.st->pad[59] = (int32_t)(clock64() - t0);
+    if (lane == 0) sm.wcnt[warp] = cnt;
+    __syncthreads();
+    if (tr && base == 0) a.st->pad[60] = (int32_t)(clock64() - t0);
+    uint32_t pos = n_surv, tot = 0;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) f |= (uint32_t)((kk[e] != 0u) && (kk[e] >= lo_key)) << e;
-    uint32_t pos, d0, tot, d1;
-    block_scan2<NT>((uint32_t)__popc(f), 0u, pos, d0, tot, d1, sm.sel);
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t c = sm.wcnt[w];
+      pos += w < warp ? c : 0u;
+      tot += c;
+    }
     if (n_surv + tot <= (uint32_t)surv_cap) {
-      pos += n_surv;
 #pragma unroll
-      for (int e = 0; e < kPer; ++e)
-        if ((f >> e) & 1u) {
-          surv_key[pos] = kk[e];
-          surv_ent[pos] = ii[e];
-          ++pos;
+      for (int k = 0; k < kU; ++k) {
+        if ((bal[k] >> lane) & 1u) {
+          const uint32_t at = pos + __popc(bal[k] & ((1u << lane) - 1u));
+          surv_key[at] = u[k];
+          surv_ent[at] = x[k];
         }
+        pos += __popc(bal[k]);
+      }
     }
     n_surv += tot;
+    __syncthreads();   // wcnt is rewritten next round
   }
-  __syncthreads();
   trace_at(a.st, tr, 21, t0);
-  if (tr) a.st->pad[23] = (int32_t)n_surv;
+  if (tr) {
+    a.st->pad[23] = (int32_t)n_surv;
+    a.st->pad[25] = n_cand;
+    a.st->pad[26] = (int32_t)tb;
+    a.st->pad[27] = (int32_t)above;
+    a.st->pad[28] = (int32_t)n_total;
+  }
+  // The sub-bin of the threshold bin that holds the keff-th largest key: the
+  // survivors below it are dropped (in order, in place) before the select.
+  uint32_t prefix = lo_key, above2 = above;
+  int top_bits = kBinShift;
+  if (hint && n_surv <= (uint32_t)surv_cap) {
+    const uint32_t need = (uint32_t)keff - above;
+    if (warp == 0) {
+      // lane l holds sub-bins 255 - 8l .. 248 - 8l (descending)
+      uint32_t c8[8], t8 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = sm.sub[255 - 8 * lane - j];
+        t8 += c8[j];
+      }
+      uint32_t incl = t8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t before = incl - t8;
+      if (before < need && incl >= need) {
+        uint32_t cum = before;
+        for (int j = 0; j < 8; ++j) {
+          if (cum + c8[j] >= need) {
+            sm.bcast[0] = (uint32_t)(255 - 8 * lane - j);
+            sm.bcast[1] = cum;
+            break;
+          }
+          cum += c8[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t t2 = sm.bcast[0] & 255u;
+    above2 = above + sm.bcast[1];
+    prefix = lo_key | (t2 << (kBinShift - 8));
+    top_bits = kBinShift - 8;
+    // in-place ordered compaction to keys >= prefix, kU per thread per round
+    // (a round's reads all happen before its writes, which never reach past it)
+    uint32_t kept = 0;
+#pragma unroll 1
+    for (int base = 0; base < (int)n_surv; base += NT * kU) {
+      const int wbase = base + warp * 32 * kU;
+      uint32_t u[kU];
+      int32_t x[kU];
+      uint32_t bal[kU], cnt = 0;
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        const int v = wbase + k * 32 + lane;
+        u[k] = v < (int)n_surv ? surv_key[v] : 0u;
+        x[k] = v < (int)n_surv ? surv_ent[v] : -1;
+        bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && u[k] >= prefix);
+        cnt += __popc(bal[k]);
+      }
+      if (lane == 0) sm.wcnt[warp] = cnt;
+      __syncthreads();
+      uint32_t pos = kept, tot = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const uint32_t c = sm.wcnt[w];
+        pos += w < warp ? c : 0u;
+        tot += c;
+      }
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
+        if ((bal[k] >> lane) & 1u) {
+          const uint32_t at = pos + __popc(bal[k] & ((1u << lane) - 1u));
+          surv_key[at] = u[k];
+          surv_ent[at] = x[k];
+        }
+        pos += __popc(bal[k]);
+      }
+      kept += tot;
+      __syncthreads();
+    }
+    n_surv = kept;
+  }
+  trace_at(a.st, tr, 19, t0);
+  if (tr) a.st->pad[31] = (int32_t)n_surv;
   if (n_surv <= (uint32_t)surv_cap) {
-    emit_outputs<NT>(
-        a, b, (int)n_surv, n_real, [&](int i) { return surv_key[i]; },
-        [&](int i) { return surv_ent[i]; }, sm);
+    SelSrc ss{};
+    ss.key = surv_key;
+    ss.ent = surv_ent;
+    emit_outputs<NT>(a, b, ss, (int)n_surv, (int)n_total, pool_key, pool_ent, sm, prefix,
+                     hint ? top_bits : 32, hint ? (int)above2 : 0);
   } else {
-    // a crowded threshold bin: select on the full lists in global memory
-    emit_outputs<NT>(
-        a, b, n_slots, n_real, [&](int i) { return __ldcg(ck + i); },
-        [&](int i) { return __ldcg(ci + i); }, sm);
+    // a crowded threshold bin: select on the candidate lists in global memory
+    emit_outputs<NT>(a, b, cl, n_cand, (int)n_total, pool_key, pool_ent, sm, lo_key,
+                     hint ? kBinShift : 32, hint ? (int)above : 0);
   }
   trace_at(a.st, tr, 22, t0);
+  // leave the sequence's histogram and state zero for the next call
+  const int bot = kBins - (int)__ldcg(seq + 2);
+  if (top > 0) {
+    const int z0 = bot & ~3, z1 = (top + 3) & ~3;
+    for (int v = z0 / 4 + (int)threadIdx.x; v < z1 / 4; v += NT)
+      reinterpret_cast<uint4*>(gh)[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (threadIdx.x == 0) {
+    seq[1] = 0u;
+    seq[2] = 0u;
+    seq[0] = 0u;
+  }
 }
 
-// Local top-K of a scored chunk -> workspace (+ histogram); then the ticket.
-// `scratch` (2 * surv_cap words of shared memory, free once the chunk's own
-// selection is done) may alias `keys`.
+// After scoring: `keys[0, n_elem)` hold this chunk's keys (0 = no entry),
+// `hist` (kBins words of shared memory) their histogram, sm.n_real / kmin /
+// kmax the count and range of real keys.  Publishes the histogram, writes
+// the chunk's candidates and takes the ticket; the last CTA merges.
+// `scratch` (scratch_words words of shared memory, dead after this chunk's
+// candidates are written; may alias `keys` and `hist`) serves the merge.
 template <int NT>
 __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int n_elem,
-                                       int64_t first_entry, const uint32_t* keys, uint32_t* scratch,
-                                       int surv_cap, MergeSmem<NT>& sm) {
-  const int slot0 = (b * a.n_chunks + chunk) * a.K_sel;
-  uint32_t* ck = a.cand_key + slot0;
-  int32_t* ci = a.cand_idx + slot0;
-  uint32_t* hist = a.ghist + (int64_t)b * kHistBins;
-  const int kk = min(a.K_sel, (int)sm.n_real);
+                                       int64_t first_entry, const uint32_t* keys, const uint32_t* hist,
+                                       uint32_t* scratch, int scratch_words, MergeSmem<NT>& sm) {
   const int32_t* pool = a.pool ? a.pool + (int64_t)b * a.pool_len + first_entry : nullptr;
   const bool tr = a.trace && b == 0 && chunk == 0 && threadIdx.x == 0;
+  const int n_real = (int)sm.n_real;
+  const int K = a.pool_out > 0 ? a.pool_out : a.topk;
+  auto entry_of = [&](int i) { return pool ? pool[i] : (int32_t)(first_entry + i); };
   if (a.n_chunks == 1 && a.pool_out == 0) {
     // one chunk holds the whole sequence: its top-k is the answer
     int32_t* oi = a.out_idx + (int64_t)b * a.topk;
-    const int kt = min(a.topk, (int)sm.n_real);
-    block_select_ordered<NT>(
-        n_elem, kt, [&](int i) { return keys[i]; },
-        [&](int pos, int i) { oi[pos] = pool ? pool[i] : (int32_t)(first_entry + i); }, sm.sel);
+    const int kt = min(a.topk, n_real);
+    SelSrc src{};
+    src.key = keys;
+    src.pool = pool;
+    src.first = first_entry;
+    select_ordered<NT>(src, n_elem, kt, 0u, 32, 0, oi, nullptr, sm.sel);
+#pragma unroll 1
     for (int i = kt + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
     pdl_launch_dependents();
     return;
   }
   const long long t0 = clock64();
-  long long marks[2] = {0, 0};
-  block_select_ordered<NT>(
-      n_elem, kk, [&](int i) { return keys[i]; },
-      [&](int pos, int i) {
-        const uint32_t u = keys[i];
-        ck[pos] = u;
-        ci[pos] = pool ? pool[i] : (int32_t)(first_entry + i);
-        sm.pool_key[pos] = u;   // free until the merge
-      },
-      sm.sel, tr ? marks : nullptr);
-  if (tr) {
-    a.st->pad[12] = (int32_t)(marks[0] - t0);
-    a.st->pad[13] = (int32_t)(marks[1] - t0);
+  uint32_t* seq = a.seq_state + (int64_t)b * kSeqWords;
+  uint32_t* gh = a.ghist + (int64_t)b * kBins;
+  // 1. publish the histogram of the real keys
+  const int bmin = n_real > 0 ? (int)key_bin(sm.kmin) : 0;
+  const int bmax = n_real > 0 ? (int)key_bin(sm.kmax) : -1;
+#pragma unroll 1
+  for (int v = bmin + (int)threadIdx.x; v <= bmax; v += NT) {
+    const uint32_t c = hist[v];
+    if (c) atomicAdd(gh + v, c);
   }
-  for (int i = kk + threadIdx.x; i < a.K_sel; i += NT) {
-    ck[i] = 0u;
-    ci[i] = -1;
-  }
-  __syncthreads();
-  // The candidates' keys crowd into a few histogram bins: one global atomic
-  // per distinct bin per warp instead of one per candidate.
-  {
-    const int lane = threadIdx.x & 31;
-    const int k_round = (kk + 31) / 32 * 32;
-    for (int i = threadIdx.x; i < k_round; i += NT) {
-      const uint32_t bin = i < kk ? (sm.pool_key[i] >> kHistShift) : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin != 0xFFFFFFFFu && (__ffs(peers) - 1) == lane) atomicAdd(hist + bin, (uint32_t)__popc(peers));
-    }
+  if (threadIdx.x == 0 && n_real > 0) {
+    atomicMax(seq + 1, (uint32_t)bmax + 1u);
+    atomicMax(seq + 2, (uint32_t)(kBins - bmin));
   }
   trace_at(a.st, tr, 10, t0);
+  // 2. lower bound on the sequence's threshold bin (no wait for this chunk's
+  // own additions: the bound holds for any snapshot).  The scan starts at
+  // this chunk's own top bin: keys of other chunks above it are left out,
+  // which only lowers the counts and so keeps the bound valid.
+  uint32_t bound = 0;
+  if (n_real > K) bound = chunk_bound<NT>(gh, hist, bmax + 1, (uint32_t)K, sm);
+  const uint32_t lo_key = bound << kBinShift;
+  trace_at(a.st, tr, 11, t0);
+  // 3. candidates (real keys >= lo_key) in entry order
+  const int64_t slot0 = ((int64_t)b * a.n_chunks + chunk) * a.chunk;
+  uint32_t* ck = a.cand_key + slot0;
+  int32_t* ci = a.cand_idx + slot0;
+  {
+    // warp w takes a contiguous range of 32-key groups: count, one barrier
+    // for the warps' offsets, then write in order
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = NT / 32;
+    const int groups = (n_elem + 31) / 32, gper = (groups + kWarps - 1) / kWarps;
+    const int i0 = min(n_elem, warp * gper * 32), i1 = min(n_elem, (warp + 1) * gper * 32);
+    auto take = [&](int i) {
+      const uint32_t u = i < i1 ? keys[i] : 0u;
+      return u != 0u && u >= lo_key;
+    };
+    uint32_t cnt = 0;
+#pragma unroll 1
+    for (int i = i0 + lane; i - lane < i1; i += 32) cnt += __popc(__ballot_sync(0xffffffffu, take(i)));
+    if (lane == 0) sm.wcnt[warp] = cnt;
+    __syncthreads();
+    uint32_t pos = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t c = sm.wcnt[w];
+      pos += w < warp ? c : 0u;
+      tot += c;
+    }
+#pragma unroll 1
+    for (int i = i0 + lane; i - lane < i1; i += 32) {
+      const bool f = take(i);
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const uint32_t at = pos + __popc(bal & ((1u << lane) - 1u));
+        ck[at] = keys[i];
+        ci[at] = entry_of(i);
+      }
+      pos += __popc(bal);
+    }
+    if (threadIdx.x == 0)
+      reinterpret_cast<uint2*>(a.ccount)[(int64_t)b * a.n_chunks + chunk] = make_uint2(tot, (uint32_t)n_real);
+  }
+  trace_at(a.st, tr, 12, t0);
+  if (tr) {
+    a.st->pad[29] = (int32_t)bound;
+    a.st->pad[30] = (int32_t)reinterpret_cast<uint2*>(a.ccount)[(int64_t)b * a.n_chunks + chunk].x;
+  }
   __threadfence();
   __syncthreads();
-  trace_at(a.st, tr, 11, t0);
   pdl_launch_dependents();   // the next kernel may take the SMs this grid frees
-  if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(a.counters + b, 1u);
+  if (threadIdx.x == 0) sm.ticket = (int)atomicAdd(seq, 1u);
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
   __threadfence();
-  merge_and_emit<NT>(a, b, sm, scratch, reinterpret_cast<int32_t*>(scratch + surv_cap), surv_cap);
-  if (threadIdx.x == 0) atomicExch(a.counters + b, 0u);
+  merge_and_emit<NT>(a, b, sm, scratch, scratch_words, bound);
 }
 
 }  // namespace ckv

@@ -47,12 +47,15 @@ def test_workspace_sizes(lib):
     a = f(1, 4, 128, 64, 262144, 512, 0)
     b = f(1, 8, 128, 64, 262144, 512, 0)
     assert 256 < a < b
-    assert f(1, 8, 64, 64, 65536, 512, 2048) > f(1, 8, 64, 64, 65536, 512, 0)
-    # attention: status word + the shared between-call state (index tickets
-    # and 4096-bin histograms, then the attention's merge counters, each
-    # 256-byte aligned) + the merge partials of up to 16 CTAs per sequence
+    # candidates are sized by the chunking (one slot per entry), not by the
+    # pool of a CSA2 Full layer
+    assert f(1, 8, 64, 64, 65536, 512, 2048) == f(1, 8, 64, 64, 65536, 512, 0)
+    # attention: status word + the shared between-call state (per-sequence
+    # index state and 8192-bin histograms, then the attention's merge
+    # counters, each 256-byte aligned) + the merge partials of up to 16 CTAs
+    # per sequence
     part = 16 * (32 * 128 * 4 + 256) * 4
-    zero = 256 + 3 * 4096 * 4 + 256
+    zero = 256 + 3 * 8192 * 4 + 256
     assert f(2, 3, 128, 0, 0, 0, 0) == 256 + zero + 3 * part
     assert f(3, 3, 128, 0, 0, 0, 0) == 256 + zero + 3 * part
     # the index/top-k call reserves the same state before its candidates

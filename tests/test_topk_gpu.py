@@ -143,3 +143,30 @@ def test_index_out_of_range_pool_entry_is_flagged():
     assert b.read_device_status(ws) == -6
     sc, _ = _oracle_scores(keys[0], qi[0], w[0], "fp4")
     assert list(idx.cpu().numpy()[0]) == list(oi.topk_set(sc, 2, candidates=[5, 7, 9]))
+
+
+@pytest.mark.parametrize("fmt,HI,n,topk,pool_out", [
+    ("fp4", 64, 20000, 512, 0),       # tensor-core scorer: more equal keys than its merge buffer
+    ("fp4", 64, 20000, 512, 2048),    # ... with the CSA2 Full layer's pool
+    ("bf16", 8, 20000, 512, 0),       # CUDA-core scorer
+    ("fp4", 64, 3000, 512, 0),        # equal keys that still fit the merge buffer
+])
+def test_index_all_equal_scores_take_the_lowest_entries(fmt, HI, n, topk, pool_out):
+    """A zero indexer query makes every score 0: every key ties, the whole
+    sequence lands in one histogram bin, and the top-k must be the lowest
+    entries (the merge's crowded-boundary path when they outnumber its
+    shared-memory buffer)."""
+    b = ckv()
+    keys = [wl.rms_rows((n, 128), 77, "cuda")]
+    plane = gpu_plane(fmt, 128, keys, n)
+    qi = torch.zeros((1, HI, 128), dtype=torch.bfloat16, device="cuda")
+    w = wl.head_weights((1, HI), 78, "cuda")
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, HI, n, topk, pool_out))
+    for _ in range(2):    # the second call checks that the workspace was left clean
+        res = b.csa_index_topk(plane, n_comp, n, qi, w, topk, pool_out=pool_out, ws=ws)
+        assert b.read_device_status(ws) == 0
+        idx = (res[0] if pool_out else res).cpu().numpy()[0]
+        assert np.array_equal(idx, np.arange(topk))
+        if pool_out:
+            assert np.array_equal(res[1].cpu().numpy()[0], np.arange(pool_out))
