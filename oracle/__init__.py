@@ -13,8 +13,9 @@ generator with the CUDA path.
 
 Sources (titles of the pages, with the section each function follows):
   * "DeepSeek-V4 KV Cache 深度分析" -- appendix calculator, §二 (entry layout),
-    §三 (CSA/HCA), §四 (indexer), §六 (precision), §七 (total formula),
-    §十一 (forward flow chart).
+    §三 (CSA/HCA), §四 (indexer, its Hadamard rotation before FP4), §五
+    (RoPE at the query and at the output, position -i), §六 (precision), §七
+    (total formula), §十一 (forward flow chart).
   * "DeepSeek, KV 캐시를 토큰당 890바이트로 줄인 V4.1-Flash 공개" -- 핵심 내용
     (CSA2 modes, FP4 E2M1 + E4M3/16-channel main KV, the 2688 bound).
   * "KV cache 890 bajtów na token" -- "Trzy mechanizmy" (CSA2 Full / Reindex /
@@ -26,4 +27,4 @@ The pages' 890 B/token figure for V4.1-Flash cannot be derived from what they
 print, so no function computes it.
 """
 
-from . import fp_formats, sizes, indexer, attention, csa2  # noqa: F401
+from . import fp_formats, sizes, indexer, attention, csa2, rope, hadamard  # noqa: F401

@@ -227,13 +227,17 @@ def mixed_dequantize(data, scale, nope_block: int = NOPE_DIM) -> np.ndarray:
 
 def quantize_entries(x, fmt: str, nope_block: int = NOPE_DIM):
     """Entry rows -> (data bytes, scale) of the plane format ``fmt``
-    ('bf16', 'mixed' or 'fp4')."""
+    ('bf16', 'mixed', 'fp4', or 'fp4h': FP4 of the Hadamard-rotated 128-d
+    indexer vector, see ``oracle/hadamard.py``)."""
     if fmt == "bf16":
         return bf16_bytes(x), None
     if fmt == "mixed":
         return mixed_quantize(x, nope_block)
     if fmt == "fp4":
         return fp4_quantize(x)
+    if fmt == "fp4h":
+        from .hadamard import fp4_quantize_hadamard
+        return fp4_quantize_hadamard(x)
     raise ValueError(fmt)
 
 
@@ -243,6 +247,6 @@ def dequantize_entries(data, scale, fmt: str, nope_block: int = NOPE_DIM) -> np.
         return bf16_from_bytes(data)
     if fmt == "mixed":
         return mixed_dequantize(data, scale, nope_block)
-    if fmt == "fp4":
-        return fp4_dequantize(data, scale)
+    if fmt in ("fp4", "fp4h"):
+        return fp4_dequantize(data, scale)   # fp4h: values in the rotated basis
     raise ValueError(fmt)

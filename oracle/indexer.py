@@ -24,10 +24,15 @@ import numpy as np
 from .fp_formats import fp4_quantize, fp4_dequantize
 
 
-def indexer_query(q_idx, quantize_fp4: bool) -> np.ndarray:
-    """float64 query values as the product sees them."""
+def indexer_query(q_idx, quantize_fp4: bool, hadamard: bool = False) -> np.ndarray:
+    """float64 query values as the product sees them.  With ``hadamard`` (keys
+    stored Hadamard-rotated, §四) the query is rotated the same way before its
+    FP4 quantisation."""
     q_idx = np.asarray(q_idx, dtype=np.float32)
     if quantize_fp4:
+        if hadamard:
+            from .hadamard import hadamard_rotate_f32
+            q_idx = hadamard_rotate_f32(q_idx)
         packed, sc = fp4_quantize(q_idx)
         return fp4_dequantize(packed, sc)
     return q_idx.astype(np.float64)
