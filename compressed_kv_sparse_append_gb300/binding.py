@@ -17,7 +17,7 @@ if not os.path.exists(_LIB_PATH):
                       "python compressed_kv_sparse_append_gb300/build.py)")
 lib = ctypes.CDLL(_LIB_PATH)
 
-FMT = {"bf16": 0, "mixed": 1, "fp4": 2}
+FMT = {"bf16": 0, "mixed": 1, "fp4": 2, "fp4h": 3}
 OP_APPEND, OP_INDEX_TOPK, OP_SPARSE_ATTN, OP_HCA_ATTN, OP_CSA2 = range(5)
 CSA2_FULL, CSA2_REINDEX, CSA2_REUSE = 0, 1, 2
 MAX_LAYERS = 8
@@ -30,12 +30,26 @@ class CPlane(ctypes.Structure):
                 ("cap", _i64), ("data", _vp), ("scale", _vp)]
 
 
+class CRope(ctypes.Structure):
+    _fields_ = [("pos", _vp), ("inv_freq", _vp), ("rotate_q", _i32), ("rotate_out", _i32)]
+
+
+class Rope:
+    """RoPE at the attention's ends (include/ckv.h, ckv_rope): pos [B] int32
+    query positions, inv_freq [32] f32 on the device."""
+
+    def __init__(self, pos, inv_freq, rotate_q=True, rotate_out=True):
+        self.pos, self.inv_freq = pos, inv_freq
+        self.c = CRope(pos.data_ptr(), inv_freq.data_ptr(), int(bool(rotate_q)), int(bool(rotate_out)))
+
+
 class CGroup(ctypes.Structure):
     _fields_ = [("n_layers", _i32), ("role", _i32 * MAX_LAYERS), ("kv_src", _i32 * MAX_LAYERS),
                 ("idx_src", _i32 * MAX_LAYERS), ("kv", CPlane * MAX_LAYERS),
                 ("win", CPlane * MAX_LAYERS), ("idx_keys", CPlane), ("q", _vp * MAX_LAYERS),
                 ("q_idx", _vp * MAX_LAYERS), ("w", _vp * MAX_LAYERS), ("out", _vp * MAX_LAYERS),
-                ("lse", _vp * MAX_LAYERS), ("idx_out", _vp * MAX_LAYERS), ("pool_len", _i32)]
+                ("lse", _vp * MAX_LAYERS), ("idx_out", _vp * MAX_LAYERS), ("pool_len", _i32),
+                ("rope", CRope)]
 
 
 _P = ctypes.POINTER(CPlane)
@@ -52,6 +66,12 @@ lib.ckv_csa_index_topk.argtypes = [_P, _vp, _i32, _i32, _vp, _vp, _i32, _i32, _v
 lib.ckv_csa_sparse_attn.restype = _i32
 lib.ckv_csa_sparse_attn.argtypes = [_P, _P, _vp, _vp, _i32, _i32, _vp, _i32, _f32, _vp, _vp, _vp,
                                     _sz, _vp]
+lib.ckv_csa_sparse_attn_rope.restype = _i32
+lib.ckv_csa_sparse_attn_rope.argtypes = [_P, _P, _vp, _vp, _i32, _i32, _vp, _i32, _f32, _vp, _vp,
+                                         ctypes.POINTER(CRope), _vp, _sz, _vp]
+lib.ckv_hca_attn_rope.restype = _i32
+lib.ckv_hca_attn_rope.argtypes = [_P, _vp, _i32, _P, _vp, _i32, _vp, _i32, _f32, _vp, _vp,
+                                  ctypes.POINTER(CRope), _vp, _sz, _vp]
 lib.ckv_hca_attn.restype = _i32
 lib.ckv_hca_attn.argtypes = [_P, _vp, _i32, _P, _vp, _i32, _vp, _i32, _f32, _vp, _vp, _vp, _sz, _vp]
 lib.ckv_csa2_group_decode.restype = _i32
@@ -100,13 +120,13 @@ def _stream(stream):
 
 
 def entry_bytes(fmt: str, dim: int) -> int:
-    return {"bf16": dim * 2, "mixed": 576, "fp4": dim // 2}[fmt]
+    return {"bf16": dim * 2, "mixed": 576, "fp4": dim // 2, "fp4h": dim // 2}[fmt]
 
 
 def scale_shape(fmt: str, dim: int, nope_block: int = 448):
     if fmt == "mixed":
         return (448 // nope_block,), torch.float32
-    if fmt == "fp4":
+    if fmt in ("fp4", "fp4h"):
         return (dim // 16,), torch.uint8
     return None, None
 
@@ -222,12 +242,17 @@ def csa_index_topk_static(keys: Plane, n_comp, n_comp_max, q_idx, w, topk, pool=
 
 
 def csa_sparse_attn(kv: Plane, win: Plane, win_len, idx, q, sm_scale, out=None, lse=None, ws=None,
-                    stream=None):
+                    stream=None, rope: "Rope" = None):
     B, H = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty_like(q)
     ws = ws if ws is not None else new_workspace(workspace_bytes(OP_SPARSE_ATTN, B), q.device)
     ck, cw = kv.c(), win.c()
+    if rope is not None:
+        _check(lib.ckv_csa_sparse_attn_rope(ck, cw, _ptr(win_len), _ptr(idx), B, idx.shape[1], _ptr(q), H,
+                                            sm_scale, _ptr(out), _ptr(lse), ctypes.byref(rope.c), _ptr(ws),
+                                            ws.numel(), _stream(stream)), "csa_sparse_attn_rope")
+        return out
     _check(lib.ckv_csa_sparse_attn(ck, cw, _ptr(win_len), _ptr(idx), B,
                                    idx.shape[1], _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
                                    ws.numel(), _stream(stream)), "csa_sparse_attn")
@@ -235,12 +260,17 @@ def csa_sparse_attn(kv: Plane, win: Plane, win_len, idx, q, sm_scale, out=None, 
 
 
 def hca_attn(kv: Plane, n_comp, n_comp_max, win: Plane, win_len, q, sm_scale, out=None, lse=None,
-             ws=None, stream=None):
+             ws=None, stream=None, rope: "Rope" = None):
     B, H = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty_like(q)
     ws = ws if ws is not None else new_workspace(workspace_bytes(OP_HCA_ATTN, B), q.device)
     ck, cw = kv.c(), win.c()
+    if rope is not None:
+        _check(lib.ckv_hca_attn_rope(ck, _ptr(n_comp), n_comp_max, cw, _ptr(win_len), B, _ptr(q), H, sm_scale,
+                                     _ptr(out), _ptr(lse), ctypes.byref(rope.c), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "hca_attn_rope")
+        return out
     _check(lib.ckv_hca_attn(ck, _ptr(n_comp), n_comp_max, cw,
                             _ptr(win_len), B, _ptr(q), H, sm_scale, _ptr(out), _ptr(lse), _ptr(ws),
                             ws.numel(), _stream(stream)), "hca_attn")
@@ -248,7 +278,7 @@ def hca_attn(kv: Plane, n_comp, n_comp_max, win: Plane, win_len, q, sm_scale, ou
 
 
 def make_group(roles, kv_src, idx_src, kv, win, idx_keys, q, q_idx, w, out, lse=None,
-               idx_out=None, pool_len=2048) -> CGroup:
+               idx_out=None, pool_len=2048, rope: "Rope" = None) -> CGroup:
     g = CGroup()
     L = len(roles)
     g.n_layers = L
@@ -264,6 +294,9 @@ def make_group(roles, kv_src, idx_src, kv, win, idx_keys, q, q_idx, w, out, lse=
         g.idx_out[l] = idx_out[l].data_ptr() if idx_out is not None and idx_out[l] is not None else None
     g.idx_keys = idx_keys.c()
     g.pool_len = pool_len
+    if rope is not None:
+        g.rope = rope.c
+        g._rope_keepalive = rope
     return g
 
 

@@ -74,6 +74,11 @@ ckv_status check_plane(const ckv_plane* p, int dim, int B) {
     if (!p->scale || (dim != 512 && dim != 128)) return CKV_ERR_INVALID;
     return CKV_OK;
   }
+  if (p->fmt == CKV_FMT_FP4H) {   // Hadamard-rotated FP4: indexer keys only
+    if (dim != 128) return CKV_ERR_UNSUPPORTED;
+    if (!p->scale) return CKV_ERR_INVALID;
+    return CKV_OK;
+  }
   if (p->fmt == CKV_FMT_MIXED) {
     if (dim != 512) return CKV_ERR_UNSUPPORTED;
     if (!p->scale || !aligned16(p->scale)) return CKV_ERR_INVALID;
@@ -210,7 +215,8 @@ ckv_status check_index_args(const ckv_plane* keys, const int32_t* n_comp, int B,
   if (!aligned16(q_idx)) return CKV_ERR_INVALID;
   ckv_status s = check_plane(keys, 128, B);
   if (s) return s;
-  if (keys->fmt != CKV_FMT_FP4 && keys->fmt != CKV_FMT_BF16) return CKV_ERR_UNSUPPORTED;
+  if (keys->fmt != CKV_FMT_FP4 && keys->fmt != CKV_FMT_FP4H && keys->fmt != CKV_FMT_BF16)
+    return CKV_ERR_UNSUPPORTED;
   if (HI <= 0 || HI > kMaxHI) return CKV_ERR_UNSUPPORTED;
   if (n_comp_max < 0 || n_comp_max > keys->cap) return CKV_ERR_INVALID;
   if (topk <= 0 || topk > kMaxPool) return CKV_ERR_UNSUPPORTED;
@@ -316,7 +322,22 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.st = st;
   a.use_tma = 0;
   a.progress = debug_progress();
+  a.rope_pos = nullptr;
+  a.rope_freq = nullptr;
+  a.rope_q = 0;
+  a.rope_out = 0;
   return a;
+}
+
+// RoPE of the attention's ends: a null descriptor or pos means none.
+ckv_status set_rope(AttnArgs& a, const ckv_rope* r) {
+  if (!r || !r->pos) return CKV_OK;
+  if (!r->inv_freq) return CKV_ERR_INVALID;
+  a.rope_pos = r->pos;
+  a.rope_freq = r->inv_freq;
+  a.rope_q = r->rotate_q ? 1 : 0;
+  a.rope_out = r->rotate_out ? 1 : 0;
+  return CKV_OK;
 }
 
 }  // namespace
@@ -406,10 +427,10 @@ ckv_status ckv_csa_index_topk(const ckv_plane* idx_keys, const int32_t* n_comp, 
                    w8 + kStatusBytes, static_cast<cudaStream_t>(stream));
 }
 
-ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
-                               const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
-                               int32_t H, float sm_scale, void* out_bf16, float* lse, void* ws,
-                               size_t ws_bytes, void* stream) {
+ckv_status ckv_csa_sparse_attn_rope(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
+                                    const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
+                                    int32_t H, float sm_scale, void* out_bf16, float* lse,
+                                    const ckv_rope* rope, void* ws, size_t ws_bytes, void* stream) {
   NvtxRange nvtx_range("ckv_csa_sparse_attn");
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
@@ -419,6 +440,8 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
+  s = set_rope(a, rope);
+  if (s) return s;
   attn_set_ws_single(a, static_cast<uint8_t*>(ws) + kStatusBytes, B);
   a.idx = idx;
   a.topk = topk;
@@ -428,10 +451,19 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const 
   return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
 }
 
-ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_comp_max,
-                        const ckv_plane* win, const int32_t* win_len, int32_t B,
-                        const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
-                        float* lse, void* ws, size_t ws_bytes, void* stream) {
+ckv_status ckv_csa_sparse_attn(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
+                               const int32_t* idx, int32_t B, int32_t topk, const void* q_bf16,
+                               int32_t H, float sm_scale, void* out_bf16, float* lse, void* ws,
+                               size_t ws_bytes, void* stream) {
+  return ckv_csa_sparse_attn_rope(kv, win, win_len, idx, B, topk, q_bf16, H, sm_scale, out_bf16, lse,
+                                  nullptr, ws, ws_bytes, stream);
+}
+
+ckv_status ckv_hca_attn_rope(const ckv_plane* kv, const int32_t* n_comp, int32_t n_comp_max,
+                             const ckv_plane* win, const int32_t* win_len, int32_t B,
+                             const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
+                             float* lse, const ckv_rope* rope, void* ws, size_t ws_bytes,
+                             void* stream) {
   NvtxRange nvtx_range("ckv_hca_attn");
   ckv_status s = check_attn_common(kv, win, win_len, B, q_bf16, H, out_bf16, sm_scale);
   if (s) return s;
@@ -440,6 +472,8 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
   if (s) return s;
   AttnArgs a = attn_args(kv, win, win_len, q_bf16, H, sm_scale, out_bf16, lse,
                          static_cast<DevStatus*>(ws));
+  s = set_rope(a, rope);
+  if (s) return s;
   attn_set_ws_single(a, static_cast<uint8_t*>(ws) + kStatusBytes, B);
   a.n_comp = n_comp;
   a.n_comp_max = n_comp_max;
@@ -447,6 +481,14 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
   a.G = pc.G;
   a.cluster_all = pc.cluster_all;
   return cuda_status(launch_attention(a, B, static_cast<cudaStream_t>(stream)));
+}
+
+ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_comp_max,
+                        const ckv_plane* win, const int32_t* win_len, int32_t B,
+                        const void* q_bf16, int32_t H, float sm_scale, void* out_bf16,
+                        float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return ckv_hca_attn_rope(kv, n_comp, n_comp_max, win, win_len, B, q_bf16, H, sm_scale, out_bf16,
+                           lse, nullptr, ws, ws_bytes, stream);
 }
 
 ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
@@ -484,6 +526,7 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   }
   (void)any_reindex;
   if (topk > kMaxTopk) return CKV_ERR_UNSUPPORTED;
+  if (g->rope.pos && !g->rope.inv_freq) return CKV_ERR_INVALID;
   if (n_append > 0) {
     if (!append_dst || !append_src_bf16 || !append_slot || !aligned16(append_src_bf16))
       return CKV_ERR_INVALID;
@@ -558,6 +601,7 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
     for (int l = l0; l < l0 + n_g; ++l) {
       const int k = g->kv_src[l];
       la[l] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
+      set_rope(la[l], &g->rope);   // checked before any launch
       la[l].idx = layer_idx[l];
       la[l].topk = topk;
       la[l].G = pc.G;

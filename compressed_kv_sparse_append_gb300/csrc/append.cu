@@ -2,7 +2,8 @@
 //
 // "DeepSeek-V4 KV Cache 深度分析", §二 (code evidence): the first 448 dims of
 // the 512-d latent are quantised to FP8 and the last 64 (RoPE) dims stay
-// BF16.  "V4.1-Flash 공개", 핵심 내용, and "KV cache 890 bajtów na token",
+// BF16; §四: indexer keys may be Hadamard-rotated before their FP4
+// quantisation (CKV_FMT_FP4H, hadamard.cuh).  "V4.1-Flash 공개", 핵심 내용, and "KV cache 890 bajtów na token",
 // "Trzy mechanizmy": FP4 E2M1 values with one E4M3 scale per 16 channels,
 // no global scale.
 //
@@ -15,6 +16,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "hadamard.cuh"
 
 namespace ckv {
 
@@ -122,22 +124,14 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, int row, int lan
     const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
     if (a.fmt == CKV_FMT_BF16) {
       *reinterpret_cast<uint2*>(a.data + slot * 256 + lane * 8) = raw;
-    } else {  // CKV_FMT_FP4
+    } else {  // CKV_FMT_FP4 / CKV_FMT_FP4H (the latter rotated first)
       float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
                     __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
-      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const uint8_t sc = e4m3_code(__fdiv_rn(amax, 6.0f));
-      const float s = e4m3_value(sc);
-      uint32_t c = 0;
-      if (s > 0.f) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c |= e2m1_code(__fdiv_rn(v[i], s)) << (4 * i);
-      }
+      if (a.fmt == CKV_FMT_FP4H) hadamard128_warp(v, lane);
+      uint8_t sc;
+      const uint32_t c = fp4_quant_lane4(v, sc);
       *reinterpret_cast<uint16_t*>(a.data + slot * 64 + lane * 2) = (uint16_t)c;
-      if ((lane & 3) == 0)
-        reinterpret_cast<uint8_t*>(a.scale)[slot * 8 + (lane >> 2)] = s > 0.f ? sc : (uint8_t)0;
+      if ((lane & 3) == 0) reinterpret_cast<uint8_t*>(a.scale)[slot * 8 + (lane >> 2)] = sc;
     }
   }
 }

@@ -66,7 +66,8 @@ static_assert(kRawOffFp4 + 64 * 128 <= kScaleOffFp4 && kScaleOffFp4 + 16 * 128 <
 constexpr uint32_t kOffBar = kOffVmask + kStages * 8;
 constexpr uint32_t kNumBars = 5 * kStages + 12;
 constexpr uint32_t kOffSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemUsed = kOffSlot + 16;
+constexpr uint32_t kOffRope = kOffSlot + 16;                 // float2 [32]: (cos, sin) of rope pair k
+constexpr uint32_t kSmemUsed = kOffRope + 32 * 8;
 constexpr uint32_t kSmemAttn = kSmemUsed + 1024;
 static_assert(kSmemAttn <= 232448, "fits the 227 KB opt-in limit");
 
@@ -141,9 +142,14 @@ constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pai
 // Combines the G partials of one half over units [u0, u1) of 8 columns x 128
 // head rows with the weights in `wsm`; each pass keeps 16 / GMAX items x G
 // loads of 16 bytes in flight per thread.
+//
+// rtab (null: none): (cos, sin) of the 32 rope pairs; the units holding the
+// last 64 latent dims (units 24..31 of half 1) are turned by the opposite
+// angle before they are stored (the output's RoPE at position -i).
 template <int GMAX>
 __device__ __forceinline__ void merge_items(const uint4* pq0, const float* wsm, int G, int H,
-                                            __nv_bfloat16* out, int tid, int u0, int u1) {
+                                            __nv_bfloat16* out, int tid, int u0, int u1,
+                                            const float2* rtab) {
   constexpr int kItems = 16 / GMAX;
   const int n_items = (u1 - u0) * H;   // only the H real head rows
 #pragma unroll 1
@@ -173,6 +179,15 @@ __device__ __forceinline__ void merge_items(const uint4* pq0, const float* wsm, 
             acc[2 * e] += wq * f.x;
             acc[2 * e + 1] += wq * f.y;
           }
+        }
+      }
+      if (rtab && uu >= 24) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 cs = rtab[4 * (uu - 24) + e];
+          const float re = acc[2 * e], im = acc[2 * e + 1];
+          acc[2 * e] = re * cs.x + im * cs.y;
+          acc[2 * e + 1] = im * cs.x - re * cs.y;
         }
       }
       uint4 o;
@@ -464,6 +479,23 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   };
 
   if (warp >= 6) {
+    // RoPE table of this sequence ("DeepSeek-V4 KV Cache 深度分析", §五: the
+    // query's and the output's last 64 dims, i.e. half 1): pair k turns by
+    // i * theta_k, reduced modulo 2 pi in double precision first.
+    const bool rope = half == 1 && a.rope_pos != nullptr && (a.rope_q || a.rope_out);
+    float2* rtab = reinterpret_cast<float2*>(gbase + kOffRope);
+    if (rope) {
+      if (warp == 6) {
+        const double ang = (double)a.rope_pos[b] * (double)a.rope_freq[lane];
+        const double red = fma(-6.283185307179586, rint(ang * 0.15915494309189535), ang);
+        // |red| <= pi: the hardware approximation's absolute error there is
+        // about 2^-21, far below the bf16 rounding that follows
+        float sv, cv;
+        __sincosf((float)red, &sv, &cv);
+        rtab[lane] = make_float2(cv, sv);
+      }
+      asm volatile("bar.sync 4, 128;" ::: "memory");
+    }
     // Q[b, h, half] -> TMEM as the bf16 A operand (lane h, two elements per column)
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -479,6 +511,15 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
           r[4 * k + 1] = v.y;
           r[4 * k + 2] = v.z;
           r[4 * k + 3] = v.w;
+        }
+        if (rope && a.rope_q && c == 3) {
+          // dims 448 + 2k, 449 + 2k (one bf16 pair per word) turn by +i theta_k
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 cs = rtab[k];
+            const float re = __uint_as_float(r[k] << 16), im = __uint_as_float(r[k] & 0xFFFF0000u);
+            r[k] = pack_bf16(re * cs.x - im * cs.y, re * cs.y + im * cs.x);
+          }
         }
       } else {
 #pragma unroll
@@ -1011,9 +1052,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     __syncthreads();
     __nv_bfloat16* out = a.out + (int64_t)b * a.H * 512 + half * 256;
     const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
-    if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1);
-    else if (G <= 4) merge_items<4>(pq0, wsm, G, a.H, out, tid, u0, u1);
-    else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1);
+    const float2* rtab = (half == 1 && a.rope_pos && a.rope_out)
+                             ? reinterpret_cast<const float2*>(gbase + kOffRope) : nullptr;
+    if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
+    else if (G <= 4) merge_items<4>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
+    else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
   }
   // the last CTA of the sequence to leave resets the counters for the next call
   __syncthreads();

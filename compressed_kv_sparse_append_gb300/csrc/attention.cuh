@@ -38,6 +38,9 @@ struct AttnArgs {
   int use_tma;            // set by the launcher: contiguous BF16 rows via TMA
   int progress;           // debugging: count pipeline events in the status block
   int tag;                // set by the launcher: kArgsTag ^ layer (checked on entry)
+  const int32_t* rope_pos;  // RoPE at the attention's ends: [B] query position i, or null
+  const float* rope_freq;   // [32] angle per position of rope pair k
+  int rope_q, rope_out;     // turn the query by +i / the output by -i
   DevStatus* st;
   CUtensorMap gmap[4];    // set by the launcher: row-gather maps (main, window)
 };

@@ -24,6 +24,7 @@
 #include <cstddef>
 
 #include "topk_merge.cuh"
+#include "hadamard.cuh"
 
 namespace ckv {
 
@@ -44,6 +45,24 @@ static_assert(offsetof(IndexSmem, hist) == offsetof(IndexSmem, keys) + kMaxChunk
 // quantised with the E2M1 + E4M3/16 block quantiser (the same arithmetic as
 // the append path) and its exact values stored; BF16 keys -> the BF16 values.
 __device__ void load_query(const IndexArgs& a, int b, float* q, float* w) {
+  if (a.fmt == CKV_FMT_FP4H) {
+    // Hadamard-rotated keys: each warp rotates and quantises whole heads
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int h = threadIdx.x >> 5; h < a.HI; h += kIdxThreads / 32) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + lane * 4);
+      float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                    __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      hadamard128_warp(v, lane);
+      uint8_t sc;
+      const uint32_t c = fp4_quant_lane4(v, sc);
+      const float s = e4m3_value(sc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[h * kIdxDim + lane * 4 + i] = e2m1_value((c >> (4 * i)) & 0xFu) * s;
+    }
+    for (int t = threadIdx.x; t < a.HI; t += kIdxThreads) w[t] = a.w[(int64_t)b * a.HI + t];
+    return;
+  }
   for (int t = threadIdx.x; t < a.HI * 8; t += kIdxThreads) {
     const int h = t >> 3, blk = t & 7;
     const __nv_bfloat16* src = a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16;
@@ -81,7 +100,7 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
 #pragma unroll
   for (int h = 0; h < HMAX; ++h) acc[h] = 0.f;
   const int64_t row = (int64_t)b * a.cap + entry;
-  const bool fp4 = a.fmt == CKV_FMT_FP4;
+  const bool fp4 = a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H;
   auto fetch = [&](int blk, uint4& x0, uint4& x1, uint32_t& sc) {
     if (fp4) {
       const uint2 d = *reinterpret_cast<const uint2*>(a.kdata + row * 64 + blk * 8);

@@ -29,6 +29,7 @@
 
 #include "tmap.cuh"
 #include "topk_merge.cuh"
+#include "hadamard.cuh"
 
 namespace ckv {
 
@@ -155,16 +156,38 @@ __global__ void __launch_bounds__(kUThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---- warps 1-9: FP4 query (B operand) + its scales, head weights, an
+    // ---- warps 1-13: FP4 query (B operand) + its scales, head weights, an
     // empty histogram
     const int t9 = tid - 32;
+    if (a.fmt == CKV_FMT_FP4H) {
+      // Hadamard-rotated keys: each warp rotates and quantises whole heads
+      // (4 channels per lane); lane l's two code bytes are bytes 2l, 2l + 1
+      // of row h of the SW64 tile, its block l / 4's scale goes to the scale
+      // table
+#pragma unroll 1
+      for (int h = warp - 1; h < 64; h += kUThreads / 32 - 1) {
+        uint32_t c = 0;
+        uint8_t sc = 0;
+        if (h < a.HI) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + lane * 4);
+          float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+          hadamard128_warp(v, lane);
+          c = fp4_quant_lane4(v, sc);
+        }
+        *reinterpret_cast<uint16_t*>(g + kOffQ + sw64(h, lane >> 3) + ((2 * lane) & 15)) = (uint16_t)c;
+        if ((lane & 3) == 0) g[kOffQs + h * 8 + (lane >> 2)] = sc;
+      }
+    }
+
     constexpr int kQItems = (64 * 8 + kUThreads - 33) / (kUThreads - 32);   // 16-channel blocks per thread
+    const bool plain_q = a.fmt != CKV_FMT_FP4H;
     uint4 qraw[kQItems][2];
 #pragma unroll
     for (int k = 0; k < kQItems; ++k) {
       const int j = t9 + k * (kUThreads - 32), h = j >> 3, blk = j & 7;
       qraw[k][0] = qraw[k][1] = make_uint4(0u, 0u, 0u, 0u);
-      if (j < 64 * 8 && h < a.HI) {
+      if (plain_q && j < 64 * 8 && h < a.HI) {
         const uint4* s4 = reinterpret_cast<const uint4*>(a.q_idx + ((int64_t)b * a.HI + h) * kIdxDim + blk * 16);
         qraw[k][0] = s4[0];
         qraw[k][1] = s4[1];
@@ -174,7 +197,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
 #pragma unroll
     for (int k = 0; k < kQItems; ++k) {
       const int j = t9 + k * (kUThreads - 32), h = j >> 3, blk = j & 7;
-      if (j >= 64 * 8) break;
+      if (j >= 64 * 8 || !plain_q) break;
       uint32_t lo = 0, hi = 0;
       uint8_t sc = 0;
       if (h < a.HI) {
@@ -342,7 +365,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
 bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
   // FP4 keys, no pool, 64 heads max, scale rows pair up (even cap), the
   // 2-D maps' row counts fit in int32.
-  return a.fmt == CKV_FMT_FP4 && a.pool == nullptr && a.HI <= 64 && (a.cap % 2) == 0 &&
+  return (a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H) && a.pool == nullptr && a.HI <= 64 &&
+         (a.cap % 2) == 0 &&
          batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && tmap_encode_fn() != nullptr;
 }
 

@@ -80,10 +80,20 @@ typedef int32_t ckv_status;
  *                  value = decode(code) * scale.
  *  CKV_FMT_FP4   : entry = dim/2 bytes of packed E2M1 codes, channel 2t in the
  *                  low nibble of byte t, channel 2t+1 in the high nibble; one
- *                  E4M3 scale byte per 16 channels in `scale` ([V41]).  */
+ *                  E4M3 scale byte per 16 channels in `scale` ([V41]).
+ *  CKV_FMT_FP4H  : indexer keys only (dim 128).  The FP4 layout above, of the
+ *                  Hadamard-rotated vector ([KVC] §四: Hadamard rotation, then
+ *                  FP4 over all 128 dims): x H with H the Sylvester Hadamard
+ *                  matrix of order 128 over sqrt(128), computed as f32
+ *                  butterflies (stage h = 1, 2, ..., 64: pair (j, j + h) ->
+ *                  (a + b, a - b)) and one f32 multiplication by
+ *                  fl32(1/sqrt(128)).  Scoring against such keys rotates the
+ *                  query the same way before quantising it; an orthogonal
+ *                  rotation of both sides leaves q . k unchanged. */
 #define CKV_FMT_BF16  0
 #define CKV_FMT_MIXED 1
 #define CKV_FMT_FP4   2
+#define CKV_FMT_FP4H  3
 
 /* One cache plane (main KV, window ring, or indexer keys) of `batch`
  * sequences with `cap` entry slots each.  Entry (b, pos) lives at
@@ -98,7 +108,7 @@ typedef struct ckv_plane {
   int64_t cap;        /* entry slots per sequence                            */
   void   *data;       /* [batch][cap][entry_bytes]                           */
   void   *scale;      /* MIXED: f32 [batch][cap][448/nope_block];
-                         FP4:   u8  [batch][cap][dim/16] (E4M3 codes);
+                         FP4 / FP4H: u8 [batch][cap][dim/16] (E4M3 codes);
                          BF16:  NULL                                         */
 } ckv_plane;
 
@@ -133,6 +143,7 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI,
  *          fl32(x_i / s)); rope dims copied as bf16.
  *   FP4:   s = E4M3_rn_satfinite(fl32(amax16 / 6)), code_i =
  *          E2M1_rn_satfinite(fl32(x_i / decode(s))).
+ *   FP4H:  the same on the Hadamard-rotated row (dim 128; see CKV_FMT_FP4H).
  *   Codes carry the sign of x (tiny negatives give the negative-zero code);
  *   a block whose scale is zero stores all-zero codes. */
 ckv_status ckv_kv_append_quant(const ckv_plane *dst, const void *src_bf16,
@@ -160,7 +171,7 @@ ckv_status ckv_kv_append_quant_multi(const ckv_plane *dst, const void *const *sr
  * s_j = sum_h w_h * ReLU(q_h . k_j) on the dequantised values; for FP4 keys
  * the query is first quantised with the same E2M1 + E4M3/16 block
  * quantiser, "computed entirely in FP4").
- *   idx_keys   [host] indexer-key plane, dim 128, CKV_FMT_FP4 or _BF16.
+ *   idx_keys   [host] indexer-key plane, dim 128, CKV_FMT_FP4, _FP4H or _BF16.
  *   n_comp     [B] int32: valid entries of each sequence (<= n_comp_max).
  *   n_comp_max [host] upper bound of n_comp (sizes the grid).
  *   q_idx_bf16 [B][HI][128] bf16 indexer queries; w [B][HI] f32 weights.
@@ -238,6 +249,38 @@ ckv_status ckv_csa_sparse_attn(const ckv_plane *kv, const ckv_plane *win,
                                int32_t H, float sm_scale, void *out_bf16,
                                float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* RoPE at the two ends of the attention ([KVC] §五, three RoPE sites: the
+ * query, each compressed entry, and the core attention output at position
+ * -i).  Entries reach the cache already rotated; these two sites are part of
+ * the attention step.  The last 64 latent dims form 32 pairs of adjacent dims
+ * (448 + 2k, 449 + 2k), each a complex number (real part first); pair k
+ * turns by the angle pos * inv_freq[k].
+ *   pos        [B] int32: position i of each sequence's query token.
+ *   inv_freq   [32] f32: angle per position of pair k (the model's frequency
+ *              table, e.g. 10000^(-2k/64), scaled or not).
+ *   rotate_q   nonzero: the query's last 64 dims turn by +i before the
+ *              products (the rotated query is rounded to bf16).
+ *   rotate_out nonzero: the output's last 64 dims turn by -i before the
+ *              output is rounded to bf16 (the lse does not change).
+ * The angle is reduced modulo 2 pi in double precision, then its sine and
+ * cosine are taken in f32 (absolute error about 2^-21).  The struct itself
+ * is [host]. */
+typedef struct ckv_rope {
+  const int32_t *pos;
+  const float   *inv_freq;
+  int32_t        rotate_q;
+  int32_t        rotate_out;
+} ckv_rope;
+
+/* ckv_csa_sparse_attn with RoPE at the query and / or the output (rope
+ * [host], NULL = none; see ckv_rope). */
+ckv_status ckv_csa_sparse_attn_rope(const ckv_plane *kv, const ckv_plane *win,
+                                    const int32_t *win_len, const int32_t *idx,
+                                    int32_t B, int32_t topk, const void *q_bf16,
+                                    int32_t H, float sm_scale, void *out_bf16,
+                                    float *lse, const ckv_rope *rope, void *ws,
+                                    size_t ws_bytes, void *stream);
+
 /* HCA dense attention ([KVC] §三: ratio-128 entries, no sparse selection,
  * dense attention over all entries plus the 128-token window).  Same
  * formula as ckv_csa_sparse_attn over entries [0, n_comp[b]) and the window.
@@ -247,6 +290,15 @@ ckv_status ckv_hca_attn(const ckv_plane *kv, const int32_t *n_comp,
                         const int32_t *win_len, int32_t B, const void *q_bf16,
                         int32_t H, float sm_scale, void *out_bf16, float *lse,
                         void *ws, size_t ws_bytes, void *stream);
+
+/* ckv_hca_attn with RoPE at the query and / or the output (rope [host],
+ * NULL = none; see ckv_rope). */
+ckv_status ckv_hca_attn_rope(const ckv_plane *kv, const int32_t *n_comp,
+                             int32_t n_comp_max, const ckv_plane *win,
+                             const int32_t *win_len, int32_t B, const void *q_bf16,
+                             int32_t H, float sm_scale, void *out_bf16, float *lse,
+                             const ckv_rope *rope, void *ws, size_t ws_bytes,
+                             void *stream);
 
 /* CSA2 group decode ([V41] 핵심 내용; [890] "Trzy mechanizmy").  Layer roles:
  *   FULL    scores every entry of `idx_keys` with its own q_idx / w, keeps
@@ -282,6 +334,8 @@ typedef struct ckv_csa2_group {
   float   *lse[CKV_CSA2_MAX_LAYERS];      /* NULL or [B][H] f32                 */
   int32_t *idx_out[CKV_CSA2_MAX_LAYERS];  /* NULL or [B][topk] int32: indices used */
   int32_t  pool_len;                      /* candidate pool of the FULL layer  */
+  ckv_rope rope;                          /* RoPE of every layer's query / output
+                                             (pos == NULL: none; see ckv_rope) */
 } ckv_csa2_group;
 
 ckv_status ckv_csa2_group_decode(const ckv_csa2_group *g, const int32_t *n_comp,
