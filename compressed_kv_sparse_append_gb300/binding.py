@@ -27,7 +27,8 @@ _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ct
 
 class CPlane(ctypes.Structure):
     _fields_ = [("fmt", _i32), ("dim", _i32), ("nope_block", _i32), ("batch", _i32),
-                ("cap", _i64), ("data", _vp), ("scale", _vp)]
+                ("cap", _i64), ("data", _vp), ("scale", _vp), ("block_table", _vp),
+                ("page_size", _i32), ("n_pages", _i32)]
 
 
 class CRope(ctypes.Structure):
@@ -133,24 +134,37 @@ def scale_shape(fmt: str, dim: int, nope_block: int = 448):
 
 class Plane:
     """A cache plane of ``batch`` sequences x ``cap`` entry slots in device
-    memory (data [batch, cap, entry_bytes] uint8, scale per format).
+    memory.  Dense: data [batch, cap, entry_bytes] uint8, scale per format.
+    Paged (``block_table`` [batch, cap // page_size] int32 on the device):
+    data [n_pages * page_size, entry_bytes], scale likewise; entry (b, pos) is
+    row block_table[b, pos // page_size] * page_size + pos % page_size.
 
     The C descriptor is built once and rebuilt whenever a field is
     reassigned; replace ``data`` / ``scale`` by assignment, not by resizing
     the tensors in place (that would move their storage behind the cached
     pointers)."""
 
-    def __init__(self, fmt, dim, batch, cap, device="cuda", nope_block=448, data=None, scale=None):
+    def __init__(self, fmt, dim, batch, cap, device="cuda", nope_block=448, data=None, scale=None,
+                 block_table=None, page_size=0, n_pages=0):
         self._c = None
         self.fmt, self.dim, self.batch, self.cap, self.nope_block = fmt, dim, batch, cap, nope_block
+        self.block_table, self.page_size, self.n_pages = block_table, page_size, n_pages
         eb = entry_bytes(fmt, dim)
-        self.data = data if data is not None else torch.zeros((batch, cap, eb), dtype=torch.uint8,
+        lead = (n_pages * page_size,) if block_table is not None else (batch, cap)
+        self.data = data if data is not None else torch.zeros(lead + (eb,), dtype=torch.uint8,
                                                               device=device)
         shp, dt = scale_shape(fmt, dim, nope_block)
         if scale is not None or shp is None:
             self.scale = scale
         else:
-            self.scale = torch.zeros((batch, cap) + shp, dtype=dt, device=device)
+            self.scale = torch.zeros(lead + shp, dtype=dt, device=device)
+
+    def slot(self, b, pos):
+        """Row of entry (b, pos) (int64 tensor for tensor pos): the append's slot."""
+        if self.block_table is None:
+            return pos + b * self.cap
+        pg = self.block_table[b][pos // self.page_size].to(torch.int64)
+        return pg * self.page_size + pos % self.page_size
 
     def __setattr__(self, name, value):
         # any change of the plane's fields drops the cached C descriptor
@@ -161,8 +175,11 @@ class Plane:
     def c(self) -> CPlane:
         """The C descriptor (built once, rebuilt after a field is reassigned)."""
         if self._c is None:
+            paged = self.block_table is not None
             self._c = CPlane(FMT[self.fmt], self.dim, self.nope_block, self.batch, self.cap,
-                             self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr())
+                             self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr(),
+                             self.block_table.data_ptr() if paged else None,
+                             self.page_size if paged else 0, self.n_pages if paged else 0)
         return self._c
 
 

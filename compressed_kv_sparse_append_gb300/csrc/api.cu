@@ -69,6 +69,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 ckv_status check_plane(const ckv_plane* p, int dim, int B) {
   if (!p || !p->data || !aligned16(p->data)) return CKV_ERR_INVALID;
   if (p->dim != dim || p->cap <= 0 || p->batch < B) return CKV_ERR_INVALID;
+  if (p->block_table) {
+    // paged: whole pages of a multiple of 128 rows, a cap of whole pages,
+    // row numbers that fit int32 (TMA coordinates)
+    if (p->page_size <= 0 || p->page_size % 128 != 0 || p->n_pages <= 0) return CKV_ERR_INVALID;
+    if (p->cap % p->page_size != 0) return CKV_ERR_INVALID;
+    if ((int64_t)p->n_pages * p->page_size >= ((int64_t)1 << 31)) return CKV_ERR_UNSUPPORTED;
+  }
   if (p->fmt == CKV_FMT_BF16) return CKV_OK;
   if (p->fmt == CKV_FMT_FP4) {
     if (!p->scale || (dim != 512 && dim != 128)) return CKV_ERR_INVALID;
@@ -178,6 +185,10 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.kdata = static_cast<const uint8_t*>(keys->data);
   a.kscale = static_cast<const uint8_t*>(keys->scale);
   a.cap = keys->cap;
+  a.bt = keys->block_table;
+  a.page = keys->block_table ? keys->page_size : 0;
+  a.bt_cols = keys->block_table ? (int)(keys->cap / keys->page_size) : 0;
+  a.rows = plane_rows(*keys);
   a.fmt = keys->fmt;
   a.n_comp = n_comp;
   a.B = B;
@@ -201,7 +212,7 @@ ckv_status run_index(const ckv_plane* keys, const int32_t* n_comp, int B, int n_
   a.dbg = dbg;
   a.st = st;
   a.trace = debug_progress() == 2 ? 1 : 0;
-  const int64_t rows = (int64_t)keys->batch * keys->cap;
+  const int64_t rows = plane_rows(*keys);
   if (use_umma_indexer() && index_umma_supported(a, rows))
     return cuda_status(launch_index_umma(a, rows, stream));
   return cuda_status(launch_index_simt(a, stream));
@@ -291,6 +302,7 @@ ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const in
   if (s) return s;
   if (win->fmt != kv->fmt || (kv->fmt == CKV_FMT_MIXED && win->nope_block != kv->nope_block))
     return CKV_ERR_INVALID;
+  if (win->block_table) return CKV_ERR_UNSUPPORTED;   // window rings are dense
   return CKV_OK;
 }
 
@@ -300,6 +312,10 @@ AttnArgs attn_args(const ckv_plane* kv, const ckv_plane* win, const int32_t* win
   a.kv_data = static_cast<const uint8_t*>(kv->data);
   a.kv_scale = kv->scale;
   a.kv_cap = kv->cap;
+  a.kv_rows = plane_rows(*kv);
+  a.kv_bt = kv->block_table;
+  a.kv_page = kv->block_table ? kv->page_size : 0;
+  a.kv_bt_cols = kv->block_table ? (int)(kv->cap / kv->page_size) : 0;
   a.win_data = static_cast<const uint8_t*>(win->data);
   a.win_scale = win->scale;
   a.win_cap = win->cap;

@@ -157,7 +157,7 @@ cudaError_t launch_append_multi(const ckv_plane* p, const void* const* src, cons
     a.scale = p[k].scale;
     a.src = static_cast<const __nv_bfloat16*>(src[k]);
     a.slot = slot[k];
-    a.n_slots = (int64_t)p[k].batch * p[k].cap;
+    a.n_slots = plane_rows(p[k]);
     a.n = n[k];
     a.fmt = p[k].fmt;
     a.dim = p[k].dim;

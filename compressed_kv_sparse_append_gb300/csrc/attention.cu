@@ -540,21 +540,37 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA issuer ----
-    if (use_tma && lane == 0) {
+    // Contiguous BF16 rows by TMA, lane 0 issuing.  With a paged main KV
+    // the whole warp fetches the pages of the next 32 tiles (a 64-row tile
+    // lies in one page).
+    if (use_tma) {
+      int pg_reg = 0;
+#pragma unroll 1
       for (int i = 0; i < n_my; ++i) {
         const int s = i % kStages;
-        if (i >= kStages &&
-            !mbar_wait(&bars[B_EEMPTY + s], ((i / kStages) + 1) & 1, a.st, abort_p, 21))
-          break;
+        bool ok = true;
+        if (lane == 0 && i >= kStages)
+          ok = mbar_wait(&bars[B_EEMPTY + s], ((i / kStages) + 1) & 1, a.st, abort_p, 21);
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
         const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-        const CUtensorMap* map = tl.win ? &map_win : &map_kv;
-        const int64_t row = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap) + tl.start;
-        progress(a.st, prog, 9);
-        mbar_expect_tx(&bars[B_TMA + s], kEBytes);
+        int64_t row = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap) + tl.start;
+        if (a.kv_bt) {
+          if ((i & 31) == 0) {
+            const Tile tq = tile_of(t0 + min(i + lane, n_my - 1), nt_main, n_sel, n_win);
+            pg_reg = tq.win ? 0 : __ldg(a.kv_bt + (int64_t)b * a.kv_bt_cols + tq.start / a.kv_page);
+          }
+          const int pg = __shfl_sync(0xffffffffu, pg_reg, i & 31);
+          if (!tl.win) row = (int64_t)pg * a.kv_page + tl.start % a.kv_page;
+        }
+        if (lane == 0) {
+          const CUtensorMap* map = tl.win ? &map_win : &map_kv;
+          progress(a.st, prog, 9);
+          mbar_expect_tx(&bars[B_TMA + s], kEBytes);
 #pragma unroll
-        for (int kc = 0; kc < 4; ++kc)
-          tma_load_2d(base + kOffE + s * kEBytes + kc * 8192, map, half * 256 + kc * 64, (int)row,
-                      &bars[B_TMA + s]);
+          for (int kc = 0; kc < 4; ++kc)
+            tma_load_2d(base + kOffE + s * kEBytes + kc * 8192, map, half * 256 + kc * 64, (int)row,
+                        &bars[B_TMA + s]);
+        }
       }
     }
     __syncwarp();
@@ -615,15 +631,25 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       if (tl.win) return tl.start + r;
       return idx_b ? __ldg(idx_b + tl.start + r) : tl.start + r;
     };
-    // plane row (within sequence b) of row r of tile i from its raw index,
-    // -1 for none, published with the tile's validity mask (warp-uniform i)
+    // row of the plane (dense or through the block table) feeding row r of
+    // tile i from its raw index, -1 for none, published with the tile's
+    // validity mask (warp-uniform i)
     auto publish = [&](int i, int r, int32_t x) {
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
       if (!tl.win && x >= a.kv_cap) {
         if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
         x = -1;
       }
-      const int32_t e = x >= 0 ? x : -1;
+      int32_t e = -1;
+      if (x >= 0) {
+        const int64_t row = tl.win ? (int64_t)b * a.win_cap + x
+                                   : plane_row(a.kv_bt, a.kv_page, a.kv_bt_cols, a.kv_cap, b, x);
+        if (!tl.win && (row < 0 || row >= a.kv_rows)) {   // a page id beyond the plane
+          if (half == 0) report(a.st, CKV_ERR_DEVICE_BOUNDS, x);
+        } else {
+          e = (int32_t)row;
+        }
+      }
       rsrc[(i % kStages) * 64 + r] = e;
       const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
       if ((r & 31) == 0) vmask_s[(i % kStages) * 2 + (r >> 5)] = bal;
@@ -636,7 +662,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
       const uint32_t tile = base + kOffE + s * kEBytes;
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-      const int64_t row0 = (int64_t)b * (tl.win ? a.win_cap : a.kv_cap);
       const CUtensorMap* gm = &a.gmap[tl.win ? 2 : 0];
       const int32_t* rs = rsrc + s * 64;
       if ((p & 31) == 0) {
@@ -651,10 +676,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
           int y[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            // an empty row reads the sequence's first row (a valid address)
+            // an empty row reads the plane's first row (a valid address)
             // and is zeroed or skipped by the producers from the mask
             const int32_t e = rs[4 * g + k];
-            y[k] = (int)(row0 + (e >= 0 ? e : 0));
+            y[k] = e >= 0 ? e : 0;
           }
           if constexpr (FMT == CKV_FMT_BF16) {
 #pragma unroll
@@ -676,7 +701,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         // row p's scale words for this half (at most 4: nope_block is 448 or 64)
         if (p < 64 && rs[p] >= 0) {
           const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
-          const int64_t ent = row0 + rs[p];
+          const int64_t ent = rs[p];
           const int nblk = 448 / a.nope_block, nb0 = (half * 256) / a.nope_block;
           const int nb1 = (half * 256 + (half == 0 ? 256 : 192) - 1) / a.nope_block;
           for (int k = 0; k <= nb1 - nb0; ++k)
@@ -1102,7 +1127,7 @@ bool encode_gather_rows(CUtensorMap* m, const void* data, CUtensorMapDataType dt
 bool encode_gather_maps(AttnArgs& a, int B) {
   const uint8_t* data[2] = {a.kv_data, a.win_data};
   const void* scale[2] = {a.kv_scale, a.win_scale};
-  const int64_t rows[2] = {(int64_t)B * a.kv_cap, (int64_t)B * a.win_cap};
+  const int64_t rows[2] = {a.kv_rows, (int64_t)B * a.win_cap};
   for (int k = 0; k < 2; ++k) {
     CUtensorMap* m = &a.gmap[2 * k];
     bool ok;
@@ -1169,7 +1194,7 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
   // Contiguous BF16 rows (HCA, one layer) stream through TMA; gathered or
   // quantised rows go through the producer warps.
   if (n == 1 && a0.fmt == CKV_FMT_BF16 && a0.idx == nullptr &&
-      encode_bf16_rows(&mk, a0.kv_data, (int64_t)B * a0.kv_cap) &&
+      encode_bf16_rows(&mk, a0.kv_data, a0.kv_rows) &&
       encode_bf16_rows(&mw, a0.win_data, (int64_t)B * a0.win_cap))
     batch.layer[0].use_tma = 1;
   // every other layer gathers its rows with TMA

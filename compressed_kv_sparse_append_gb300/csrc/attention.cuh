@@ -17,6 +17,9 @@ struct AttnArgs {
   const uint8_t* kv_data;
   const void* kv_scale;
   int64_t kv_cap;
+  int64_t kv_rows;          // rows of the main-KV arrays (dense: B * cap)
+  const int32_t* kv_bt;     // paged main KV: block table [B][kv_bt_cols], else null
+  int kv_page, kv_bt_cols;
   const uint8_t* win_data;
   const void* win_scale;
   int64_t win_cap;

@@ -34,6 +34,21 @@ inline cudaError_t once_per_device(DeviceOnce& o, F&& f) {
 }
 
 
+// Rows of a plane's data (and scale) arrays: batch * cap when dense,
+// n_pages * page_size when paged.
+inline int64_t plane_rows(const ckv_plane& p) {
+  return p.block_table ? (int64_t)p.n_pages * p.page_size : (int64_t)p.batch * p.cap;
+}
+
+// Row of entry `pos` of sequence b in a plane (dense: b * cap + pos; paged:
+// through the block table, bt_cols = cap / page_size entries per sequence).
+__device__ __forceinline__ int64_t plane_row(const int32_t* bt, int page, int bt_cols, int64_t cap,
+                                             int b, int64_t pos) {
+  if (!bt) return (int64_t)b * cap + pos;
+  const int pg = __ldg(bt + (int64_t)b * bt_cols + (int)(pos / page));
+  return (int64_t)pg * page + pos % page;
+}
+
 // ------------------------------------------------------------ status ----
 // The first 256 bytes of every workspace: [0] sticky error code (the most
 // recent nonzero one), [1] count of events, [2] detail (index, stage...).

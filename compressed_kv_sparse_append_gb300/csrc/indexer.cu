@@ -99,7 +99,11 @@ __device__ __forceinline__ float score_simt(const IndexArgs& a, int b, int64_t e
   float acc[HMAX];
 #pragma unroll
   for (int h = 0; h < HMAX; ++h) acc[h] = 0.f;
-  const int64_t row = (int64_t)b * a.cap + entry;
+  int64_t row = plane_row(a.bt, a.page, a.bt_cols, a.cap, b, entry);
+  if (row < 0 || row >= a.rows) {   // a page id beyond the plane: scored as row 0, recorded
+    report(a.st, CKV_ERR_DEVICE_BOUNDS, (int)entry);
+    row = 0;
+  }
   const bool fp4 = a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H;
   auto fetch = [&](int blk, uint4& x0, uint4& x1, uint32_t& sc) {
     if (fp4) {

@@ -21,7 +21,10 @@ struct IndexArgs {
   const uint8_t* kdata;           // indexer-key plane data
   const uint8_t* kscale;          // FP4: E4M3 scale bytes
   int64_t cap;
-  int fmt;                        // CKV_FMT_FP4 or CKV_FMT_BF16
+  const int32_t* bt;              // paged key plane: block table [B][bt_cols], else null
+  int page, bt_cols;
+  int64_t rows;                   // rows of the key arrays
+  int fmt;                        // CKV_FMT_FP4, _FP4H or _BF16
   const int32_t* n_comp;
   int B, n_comp_max;
   const __nv_bfloat16* q_idx;

@@ -141,14 +141,28 @@ __global__ void __launch_bounds__(kUThreads, 1)
     // ------------------------------------------------------------ TMA ----
     // The key stream does not depend on the query: it starts at once, while
     // the other warps prepare the query.
-    if (lane == 0) {
-      for (int t = 0; t < T; ++t) {
-        const int s = t % kUStages;
-        if (t >= kUStages &&
-            !mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11))
-          break;
+    // A paged plane: the whole warp fetches the pages of the next 32 tiles
+    // (a 128-key tile lies in one page), lane 0 issues.
+    int pg_reg = 0;
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      const int s = t % kUStages;
+      bool ok = true;
+      if (lane == 0 && t >= kUStages)
+        ok = mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11);
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
+      int64_t row = row0 + (int64_t)t * kUTile;
+      if (a.bt) {
+        if ((t & 31) == 0) {
+          const int64_t p0 = c0 + (int64_t)(t + lane) * kUTile;
+          pg_reg = t + lane < T ? __ldg(a.bt + (int64_t)b * a.bt_cols + (int)(p0 / a.page)) : 0;
+        }
+        const int pg = __shfl_sync(0xffffffffu, pg_reg, t & 31);
+        const int64_t pos = c0 + (int64_t)t * kUTile;
+        row = (int64_t)pg * a.page + pos % a.page;
+      }
+      if (lane == 0) {
         mbar_expect_tx(&bars[BU_FULL + s], kDataBytes + kScaleBytes);
-        const int64_t row = row0 + (int64_t)t * kUTile;
         tma_load_2d(base + kOffData + s * kDataBytes, &map_data, 0, (int)row, &bars[BU_FULL + s]);
         tma_load_2d(base + kOffScale + s * kScaleBytes, &map_scale, 0, (int)(row >> 1),
                     &bars[BU_FULL + s]);
@@ -366,7 +380,7 @@ bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
   // FP4 keys, no pool, 64 heads max, scale rows pair up (even cap), the
   // 2-D maps' row counts fit in int32.
   return (a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H) && a.pool == nullptr && a.HI <= 64 &&
-         (a.cap % 2) == 0 &&
+         (a.bt ? a.page % kUTile == 0 : (a.cap % 2) == 0) &&
          batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && tmap_encode_fn() != nullptr;
 }
 

@@ -96,20 +96,38 @@ typedef int32_t ckv_status;
 #define CKV_FMT_FP4H  3
 
 /* One cache plane (main KV, window ring, or indexer keys) of `batch`
- * sequences with `cap` entry slots each.  Entry (b, pos) lives at
- * data + (b * cap + pos) * entry_bytes; its scales at
- * scale + (b * cap + pos) * n_scales * scale_size.
- * data and scale are 16-byte aligned.  The plane struct itself is [host]. */
+ * sequences with `cap` entry slots each.  The plane struct itself is [host].
+ *
+ * Dense (block_table == NULL): entry (b, pos) is row b * cap + pos: it lives
+ * at data + row * entry_bytes, its scales at scale + row * n_scales *
+ * scale_size.
+ *
+ * Paged (block_table != NULL): the rows of the plane are n_pages pages of
+ * page_size rows each; sequence b's logical block j (positions
+ * [j * page_size, (j + 1) * page_size)) is page block_table[b * (cap /
+ * page_size) + j], so entry (b, pos) is row
+ *   block_table[b * (cap / page_size) + pos / page_size] * page_size
+ *     + pos % page_size,
+ * addressed as above.  page_size is a multiple of 128 and divides cap;
+ * every page id is in [0, n_pages).  The pages define no layout of their own
+ * (they allocate the cache dense, [batch][cap][entry]); paging lets a
+ * serving engine grow and share sequences' caches in pages.  Main-KV and
+ * indexer-key planes may be paged; window planes are dense.
+ * data and scale are 16-byte aligned. */
 typedef struct ckv_plane {
   int32_t fmt;        /* CKV_FMT_*                                           */
   int32_t dim;        /* 512 (main KV, window) or 128 (indexer keys)         */
   int32_t nope_block; /* CKV_FMT_MIXED: 448 (one scale per entry) or 64      */
   int32_t batch;      /* sequences                                           */
-  int64_t cap;        /* entry slots per sequence                            */
-  void   *data;       /* [batch][cap][entry_bytes]                           */
-  void   *scale;      /* MIXED: f32 [batch][cap][448/nope_block];
-                         FP4 / FP4H: u8 [batch][cap][dim/16] (E4M3 codes);
+  int64_t cap;        /* entry slots (logical positions) per sequence        */
+  void   *data;       /* [rows][entry_bytes]; rows = batch * cap (dense) or
+                         n_pages * page_size (paged)                         */
+  void   *scale;      /* MIXED: f32 [rows][448/nope_block];
+                         FP4 / FP4H: u8 [rows][dim/16] (E4M3 codes);
                          BF16:  NULL                                         */
+  const int32_t *block_table; /* NULL (dense) or [batch][cap / page_size]    */
+  int32_t page_size;  /* paged: rows per page (multiple of 128)              */
+  int32_t n_pages;    /* paged: pages in data / scale                        */
 } ckv_plane;
 
 /* Workspace sizing.  `op` is one of CKV_OP_*; unused arguments may be 0.
@@ -135,8 +153,10 @@ size_t ckv_workspace_bytes(int32_t op, int32_t B, int32_t H, int32_t HI,
  * here also for the 128-d indexer keys of [KVC] §四).
  *   dst      [host] destination plane (any format; dim 512 or 128).
  *   src_bf16 [n][dst->dim] bf16 rows, already normalised and rotated.
- *   slot     [n] int64: destination slot b * cap + pos.  A negative slot
- *            skips the row; a slot >= batch * cap skips it and records
+ *   slot     [n] int64: destination row of the plane: b * cap + pos for a
+ *            dense plane, page * page_size + offset for a paged one (the
+ *            caller owns the page allocation).  A negative slot skips the
+ *            row; a slot beyond the plane's rows skips it and records
  *            CKV_ERR_DEVICE_BOUNDS.
  * Quantisation (bit-exact contract):
  *   MIXED: s = fl32(amax_block / 448) (f32), code_i = E4M3_rn_satfinite(

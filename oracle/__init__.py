@@ -27,4 +27,4 @@ The pages' 890 B/token figure for V4.1-Flash cannot be derived from what they
 print, so no function computes it.
 """
 
-from . import fp_formats, sizes, indexer, attention, csa2, rope, hadamard  # noqa: F401
+from . import fp_formats, sizes, indexer, attention, csa2, rope, hadamard, paged  # noqa: F401

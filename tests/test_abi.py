@@ -205,3 +205,25 @@ def test_csa2_group_host_validation(lib):
     g.win[2] = CPlane(1, 512, 448, 2, 16, 0x2200000, 0x9200000)
     assert call(g) == -2                            # one launch format across the layers
     assert call(_group(), ws_bytes=256) == -4       # workspace too small
+
+
+def test_paged_plane_host_validation(lib):
+    """Paged planes: whole pages of a multiple of 128 rows, a cap of whole
+    pages, dense window rings; FP4H only for 128-d keys."""
+    from compressed_kv_sparse_append_gb300.binding import CPlane
+    lib.ckv_kv_append_quant.restype = ctypes.c_int32
+    fake = ctypes.c_void_p(0x10000)
+    bt = 0x50000
+    good = CPlane(2, 128, 448, 2, 512, 0x10000, 0x20000, bt, 256, 8)
+    assert lib.ckv_kv_append_quant(ctypes.byref(good), fake, fake, 0, fake, 256, None) == 0
+    for bad in (CPlane(2, 128, 448, 2, 512, 0x10000, 0x20000, bt, 100, 8),    # page not 128k
+                CPlane(2, 128, 448, 2, 500, 0x10000, 0x20000, bt, 256, 8),    # cap not whole pages
+                CPlane(2, 128, 448, 2, 512, 0x10000, 0x20000, bt, 256, 0),    # no pages
+                CPlane(3, 512, 448, 2, 512, 0x10000, 0x20000, 0, 0, 0)):      # FP4H main KV
+        assert lib.ckv_kv_append_quant(ctypes.byref(bad), fake, fake, 1, fake, 256, None) in (-1, -2)
+    kv = CPlane(0, 512, 448, 2, 512, 0x10000, 0, bt, 128, 8)
+    win = CPlane(0, 512, 448, 2, 128, 0x30000, 0, bt, 128, 2)               # a paged window
+    lib.ckv_csa_sparse_attn.restype = ctypes.c_int32
+    args = [ctypes.byref(kv), ctypes.byref(win), fake, fake, 2, 512, fake, 128, ctypes.c_float(0.04),
+            fake, None, fake, ctypes.c_size_t(1 << 30), None]
+    assert lib.ckv_csa_sparse_attn(*args) == -2

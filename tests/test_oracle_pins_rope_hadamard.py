@@ -140,3 +140,20 @@ def test_hadamard_fp4_query_and_keys_round_trip_format():
     assert np.all(np.abs(v - rot) <= half_step * (1 + 1e-6) + 1e-12)
     qv = oi.indexer_query(x[:2], True, hadamard=True)
     assert np.array_equal(qv, ff.fp4_dequantize(*ff.fp4_quantize(hd.hadamard_rotate_f32(x[:2]))))
+
+
+def test_paged_layout_round_trip():
+    """A paged plane holds the dense plane's entries: every logical entry
+    comes back from its page, with an identity table the paged array is the
+    dense one, and distinct table entries never alias."""
+    from oracle import paged
+    B, cap, ps, n_pages = 3, 512, 128, 16
+    dense = RNG.integers(0, 256, (B, cap, 7)).astype(np.uint8)
+    ident = np.arange(B * cap // ps).reshape(B, cap // ps)
+    assert np.array_equal(paged.paged_from_dense(dense, ident, ps, B * cap // ps), dense.reshape(B * cap, 7))
+    table = RNG.permutation(n_pages)[:B * cap // ps].reshape(B, cap // ps)
+    pg = paged.paged_from_dense(dense, table, ps, n_pages)
+    for b in range(B):
+        assert np.array_equal(paged.logical_rows(pg, table, ps, b, cap), dense[b])
+    rows = np.concatenate([paged.row_of(table, ps, b, np.arange(cap)) for b in range(B)])
+    assert len(set(rows.tolist())) == B * cap
