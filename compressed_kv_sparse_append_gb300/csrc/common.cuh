@@ -213,6 +213,12 @@ __device__ __forceinline__ void trace_at(DevStatus* st, bool on, int slot, long 
   if (on && st != nullptr && slot >= 0 && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
 }
 
+// Asynchronous 4-byte copy global -> shared (cp.async, cached in L1; the
+// caller waits with cp.async.wait_all / wait_group).
+__device__ __forceinline__ void cp_async4_ca(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
 // Launch attribute for programmatic stream serialisation (host side).
 inline cudaLaunchAttribute pdl_attribute() {
   cudaLaunchAttribute at;

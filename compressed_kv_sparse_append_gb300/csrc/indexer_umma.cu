@@ -13,9 +13,10 @@
 //            their scale bytes into a kUStages-deep shared-memory ring,
 //            starting as soon as the previous kernel is done (the other
 //            warps quantise the query meanwhile);
-//   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, two
-//            buffers) = keys (A, M = 128) x query (B, N = 64), K = 128 in two
-//            block-scaled steps;
+//   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, four
+//            buffers, so the MMA runs up to three tiles ahead of the
+//            epilogue) = keys (A, M = 128) x query (B, N = 64), K = 128 in
+//            two block-scaled steps;
 //   warps 6-9 move each tile's key scales into TMEM (lane = key), running
 //            ahead of the MMA by up to the ring depth;
 //   warps 2-5 epilogue: read D back (one key per thread), form
@@ -42,32 +43,36 @@ constexpr int kUStages = 14;
 constexpr int kUTile = 128;
 constexpr uint32_t kDataBytes = kUTile * 64;                 // 8 KB
 constexpr uint32_t kScaleBytes = kUTile * 8;                 // 1 KB
+// The ring, the chunk's keys and their histogram come first and are
+// contiguous: once the chunk's candidates are written they are dead and
+// serve the merge as one scratch block.
 constexpr uint32_t kOffData = 0;
 constexpr uint32_t kOffScale = kOffData + kUStages * kDataBytes;
-constexpr uint32_t kOffQ = kOffScale + kUStages * kScaleBytes;     // 64 rows x 64 B
+constexpr uint32_t kOffKeys = kOffScale + kUStages * kScaleBytes;  // u32 [kMaxChunk]
+constexpr uint32_t kOffHist = kOffKeys + kMaxChunk * 4;            // u32 [kBins]
+constexpr uint32_t kOffQ = (kOffHist + kBins * 4 + 1023) & ~1023u; // 64 rows x 64 B
 constexpr uint32_t kOffQs = kOffQ + 64 * 64;                       // 64 x 8 scale bytes
 constexpr uint32_t kOffW = kOffQs + 64 * 8;                        // 64 f32
-constexpr uint32_t kOffKeys = kOffW + 64 * 4;                      // u32 [kMaxChunk]
-constexpr uint32_t kOffHist = kOffKeys + kMaxChunk * 4;            // u32 [kBins]
-constexpr uint32_t kOffMerge = kOffHist + kBins * 4;
+constexpr uint32_t kOffMerge = kOffW + 64 * 4;
 constexpr uint32_t kOffBar = (kOffMerge + sizeof(MergeSmem<kUThreads>) + 7) & ~7u;
-constexpr int kNumBarU = 3 * kUStages + 4;
+constexpr int kDBuf = 4;          // TMEM accumulators: the MMA runs up to 3 tiles ahead
+constexpr int kNumBarU = 3 * kUStages + 2 * kDBuf;
 constexpr uint32_t kOffSlotU = kOffBar + kNumBarU * 8;
 constexpr uint32_t kSmemU = kOffSlotU + 16 + 1024;
 static_assert(kOffQ % 1024 == 0, "operand tiles 1024-aligned");
 static_assert(kSmemU <= 232448, "fits in shared memory");
-// The merge's shared-memory scratch: the pipeline ring (dead by then).
-constexpr int kMergeScratchWords = (int)(kOffQ / 4);
+// The merge's shared-memory scratch: ring, keys and histogram (dead by then).
+constexpr int kMergeScratchWords = (int)((kOffHist + kBins * 4) / 4);
 
-constexpr uint32_t kTmemU = 256;
-constexpr uint32_t kColD = 0;          // two 64-column accumulators
-constexpr uint32_t kColSFA = 128;      // 8 columns per stage
+constexpr uint32_t kTmemU = 512;
+constexpr uint32_t kColD = 0;          // kDBuf 64-column accumulators
+constexpr uint32_t kColSFA = 64 * kDBuf;   // 8 columns per stage
 constexpr uint32_t kColSFB = kColSFA + 8 * kUStages;   // 8 columns
 static_assert(kColSFB + 8 <= kTmemU, "scale columns of every stage and the query's fit");
 constexpr uint32_t kIdescNvf4 = idesc_nvf4(128, 64);
 
 enum { BU_FULL = 0, BU_EMPTY = kUStages, BU_SFA = 2 * kUStages, BU_DFULL = 3 * kUStages,
-       BU_DEMPTY = 3 * kUStages + 2 };
+       BU_DEMPTY = 3 * kUStages + kDBuf };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       mbar_init(&bars[BU_EMPTY + s], 1);
       mbar_init(&bars[BU_SFA + s], 128);
     }
-    for (int d = 0; d < 2; ++d) {
+    for (int d = 0; d < kDBuf; ++d) {
       mbar_init(&bars[BU_DFULL + d], 1);
       mbar_init(&bars[BU_DEMPTY + d], 128);
     }
@@ -273,9 +278,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
       // ------------------------------------------------------------ MMA ----
       if (lane == 0) {
         for (int t = 0; t < T; ++t) {
-          const int s = t % kUStages, d = t & 1;
+          const int s = t % kUStages, d = t % kDBuf;
           if (!mbar_wait(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
-          if (t >= 2 && !mbar_wait(&bars[BU_DEMPTY + d], ((t >> 1) + 1) & 1, a.st, abort_p, 13)) break;
+          if (t >= kDBuf && !mbar_wait(&bars[BU_DEMPTY + d], ((t / kDBuf) + 1) & 1, a.st, abort_p, 13))
+            break;
           tc_fence_after();
           if (t < 8) trace_at(a.st, tr, 32 + t, tr0);
 #pragma unroll
@@ -318,8 +324,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const uint32_t lb = (uint32_t)(qd * 32) << 16;
       uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
       for (int t = grp; t < T; t += 2) {
-        const int d = t & 1;
-        if (!mbar_wait(&bars[BU_DFULL + d], (t >> 1) & 1, a.st, abort_p, 15)) break;
+        const int d = t % kDBuf;
+        if (!mbar_wait(&bars[BU_DFULL + d], (t / kDBuf) & 1, a.st, abort_p, 15)) break;
         tc_fence_after();
         if (m == 0 && t < 8) trace_at(a.st, tr, 48 + t, tr0);
         uint32_t r[64];

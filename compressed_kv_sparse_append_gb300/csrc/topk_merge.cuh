@@ -241,11 +241,10 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   const uint32_t lo_key = tb << kBinShift;
   trace_at(a.st, tr, 20, t0);
 
-  // survivors (real keys >= lo_key) in entry order.  Rounds of kU virtual
-  // slots per lane: warp w reads 32 * kU consecutive slots of the chunks'
-  // concatenated lists (coalesced, every load of a round in flight at once),
-  // counts them per warp, meets the other warps once, writes in order.  The
-  // keys of the threshold bin are also counted by their next 8 bits.
+  // Every candidate into shared memory, in entry order (chunk c's list at
+  // offset cprefix[c]): one warp per chunk list, 4-byte asynchronous copies,
+  // all of them in flight at once.  Then the keys of the threshold bin are
+  // counted by their next 8 bits.
   const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
   const int surv_cap = (scratch_words - pool_words) / 2;
   uint32_t* surv_key = scratch;
@@ -267,76 +266,35 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     sm.bcast[0] = 0u;   // sub-bin search defaults
     sm.bcast[1] = 0u;
   }
+  const bool staged = n_cand <= surv_cap;
+  if (staged) {
+#pragma unroll 1
+    for (int c = warp; c < nch; c += kWarps) {
+      const int cnt = (int)(sm.cprefix[c + 1] - sm.cprefix[c]);
+      const uint32_t* gk = cl.gk + (int64_t)c * a.chunk;
+      const int32_t* gi = cl.gi + (int64_t)c * a.chunk;
+      const uint32_t dk = smem_u32(surv_key + sm.cprefix[c]), de = smem_u32(surv_ent + sm.cprefix[c]);
+#pragma unroll 1
+      for (int i = lane; i < cnt; i += 32) {
+        cp_async4_ca(dk + 4 * i, gk + i);
+        cp_async4_ca(de + 4 * i, gi + i);
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
   __syncthreads();
-  uint32_t n_surv = 0;
+  uint32_t n_surv = (uint32_t)n_cand;
+  if (tr) a.st->pad[17] = (int32_t)(clock64() - t0);
+  if (hint && staged) {
 #pragma unroll 1
-  for (int base = 0; base < n_cand; base += NT * kU) {
-    const int wbase = base + warp * 32 * kU;
-    uint32_t u[kU];
-    int32_t x[kU];
-    {
-      int v = wbase + lane;
-      int c = 0;
-      if (v < n_cand) {
-        int lo = 0, hi = nch;   // last c with cprefix[c] <= v
-#pragma unroll 1
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if ((int)sm.cprefix[mid] <= v) lo = mid;
-          else hi = mid;
-        }
-        c = lo;
-      }
-#pragma unroll
-      for (int k = 0; k < kU; ++k, v += 32) {
-        u[k] = 0u;
-        x[k] = -1;
-        if (v < n_cand) {
-          while ((int)sm.cprefix[c + 1] <= v) ++c;
-          const int64_t sl = (int64_t)c * a.chunk + (v - (int)sm.cprefix[c]);
-          u[k] = __ldcg(cl.gk + sl);
-          x[k] = __ldcg(cl.gi + sl);
-        }
-      }
+    for (int base = warp * 32; base < n_cand; base += NT) {
+      const int i = base + lane;
+      const uint32_t u = i < n_cand ? surv_key[i] : 0u;
+      const uint32_t d = key_bin(u) == tb && u != 0u ? ((u >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.sub[d], (uint32_t)__popc(peers));
     }
-    if (tr && base == 0) a.st->pad[17] = (int32_t)(clock64() - t0);
-    uint32_t bal[kU], cnt = 0;
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-      const bool f = u[k] != 0u && u[k] >= lo_key;
-      bal[k] = __ballot_sync(0xffffffffu, f);
-      if (tr && base == 0 && k == 0) a.st->pad[18] = (int32_t)(clock64() - t0);
-      cnt += __popc(bal[k]);
-      if (hint) {
-        const uint32_t d = (f && key_bin(u[k]) == tb) ? ((u[k] >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.sub[d], (uint32_t)__popc(peers));
-      }
-    }
-    if (tr && base == 0) a.st->pad[59] = (int32_t)(clock64() - t0);
-    if (lane == 0) sm.wcnt[warp] = cnt;
     __syncthreads();
-    if (tr && base == 0) a.st->pad[60] = (int32_t)(clock64() - t0);
-    uint32_t pos = n_surv, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t c = sm.wcnt[w];
-      pos += w < warp ? c : 0u;
-      tot += c;
-    }
-    if (n_surv + tot <= (uint32_t)surv_cap) {
-#pragma unroll
-      for (int k = 0; k < kU; ++k) {
-        if ((bal[k] >> lane) & 1u) {
-          const uint32_t at = pos + __popc(bal[k] & ((1u << lane) - 1u));
-          surv_key[at] = u[k];
-          surv_ent[at] = x[k];
-        }
-        pos += __popc(bal[k]);
-      }
-    }
-    n_surv += tot;
-    __syncthreads();   // wcnt is rewritten next round
   }
   trace_at(a.st, tr, 21, t0);
   if (tr) {
@@ -350,7 +308,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   // survivors below it are dropped (in order, in place) before the select.
   uint32_t prefix = lo_key, above2 = above;
   int top_bits = kBinShift;
-  if (hint && n_surv <= (uint32_t)surv_cap) {
+  if (hint && staged) {
     const uint32_t need = (uint32_t)keff - above;
     if (warp == 0) {
       // lane l holds sub-bins 255 - 8l .. 248 - 8l (descending)
@@ -426,7 +384,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   }
   trace_at(a.st, tr, 19, t0);
   if (tr) a.st->pad[31] = (int32_t)n_surv;
-  if (n_surv <= (uint32_t)surv_cap) {
+  if (staged) {
     SelSrc ss{};
     ss.key = surv_key;
     ss.ent = surv_ent;
