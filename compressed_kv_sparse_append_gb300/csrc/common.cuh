@@ -134,6 +134,41 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// CTA-scope variants for kernels launched without clusters: every arrival
+// comes from this CTA (or its own async operations), so the acquire need not
+// reach cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, DevStatus* st,
+                                              volatile int* abort, int where,
+                                              uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cta(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  const long long c0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cta(a, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (it >= kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
+          globaltimer() - t0 > limit_ns) {
+        report(st, CKV_ERR_TIMEOUT, where);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded polling wait (non-suspending test_wait) for barriers whose
 // arrivals come from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, DevStatus* st,

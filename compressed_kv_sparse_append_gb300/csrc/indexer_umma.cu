@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const int s = t % kUStages;
       bool ok = true;
       if (lane == 0 && t >= kUStages)
-        ok = mbar_wait(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11);
+        ok = mbar_wait_cta(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11);
       if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
       int64_t row = row0 + (int64_t)t * kUTile;
       if (a.bt) {
@@ -276,24 +276,36 @@ __global__ void __launch_bounds__(kUThreads, 1)
 
     if (warp == 1) {
       // ------------------------------------------------------------ MMA ----
+      // Two tiles per iteration: their waits, one fence, four MMAs.
       if (lane == 0) {
-        for (int t = 0; t < T; ++t) {
-          const int s = t % kUStages, d = t % kDBuf;
-          if (!mbar_wait(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
-          if (t >= kDBuf && !mbar_wait(&bars[BU_DEMPTY + d], ((t / kDBuf) + 1) & 1, a.st, abort_p, 13))
-            break;
-          tc_fence_after();
-          if (t < 8) trace_at(a.st, tr, 32 + t, tr0);
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
-            const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
-            umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
-                      tmem + kColSFB + 4 * ks, ks > 0);
+#pragma unroll 1
+        for (int t0 = 0; t0 < T; t0 += 2) {
+          const int nt = min(2, T - t0);
+          bool ok = true;
+#pragma unroll 1
+          for (int j = 0; j < nt && ok; ++j) {
+            const int t = t0 + j, s = t % kUStages, d = t % kDBuf;
+            ok = mbar_wait_cta(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12);
+            if (ok && t >= kDBuf)
+              ok = mbar_wait_cta(&bars[BU_DEMPTY + d], ((t / kDBuf) + 1) & 1, a.st, abort_p, 13);
           }
-          umma_commit(&bars[BU_DFULL + d]);
-          umma_commit(&bars[BU_EMPTY + s]);
-          if (t < 4) trace_at(a.st, tr, 13 + t, tr0);
+          if (!ok) break;
+          tc_fence_after();
+          if (t0 < 8) trace_at(a.st, tr, 32 + t0, tr0);
+#pragma unroll 1
+          for (int j = 0; j < nt; ++j) {
+            const int t = t0 + j, s = t % kUStages, d = t % kDBuf;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
+              const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
+              umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
+                        tmem + kColSFB + 4 * ks, ks > 0);
+            }
+            umma_commit(&bars[BU_DFULL + d]);
+            umma_commit(&bars[BU_EMPTY + s]);
+          }
+          if (t0 < 8) trace_at(a.st, tr, 13 + t0 / 2, tr0);
         }
       }
       __syncwarp();
@@ -304,7 +316,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const uint32_t lb = (uint32_t)(qd * 32) << 16;
       for (int t = 0; t < T; ++t) {
         const int s = t % kUStages;
-        if (!mbar_wait(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) break;
+        if (!mbar_wait_cta(&bars[BU_FULL + s], (t / kUStages) & 1, a.st, abort_p, 14)) break;
         const uint2 sc = *reinterpret_cast<const uint2*>(g + kOffScale + s * kScaleBytes + m * 8);
         tmem_st4(tmem + lb + kColSFA + 8 * s, sc.x, sc.x, sc.x, sc.x);
         tmem_st4(tmem + lb + kColSFA + 8 * s + 4, sc.y, sc.y, sc.y, sc.y);
@@ -325,7 +337,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
       for (int t = grp; t < T; t += 2) {
         const int d = t % kDBuf;
-        if (!mbar_wait(&bars[BU_DFULL + d], (t / kDBuf) & 1, a.st, abort_p, 15)) break;
+        if (!mbar_wait_cta(&bars[BU_DFULL + d], (t / kDBuf) & 1, a.st, abort_p, 15)) break;
         tc_fence_after();
         if (m == 0 && t < 8) trace_at(a.st, tr, 48 + t, tr0);
         uint32_t r[64];

@@ -123,11 +123,16 @@ __device__ __forceinline__ void block_radix_threshold(const SelSrc src, int n, i
   const uint32_t mask0 = top0 >= 32 ? 0u : (0xFFFFFFFFu << top0);
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll 1
-  for (int i = threadIdx.x; i < n; i += NT) {
-    const uint32_t u = src.k(i);
-    if (((u ^ prefix0) & mask0) != 0u) continue;
-    lo = min(lo, u);
-    hi = max(hi, u);
+  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * NT) {
+    uint32_t u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) u[q] = i0 + q * NT < n ? src.k(i0 + q * NT) : 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (i0 + q * NT < n && ((u[q] ^ prefix0) & mask0) == 0u) {
+        lo = min(lo, u[q]);
+        hi = max(hi, u[q]);
+      }
   }
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
@@ -168,18 +173,16 @@ __device__ __forceinline__ void block_radix_threshold(const SelSrc src, int n, i
     const int width = top < 8 ? top : 8, shift = top - width;
     const uint32_t mask = top == 32 ? 0u : (0xFFFFFFFFu << top);   // settled bits
     const uint32_t dmask = (1u << width) - 1u;
-    // one shared atomic per distinct digit per warp: keys that tie exactly
-    // (or share the digit) would otherwise serialise on one counter
+    // four independent elements per thread per iteration (plain shared
+    // atomics: warp-aggregating them with match.any measured far slower)
 #pragma unroll 1
-    for (int base = warp * 32; base < n; base += NT) {
-      const int i = base + lane;
-      uint32_t d = 0xFFFFFFFFu;
-      if (i < n) {
-        const uint32_t u = src.k(i);
-        if (((u ^ prefix) & mask) == 0) d = (u >> shift) & dmask;
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[d], (uint32_t)__popc(peers));
+    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * NT) {
+      uint32_t u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[q] = i0 + q * NT < n ? src.k(i0 + q * NT) : 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q * NT < n && ((u[q] ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u[q] >> shift) & dmask], 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -241,10 +244,15 @@ __device__ __forceinline__ int select_ordered(const SelSrc src, int n, int K, ui
   uint32_t gt = 0, eq = 0;
   if (!all) {
 #pragma unroll 1
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t u = src.k(i);
-      gt += u > T;
-      eq += u == T;
+    for (int i = i0; i < i1; i += 4) {
+      uint32_t u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[q] = i + q < i1 ? src.k(i + q) : 0u;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gt += (i + q < i1) && u[q] > T;
+        eq += (i + q < i1) && u[q] == T;
+      }
     }
   } else {
     gt = (uint32_t)(i1 - i0);

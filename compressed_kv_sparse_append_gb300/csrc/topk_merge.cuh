@@ -15,8 +15,9 @@
 //   4. it takes a ticket; the last CTA of the sequence merges: the complete
 //      histogram gives the threshold bin T and the count above it; the
 //      candidates in bins >= T are exactly the sequence's keys there (every
-//      chunk's bound is <= T); they are compacted in entry order, and an
-//      exact radix select restricted to bin T picks the top K.
+//      chunk's bound is <= T); all candidates are staged in shared memory in
+//      entry order, the keys of bin T are counted by their next 8 bits, and
+//      an exact radix select restricted to that sub-bin picks the top K.
 // Equal keys go to the earliest, i.e. lowest, entries.  When more survivors
 // reach the merge than its shared memory holds (a huge exact tie at the
 // boundary), the select runs on the candidate lists in global memory.
@@ -245,11 +246,13 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   // offset cprefix[c]): one warp per chunk list, 4-byte asynchronous copies,
   // all of them in flight at once.  Then the keys of the threshold bin are
   // counted by their next 8 bits.
+  constexpr int kWarps = NT / 32;
   const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
-  const int surv_cap = (scratch_words - pool_words) / 2;
+  const int surv_cap = (scratch_words - pool_words - kWarps * 256) / 2;
   uint32_t* surv_key = scratch;
   int32_t* surv_ent = reinterpret_cast<int32_t*>(scratch + surv_cap);
-  uint32_t* pool_key = scratch + 2 * surv_cap;
+  uint32_t* wsub = scratch + 2 * surv_cap;            // [warp][256] private sub-bin counts
+  uint32_t* pool_key = wsub + kWarps * 256;
   int32_t* pool_ent = reinterpret_cast<int32_t*>(pool_key + kMaxPool);
   SelSrc cl{};   // the candidate lists in global memory
   cl.gk = a.cand_key + (int64_t)b * nch * a.chunk;
@@ -258,10 +261,8 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   cl.n_chunks = nch;
   cl.stride = a.chunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kWarps = NT / 32;
-  constexpr int kU = 8;
   const bool hint = (int)n_total > K && keff > 0;
-  for (int i = threadIdx.x; i < 256; i += NT) sm.sub[i] = 0u;
+  for (int i = threadIdx.x; i < kWarps * 256; i += NT) wsub[i] = 0u;
   if (threadIdx.x == 0) {
     sm.bcast[0] = 0u;   // sub-bin search defaults
     sm.bcast[1] = 0u;
@@ -286,13 +287,29 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   uint32_t n_surv = (uint32_t)n_cand;
   if (tr) a.st->pad[17] = (int32_t)(clock64() - t0);
   if (hint && staged) {
+    // warp-private counters (no contention between warps on the few
+    // sub-bins that exact ties crowd), four independent elements per lane,
+    // plain shared atomics (match.any aggregation measured far slower)
+    uint32_t* ws = wsub + warp * 256;
 #pragma unroll 1
-    for (int base = warp * 32; base < n_cand; base += NT) {
-      const int i = base + lane;
-      const uint32_t u = i < n_cand ? surv_key[i] : 0u;
-      const uint32_t d = key_bin(u) == tb && u != 0u ? ((u >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&sm.sub[d], (uint32_t)__popc(peers));
+    for (int base = warp * 32; base < n_cand; base += 4 * NT) {
+      uint32_t d[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = base + q * NT + lane;
+        const uint32_t u = i < n_cand ? surv_key[i] : 0u;
+        d[q] = key_bin(u) == tb && u != 0u ? ((u >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (d[q] != 0xFFFFFFFFu) atomicAdd(&ws[d[q]], 1u);
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < 256; v += NT) {
+      uint32_t t = 0;
+#pragma unroll 1
+      for (int w = 0; w < kWarps; ++w) t += wsub[w * 256 + v];
+      sm.sub[v] = t;
     }
     __syncthreads();
   }
@@ -305,7 +322,8 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     a.st->pad[28] = (int32_t)n_total;
   }
   // The sub-bin of the threshold bin that holds the keff-th largest key: the
-  // survivors below it are dropped (in order, in place) before the select.
+  // candidates below it are dropped (in order, in place), and the exact
+  // select resolves only the keys of that sub-bin.
   uint32_t prefix = lo_key, above2 = above;
   int top_bits = kBinShift;
   if (hint && staged) {
@@ -342,8 +360,10 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     above2 = above + sm.bcast[1];
     prefix = lo_key | (t2 << (kBinShift - 8));
     top_bits = kBinShift - 8;
-    // in-place ordered compaction to keys >= prefix, kU per thread per round
-    // (a round's reads all happen before its writes, which never reach past it)
+    // in-place ordered compaction to the keys >= prefix, kU per thread per
+    // round (a round's reads all happen before its writes, which never reach
+    // past it)
+    constexpr int kU = 8;
     uint32_t kept = 0;
 #pragma unroll 1
     for (int base = 0; base < (int)n_surv; base += NT * kU) {
@@ -356,13 +376,16 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
         const int v = wbase + k * 32 + lane;
         u[k] = v < (int)n_surv ? surv_key[v] : 0u;
         x[k] = v < (int)n_surv ? surv_ent[v] : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kU; ++k) {
         bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && u[k] >= prefix);
         cnt += __popc(bal[k]);
       }
       if (lane == 0) sm.wcnt[warp] = cnt;
       __syncthreads();
       uint32_t pos = kept, tot = 0;
-#pragma unroll
+#pragma unroll 1
       for (int w = 0; w < kWarps; ++w) {
         const uint32_t c = sm.wcnt[w];
         pos += w < warp ? c : 0u;
@@ -480,7 +503,13 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
     };
     uint32_t cnt = 0;
 #pragma unroll 1
-    for (int i = i0 + lane; i - lane < i1; i += 32) cnt += __popc(__ballot_sync(0xffffffffu, take(i)));
+    for (int i = i0 + lane; i - lane < i1; i += 128) {
+      bool f[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) f[q] = take(i + 32 * q);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cnt += __popc(__ballot_sync(0xffffffffu, f[q]));
+    }
     if (lane == 0) sm.wcnt[warp] = cnt;
     __syncthreads();
     uint32_t pos = 0, tot = 0;
@@ -491,15 +520,20 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
       tot += c;
     }
 #pragma unroll 1
-    for (int i = i0 + lane; i - lane < i1; i += 32) {
-      const bool f = take(i);
-      const uint32_t bal = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const uint32_t at = pos + __popc(bal & ((1u << lane) - 1u));
-        ck[at] = keys[i];
-        ci[at] = entry_of(i);
+    for (int i = i0 + lane; i - lane < i1; i += 128) {
+      bool f[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) f[q] = take(i + 32 * q);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, f[q]);
+        if (f[q]) {
+          const uint32_t at = pos + __popc(bal & ((1u << lane) - 1u));
+          ck[at] = keys[i + 32 * q];
+          ci[at] = entry_of(i + 32 * q);
+        }
+        pos += __popc(bal);
       }
-      pos += __popc(bal);
     }
     if (threadIdx.x == 0)
       reinterpret_cast<uint2*>(a.ccount)[(int64_t)b * a.n_chunks + chunk] = make_uint2(tot, (uint32_t)n_real);
