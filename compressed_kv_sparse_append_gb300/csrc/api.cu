@@ -159,12 +159,12 @@ bool use_umma_indexer() {
   return v;
 }
 
-// CKV_DEBUG_PROGRESS (1, 2 or 3; read once per process) turns on the
+// CKV_DEBUG_PROGRESS (1 .. 6; read once per process) turns on the
 // kernels' debugging records in the status block.
 int debug_progress() {
   static const int v = [] {
     const char* e = getenv("CKV_DEBUG_PROGRESS");
-    return (e && e[0] >= '1' && e[0] <= '3') ? e[0] - '0' : 0;
+    return (e && e[0] >= '1' && e[0] <= '6') ? e[0] - '0' : 0;
   }();
   return v;
 }

@@ -115,6 +115,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Fetch a tensor map's descriptor ahead of its first use.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Four rows (y0..y3; a negative or out-of-range row reads zeros) of the
 // one-row box at column x of a 2-D tensor map, stacked at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0,
@@ -147,7 +152,7 @@ constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pai
 // last 64 latent dims (units 24..31 of half 1) are turned by the opposite
 // angle before they are stored (the output's RoPE at position -i).
 template <int GMAX>
-__device__ __forceinline__ void merge_items(const uint4* pq0, const float* wsm, int G, int H,
+__device__ __noinline__ void merge_items(const uint4* pq0, const float* wsm, int G, int H,
                                             __nv_bfloat16* out, int tid, int u0, int u1,
                                             const float2* rtab) {
   constexpr int kItems = 16 / GMAX;
@@ -240,10 +245,13 @@ __device__ __forceinline__ Tile tile_of(int t, int nt_main, int n_sel, int n_win
   return r;
 }
 
-// Asynchronous 4-byte global -> shared copies (cp.async) for the MIXED
-// scale words, whose rows are too narrow for TMA.
+// Asynchronous global -> shared copies (cp.async): 4-byte MIXED scale
+// words, and the 16-byte chunks of gathered quantised rows.
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -364,10 +372,13 @@ __device__ __forceinline__ int chunk_row(int j, int half) {
 
 }  // namespace
 
-// Debug timeline (progress mode 2): CTA (0, 0, 0) stores clock64 offsets of
+// Debug timeline (progress mode 2 / 4): CTA (0 / 1, 0, 0) stores clock64 offsets of
 // its pipeline hand-offs in the status block's spare words.
+static __device__ __noinline__ void trace_store(DevStatus* st, int slot, long long t0) {
+  if (slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
+}
 __device__ __forceinline__ void trace(DevStatus* st, bool on, int slot, long long t0) {
-  if (on && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
+  if (on) trace_store(st, slot, t0);
 }
 
 template <int FMT>
@@ -402,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const uint32_t peer = rank ^ 1u;
   const int b = blockIdx.y;
   const int G = a.G;
-  const bool use_tma = a.use_tma != 0;
+  const bool use_tma = FMT == CKV_FMT_BF16 && a.use_tma != 0;   // contiguous BF16 rows only
 
   if (tid == 0) {
     abort_flag = 0;
@@ -425,6 +436,16 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     fence_mbar_init();
   }
   if (warp == 5) tmem_alloc(tslot, kTmemCols);
+  if (tid == 32) {
+    // kernel parameters, not outputs of the previous kernel: fetched
+    // before the grid dependency resolves
+    if (use_tma) {
+      prefetch_tmap(&map_kv);
+      prefetch_tmap(&map_win);
+    } else if (FMT == CKV_FMT_BF16) {
+      for (int k = 0; k < 4; ++k) prefetch_tmap(&a.gmap[k]);
+    }
+  }
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
@@ -442,7 +463,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   volatile int* abort_p = &abort_flag;
   const bool prog = a.progress == 1;
-  const bool tr = a.progress == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  // progress modes 2 / 4 trace CTA 0 / 1 of sequence 0 over tiles 0..7,
+  // modes 5 / 6 the same CTAs over tiles 8..15
+  const bool tr = (a.progress == 2 || a.progress >= 4) && blockIdx.y == 0 && blockIdx.z == 0 &&
+                  (int)blockIdx.x == ((a.progress == 4 || a.progress == 6) ? 1 : 0);
+  const int toff = a.progress >= 5 ? 8 : 0;
   const long long tr0 = clock64();
   // progress mode 3: the CTAs of sequence 0 (layer 0) store %globaltimer
   // (low 32 bits) at start, softmax end and cluster-barrier exit
@@ -479,6 +504,18 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   };
 
   if (warp >= 6) {
+    // Q[b, h, half]: the thread's 512 bytes are all requested at once (one
+    // memory round trip, however loaded the memory system is).
+    const int h = (warp & 3) * 32 + lane;
+    uint4 qv[32];
+    if (h < a.H) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.H + h) * 512 + half * 256);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) qv[k] = __ldg(src + k);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) qv[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
     // RoPE table of this sequence ("DeepSeek-V4 KV Cache 深度分析", §五: the
     // query's and the output's last 64 dims, i.e. half 1): pair k turns by
     // i * theta_k, reduced modulo 2 pi in double precision first.
@@ -496,34 +533,26 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
       asm volatile("bar.sync 4, 128;" ::: "memory");
     }
-    // Q[b, h, half] -> TMEM as the bf16 A operand (lane h, two elements per column)
-    const int h = (warp & 3) * 32 + lane;
+    // Q -> TMEM as the bf16 A operand (lane h, two elements per column)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t r[32];
-      if (h < a.H) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.H + h) * 512 + half * 256 + c * 64);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = src[k];
-          r[4 * k] = v.x;
-          r[4 * k + 1] = v.y;
-          r[4 * k + 2] = v.z;
-          r[4 * k + 3] = v.w;
+      for (int k = 0; k < 8; ++k) {
+        r[4 * k] = qv[8 * c + k].x;
+        r[4 * k + 1] = qv[8 * c + k].y;
+        r[4 * k + 2] = qv[8 * c + k].z;
+        r[4 * k + 3] = qv[8 * c + k].w;
+      }
+      if (c == 3 && rope && a.rope_q && h < a.H) {
+        // dims 448 + 2k, 449 + 2k (one bf16 pair per word) turn by +i theta_k
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 cs = rtab[k];
+          const float re = __uint_as_float(r[k] << 16), im = __uint_as_float(r[k] & 0xFFFF0000u);
+          r[k] = pack_bf16(re * cs.x - im * cs.y, re * cs.y + im * cs.x);
         }
-        if (rope && a.rope_q && c == 3) {
-          // dims 448 + 2k, 449 + 2k (one bf16 pair per word) turn by +i theta_k
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float2 cs = rtab[k];
-            const float re = __uint_as_float(r[k] << 16), im = __uint_as_float(r[k] & 0xFFFF0000u);
-            r[k] = pack_bf16(re * cs.x - im * cs.y, re * cs.y + im * cs.x);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = 0u;
       }
       tmem_st32(tmem + lane_base + kColQ + c * 32, r);
     }
@@ -592,16 +621,20 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
           const int j = next_fix, s = j % kStages;
           const uint32_t tile = base + kOffE + s * kEBytes;
           const Tile tl = tile_of(t0 + j, nt_main, n_sel, n_win);
-          if (!mbar_wait(&bars[B_TMA + s], (j / kStages) & 1, a.st, abort_p, 22)) {
-            ok = false;
-            break;
+          // A full tile needs no fix-up: e_full only keeps its phase count
+          // (the MMA waits for the TMA bytes itself), so the exchange below
+          // never waits for memory.
+          if (tl.valid < kTile) {
+            if (!mbar_wait(&bars[B_TMA + s], (j / kStages) & 1, a.st, abort_p, 22)) {
+              ok = false;
+              break;
+            }
+            for (int e = p; e < (kTile - tl.valid) * 32; e += 128) {
+              const int r = tl.valid + (e >> 5), cc = e & 31;
+              st_shared_v4(sw128(tile + (cc >> 3) * 8192, r, cc & 7), make_uint4(0, 0, 0, 0));
+            }
+            fence_proxy_async_smem();
           }
-          if (p == 0 && j < 8) trace(a.st, tr, 49 + j, tr0);
-          for (int e = p; e < (kTile - tl.valid) * 32; e += 128) {
-            const int r = tl.valid + (e >> 5), cc = e & 31;
-            st_shared_v4(sw128(tile + (cc >> 3) * 8192, r, cc & 7), make_uint4(0, 0, 0, 0));
-          }
-          fence_proxy_async_smem();
           mbar_arrive(&bars[B_EFULL + s]);
           if (p == 0) progress(a.st, prog, 5);
         }
@@ -654,58 +687,71 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const uint32_t bal = __ballot_sync(0xffffffffu, e >= 0);
       if ((r & 31) == 0) vmask_s[(i % kStages) * 2 + (r >> 5)] = bal;
     };
-    // the copies of tile i (rows published, stage free): the tile's rows by
-    // TMA gathers of four rows each, issued by one thread; MIXED scale words
-    // (4-byte row strides, which TMA cannot address) by cp.async
+    // the copies of tile i (rows published, stage free).  BF16 rows go by
+    // TMA gathers of four rows each, issued by one thread per warp, straight
+    // to their swizzled place.  Quantised rows and their scales go by
+    // cp.async into the staging area, 16 bytes (MIXED scale words: 4 bytes,
+    // a row stride TMA cannot address) a copy, every producer thread
+    // issuing its own chunks: they need no tensor map and complete under the
+    // thread's cp.async groups, which finish(i) waits for.
     auto copies = [&](int i) {
       const int s = i % kStages;
       if (p == 0 && i < 4) trace(a.st, tr, 49 + i, tr0);
       const uint32_t tile = base + kOffE + s * kEBytes;
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
-      const CUtensorMap* gm = &a.gmap[tl.win ? 2 : 0];
       const int32_t* rs = rsrc + s * 64;
-      if ((p & 31) == 0) {
-        // lane 0 of each producer warp issues four of the sixteen groups;
-        // warp 0's also arms the barrier (the transaction count may go
-        // negative until it does)
-        constexpr uint32_t kBytes = FMT == CKV_FMT_BF16 ? 64 * 512 : FMT == CKV_FMT_FP4 ? 64 * 144 : 0;
-        const uint32_t bytes = FMT == CKV_FMT_MIXED ? 64u * (half == 0 ? 256u : 320u) : kBytes;
-        if (p == 0) mbar_expect_tx(&bars[B_GFULL + s], bytes);
+      if constexpr (FMT == CKV_FMT_BF16) {
+        const CUtensorMap* gm = &a.gmap[tl.win ? 2 : 0];
+        if ((p & 31) == 0) {
+          // lane 0 of each producer warp issues four of the sixteen groups;
+          // warp 0's also arms the barrier (the transaction count may go
+          // negative until it does)
+          if (p == 0) mbar_expect_tx(&bars[B_GFULL + s], 64u * 512u);
 #pragma unroll 1
-        for (int g = (p >> 5) * 4; g < (p >> 5) * 4 + 4; ++g) {
-          int y[4];
+          for (int g = (p >> 5) * 4; g < (p >> 5) * 4 + 4; ++g) {
+            int y[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // an empty row reads the plane's first row (a valid address)
-            // and is zeroed or skipped by the producers from the mask
-            const int32_t e = rs[4 * g + k];
-            y[k] = e >= 0 ? e : 0;
-          }
-          if constexpr (FMT == CKV_FMT_BF16) {
+            for (int k = 0; k < 4; ++k) {
+              // an empty row reads the plane's first row (a valid address)
+              // and is zeroed from the mask
+              const int32_t e = rs[4 * g + k];
+              y[k] = e >= 0 ? e : 0;
+            }
 #pragma unroll
             for (int kc = 0; kc < 4; ++kc)
               tma_gather4(tile + kc * 8192 + g * 512, gm, half * 256 + kc * 64, y[0], y[1], y[2], y[3],
                           &bars[B_GFULL + s]);
-          } else if constexpr (FMT == CKV_FMT_MIXED) {
-            tma_gather4(tile + kRawOffMixed + g * 4 * (half == 0 ? 256 : 320), gm + half, half * 128,
-                        y[0], y[1], y[2], y[3], &bars[B_GFULL + s]);
-          } else {
-            tma_gather4(tile + kRawOffFp4 + g * 512, gm, half * 128, y[0], y[1], y[2], y[3],
-                        &bars[B_GFULL + s]);
-            tma_gather4(tile + kScaleOffFp4 + g * 128, gm + 1, half * 16, y[0], y[1], y[2], y[3],
-                        &bars[B_GFULL + s]);   // 128-byte aligned groups of four 16-byte rows
           }
         }
-      }
-      if constexpr (FMT == CKV_FMT_MIXED) {
-        // row p's scale words for this half (at most 4: nope_block is 448 or 64)
-        if (p < 64 && rs[p] >= 0) {
-          const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
-          const int64_t ent = rs[p];
-          const int nblk = 448 / a.nope_block, nb0 = (half * 256) / a.nope_block;
-          const int nb1 = (half * 256 + (half == 0 ? 256 : 192) - 1) / a.nope_block;
-          for (int k = 0; k <= nb1 - nb0; ++k)
-            cp_async4(tile + kScaleOffMixed + p * 32 + k * 4, scale + (ent * nblk + nb0 + k) * 4);
+      } else {
+        const uint8_t* data = tl.win ? a.win_data : a.kv_data;
+        constexpr int kRowBytes = FMT == CKV_FMT_MIXED ? 576 : 256;
+        const int hoff = FMT == CKV_FMT_MIXED ? half * 256 : half * 128;
+        const int hbytes = FMT == CKV_FMT_MIXED ? (half == 0 ? 256 : 320) : 128;
+        const uint32_t raw0 = tile + (FMT == CKV_FMT_MIXED ? kRawOffMixed : kRawOffFp4);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = p + 128 * u;
+          if (j < kTile * J) {
+            const int r = chunk_row<FMT>(j, half), q = j - r * J;
+            const int32_t e = rs[r];
+            if (e >= 0) cp_async16(raw0 + r * hbytes + q * 16, data + (int64_t)e * kRowBytes + hoff + q * 16);
+          }
+        }
+        const uint8_t* scale = static_cast<const uint8_t*>(tl.win ? a.win_scale : a.kv_scale);
+        if constexpr (FMT == CKV_FMT_MIXED) {
+          // row p's scale words for this half (at most 4: nope_block is 448 or 64)
+          if (p < 64 && rs[p] >= 0) {
+            const int64_t ent = rs[p];
+            const int nblk = 448 / a.nope_block, nb0 = (half * 256) / a.nope_block;
+            const int nb1 = (half * 256 + (half == 0 ? 256 : 192) - 1) / a.nope_block;
+            for (int k = 0; k <= nb1 - nb0; ++k)
+              cp_async4(tile + kScaleOffMixed + p * 32 + k * 4, scale + (ent * nblk + nb0 + k) * 4);
+          }
+        } else {
+          // row p's 16 scale bytes of this half, in 128-byte groups of four rows
+          if (p < 64 && rs[p] >= 0)
+            cp_async16(tile + kScaleOffFp4 + (p >> 2) * 128 + (p & 3) * 16, scale + (int64_t)rs[p] * 32 + half * 16);
         }
       }
       cp_async_commit();
@@ -713,7 +759,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     auto finish = [&](int i, int newer) -> bool {
       const int s = i % kStages;
       const uint32_t tile = base + kOffE + s * kEBytes;
-      bool landed = mbar_wait(&bars[B_GFULL + s], (i / kStages) & 1, a.st, abort_p, 35);
+      bool landed = FMT != CKV_FMT_BF16 || mbar_wait(&bars[B_GFULL + s], (i / kStages) & 1, a.st, abort_p, 35);
       cp_async_wait(newer);                      // this thread's copies of tile i
       if (!bar_and(2, 128, landed)) return false;   // everyone's
       if (p == 0 && i < 2) trace(a.st, tr, 51 + i, tr0);   // debug: data landed
@@ -783,7 +829,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
       int32_t x_next = p < 64 ? raw_index(n_init, p) : -1;   // used one tile later
       asm volatile("bar.sync 2, 128;" ::: "memory");
+      if (p == 0) trace(a.st, tr, 3, tr0);   // debug: first rows published
       for (int t = 0; t < n_init; ++t) copies(t);
+      if (p == 0) trace(a.st, tr, 7, tr0);   // debug: first copies issued
       int issued = n_init, finished = 0;
       bool ok = true;
       for (int i = 0; i < n_my && ok; ++i) {
@@ -806,7 +854,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
       }
       cp_async_wait(0);   // nothing stays in flight past this point
-      if (p == 0 && finished < issued) {
+      if (FMT == CKV_FMT_BF16 && p == 0 && finished < issued) {
         // a wait failed: let the gathers already issued land (bounded)
         // before this CTA can exit
         volatile int keep_waiting = 0;
@@ -822,7 +870,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const int sj = j % kStages, bj = j & 1;
         if (!mbar_wait(&bars[B_PFULL + bj], (j >> 1) & 1, a.st, abort_p, 24)) return false;
         tc_fence_after();
-        if (j < 8) trace(a.st, tr, 17 + j, tr0);
+        if ((unsigned)(j - toff) < 8u) trace(a.st, tr, 17 + j - toff, tr0);
         const uint32_t tile = base + kOffE + sj * kEBytes;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -839,8 +887,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const int s = i % kStages, bi = i & 1;
         const uint32_t tile = base + kOffE + s * kEBytes;
         if (!mbar_wait(&bars[B_EFULL + s], (i / kStages) & 1, a.st, abort_p, 25)) break;
+        if (use_tma && !mbar_wait(&bars[B_TMA + s], (i / kStages) & 1, a.st, abort_p, 37)) break;
         tc_fence_after();
-        if (i < 8) trace(a.st, tr, 1 + i, tr0);
+        if (use_tma && (unsigned)(i - toff) < 8u) trace(a.st, tr, 49 + i - toff, tr0);   // the tile's bytes have landed
+        if ((unsigned)(i - toff) < 8u) trace(a.st, tr, 1 + i - toff, tr0);
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
           const uint32_t kc = ks >> 2, w = ks & 3;
@@ -849,7 +899,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
         umma_commit(&bars[B_SFULL + bi]);
         progress(a.st, prog, 1);
-        if (i < 8) trace(a.st, tr, 9 + i, tr0);
+        if ((unsigned)(i - toff) < 8u) trace(a.st, tr, 9 + i - toff, tr0);
         if (i > 0) ok = issue_pv(i - 1);
       }
       if (ok && n_my > 0) issue_pv(n_my - 1);
@@ -871,10 +921,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       if (!mbar_wait(&bars[B_SFULL + bi], (i >> 1) & 1, a.st, abort_p, 26)) break;
       tc_fence_after();
       if (h == 0) progress(a.st, prog, 2);
-      if (h == 0 && i < 8) trace(a.st, tr, 25 + i, tr0);
+      if (h == 0 && (unsigned)(i - toff) < 8u) trace(a.st, tr, 25 + i - toff, tr0);
       if (!use_tma) {
         send_scores(i, h);
         mbar_arrive_remote(mapa(smem_u32(&bars[B_XFULL + i % kXBufs]), peer));
+        if (h == 0 && i < 2) trace(a.st, tr, 5 + i, tr0);   // debug: S(i) sent
       }
       const Tile tl = tile_of(t0 + i, nt_main, n_sel, n_win);
       // validity of the tile's rows (selected entries may be -1 / out of range)
@@ -889,7 +940,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const uint32_t xi = i % kXBufs;
       if (!mbar_wait_poll(&bars[B_XFULL + xi], (i / kXBufs) & 1, a.st, abort_p, 27)) break;
       if (h == 0) progress(a.st, prog, 3);
-      if (h == 0 && i < 8) trace(a.st, tr, 33 + i, tr0);
+      if (h == 0 && (unsigned)(i - toff) < 8u) trace(a.st, tr, 33 + i - toff, tr0);
       const uint32_t xrow = base + kOffX + xi * kXBytes + h * 128;
       // Raw scores of row h: s_j = own_j + peer_j (own: S(i) in TMEM, fp32;
       // peer: its fp16 partial), -inf for an invalid column.  All 64 stay in
@@ -974,7 +1025,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       tc_fence_before();
       mbar_arrive(&bars[B_PFULL + bi]);
       if (h == 0) progress(a.st, prog, 8);
-      if (h == 0 && i < 8) trace(a.st, tr, 41 + i, tr0);
+      if (h == 0 && (unsigned)(i - toff) < 8u) trace(a.st, tr, 41 + i - toff, tr0);
     }
     if (n_my > 0) {
       // s_full of the last tile implies every PV up to n_my - 3 is done, so
@@ -1014,7 +1065,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
     }
     reinterpret_cast<float2*>(po + 32 * 128)[h] = make_float2(m_used, l);
-    __threadfence();
+    // No fence here: the CTA barrier below orders these stores before the
+    // cluster barrier's release (a sequence-wide cluster) or before thread
+    // 0's fence and counter increment (pair clusters).
+    if (h == 0 && !use_tma) trace(a.st, tr, 11, tr0);   // debug: partial stored
   }
   tc_fence_before();
   if (tid == 0) progress(a.st, prog, 6);
@@ -1043,6 +1097,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   }
   __syncthreads();
   if (tid == 0) stamp3(2);
+  if (tid == 0 && !use_tma) trace(a.st, tr, 13, tr0);   // debug: every partial of the sequence written
   if (!*abort_p) {
     const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
                        (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
@@ -1082,6 +1137,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
     else if (G <= 4) merge_items<4>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
     else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
+    if (tid == 0 && !use_tma) trace(a.st, tr, 4, tr0);   // debug: merge done
   }
   // the last CTA of the sequence to leave resets the counters for the next call
   __syncthreads();
@@ -1126,27 +1182,13 @@ bool encode_gather_rows(CUtensorMap* m, const void* data, CUtensorMapDataType dt
 // elements); FP4: 128-byte code boxes and 16-byte scale boxes.
 bool encode_gather_maps(AttnArgs& a, int B) {
   const uint8_t* data[2] = {a.kv_data, a.win_data};
-  const void* scale[2] = {a.kv_scale, a.win_scale};
   const int64_t rows[2] = {a.kv_rows, (int64_t)B * a.win_cap};
   for (int k = 0; k < 2; ++k) {
     CUtensorMap* m = &a.gmap[2 * k];
-    bool ok;
-    if (a.fmt == CKV_FMT_BF16) {
-      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows[k], 512, 64,
-                              CU_TENSOR_MAP_SWIZZLE_128B);
-      m[1] = m[0];
-    } else if (a.fmt == CKV_FMT_MIXED) {
-      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, rows[k], 288, 128,
-                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode_gather_rows(m + 1, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, rows[k], 288, 160,
-                              CU_TENSOR_MAP_SWIZZLE_NONE);
-    } else {
-      ok = encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows[k], 256, 128,
-                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode_gather_rows(m + 1, scale[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows[k], 32, 16,
-                              CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
-    if (!ok) return false;
+    if (!encode_gather_rows(m, data[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows[k], 512, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+    m[1] = m[0];
   }
   return true;
 }
@@ -1197,9 +1239,11 @@ cudaError_t launch_attention_layers(const AttnArgs* layers, int n, int B, cudaSt
       encode_bf16_rows(&mk, a0.kv_data, a0.kv_rows) &&
       encode_bf16_rows(&mw, a0.win_data, (int64_t)B * a0.win_cap))
     batch.layer[0].use_tma = 1;
-  // every other layer gathers its rows with TMA
+  // BF16 layers gather their rows with TMA (quantised rows go by cp.async)
   for (int l = 0; l < n; ++l)
-    if (!batch.layer[l].use_tma && !encode_gather_maps(batch.layer[l], B)) return cudaErrorInvalidValue;
+    if (!batch.layer[l].use_tma && batch.layer[l].fmt == CKV_FMT_BF16 &&
+        !encode_gather_maps(batch.layer[l], B))
+      return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * a0.G, B, n);
   cfg.blockDim = dim3(kThreadsAttn, 1, 1);

@@ -45,7 +45,7 @@ struct AttnArgs {
   const float* rope_freq;   // [32] angle per position of rope pair k
   int rope_q, rope_out;     // turn the query by +i / the output by -i
   DevStatus* st;
-  CUtensorMap gmap[4];    // set by the launcher: row-gather maps (main, window)
+  CUtensorMap gmap[4];    // set by the launcher for BF16 rows: row-gather maps (main, window)
 };
 
 constexpr int kMaxPairs = 8;      // CTA pairs per sequence

@@ -60,7 +60,7 @@ struct DevStatus {
 };
 static_assert(sizeof(DevStatus) == 256, "status block is 256 bytes");
 
-__device__ __forceinline__ void report(DevStatus* st, int32_t code, int32_t detail) {
+static __device__ __noinline__ void report(DevStatus* st, int32_t code, int32_t detail) {
   if (st == nullptr) return;
   atomicExch(&st->code, code);
   atomicAdd(&st->count, 1u);
@@ -148,19 +148,23 @@ __device__ __forceinline__ bool mbar_try_wait_cta(uint32_t bar, uint32_t parity)
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, DevStatus* st,
-                                              volatile int* abort, int where,
-                                              uint64_t limit_ns = kWaitLimitNs) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cta(a, parity)) return true;
+// The bounded loop behind every wait below.
+// kind 0: try_wait, acquire at cluster scope; 1: try_wait, CTA scope;
+// 2: polling test_wait, cluster scope.
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, DevStatus* st,
+                                            volatile int* abort, int where, uint64_t limit_ns,
+                                            int kind) {
   const uint64_t t0 = globaltimer();
   const long long c0 = clock64();
+  const uint32_t mask = kind == 2 ? 255u : 63u;
+  const uint32_t max_it = kind == 2 ? 16u * kWaitLimitIters : kWaitLimitIters;
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cta(a, parity)) return true;
-    if ((it & 63u) == 0) {
+    const bool ok = kind == 0 ? mbar_try_wait(a, parity)
+                              : kind == 1 ? mbar_try_wait_cta(a, parity) : mbar_test_wait(a, parity);
+    if (ok) return true;
+    if ((it & mask) == 0) {
       if (*abort) return false;
-      if (it >= kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
-          globaltimer() - t0 > limit_ns) {
+      if (it >= max_it || clock64() - c0 > kWaitLimitCycles || globaltimer() - t0 > limit_ns) {
         report(st, CKV_ERR_TIMEOUT, where);
         *abort = 1;
         return false;
@@ -169,26 +173,22 @@ __device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, De
   }
 }
 
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, DevStatus* st,
+                                              volatile int* abort, int where,
+                                              uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cta(a, parity)) return true;
+  return mbar_wait_slow(a, parity, st, abort, where, limit_ns, 1);
+}
+
 // Bounded polling wait (non-suspending test_wait) for barriers whose
 // arrivals come from other CTAs of the cluster.
 __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, DevStatus* st,
                                                volatile int* abort, int where,
                                                uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer();
-  const long long c0 = clock64();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_test_wait(a, parity)) return true;
-    if ((it & 255u) == 255u) {
-      if (*abort) return false;
-      if (it >= 16u * kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
-          globaltimer() - t0 > limit_ns) {
-        report(st, CKV_ERR_TIMEOUT, where);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
+  if (mbar_test_wait(a, parity)) return true;
+  return mbar_wait_slow(a, parity, st, abort, where, limit_ns, 2);
 }
 
 // Bounded wait for the phase with parity `parity` to complete.  On expiry
@@ -199,20 +199,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevSta
                                           uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  const long long c0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort) return false;
-      if (it >= kWaitLimitIters || clock64() - c0 > kWaitLimitCycles ||
-          globaltimer() - t0 > limit_ns) {
-        report(st, CKV_ERR_TIMEOUT, where);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait_slow(a, parity, st, abort, where, limit_ns, 0);
 }
 
 // Bounded spin of one thread until the global counter *cnt reaches
@@ -238,14 +225,20 @@ __device__ __forceinline__ bool spin_until_geq(const uint32_t* cnt, uint32_t tar
 
 // Optional progress counters (debugging): slot k of the status block's
 // spare words counts events of kind k.  Enabled per launch.
+static __device__ __noinline__ void progress_add(DevStatus* st, int k) {
+  if (st != nullptr) atomicAdd(reinterpret_cast<unsigned int*>(&st->pad[k]), 1u);
+}
 __device__ __forceinline__ void progress(DevStatus* st, bool on, int k) {
-  if (on && st != nullptr) atomicAdd(reinterpret_cast<unsigned int*>(&st->pad[k]), 1u);
+  if (on) progress_add(st, k);
 }
 
 // Debug timeline: store the clock64 offset of an event in spare word `slot`
 // of the status block.
+static __device__ __noinline__ void trace_at_store(DevStatus* st, int slot, long long t0) {
+  if (st != nullptr && slot >= 0 && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
+}
 __device__ __forceinline__ void trace_at(DevStatus* st, bool on, int slot, long long t0) {
-  if (on && st != nullptr && slot >= 0 && slot < 61) st->pad[slot] = (int32_t)(clock64() - t0);
+  if (on) trace_at_store(st, slot, t0);
 }
 
 // Asynchronous 4-byte copy global -> shared (cp.async, cached in L1; the
