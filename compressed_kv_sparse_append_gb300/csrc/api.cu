@@ -269,12 +269,13 @@ void attn_set_ws_single(AttnArgs& a, uint8_t* region, int B) {
   a.part = reinterpret_cast<float*>(region + shared_zero_bytes(B));
 }
 
-// Picks the number of CTA pairs per sequence and the cluster shape.  Every
-// pair of the launch (n_seq sequence-layers x G) must be resident at once and
-// each pair keeps at least two 64-row tiles.  A cluster of all 2G CTAs of a
-// sequence merges through a hardware-scheduled cluster barrier; pair clusters
-// merge through a counter in the workspace but fit more pairs on the GPU, so
-// they are taken only when they allow a larger G.
+// Picks the number of CTA pairs per sequence and the cluster shape; each
+// pair keeps at least two 64-row tiles.  A cluster of all 2G CTAs of a
+// sequence merges after a hardware-scheduled cluster barrier.  Pair clusters
+// fit more pairs on the GPU; their sequence's partials are merged by the
+// last CTA of each half to finish (a counter in the workspace, no waiting),
+// and they are taken when they allow a larger G.  Neither needs more than
+// the launch's clusters resident at once.
 struct PairChoice {
   int G;
   int cluster_all;

@@ -1082,23 +1082,35 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   pdl_launch_dependents();
 
   // ------------------------------------ merge of the G partials of half c ----
-  // With pair clusters, every CTA of the sequence (2G, all resident: the
-  // launcher sizes the grid to fit the GPU) counts itself in once its
-  // partial is written and waits (bounded) for the others.  Then pair `pair`
-  // merges units [u0, u1) of 8
-  // columns of its half: each head row's (m, l) of the G pairs become weights
-  // l_q 2^(m_q - M) / L in shared memory (the tile ring is dead by now), and
-  // all 320 threads combine (row, unit) items, 16 loads in flight each.
+  // With a sequence-wide cluster every partial of the sequence is written
+  // once the cluster barrier above is through, and pair `pair` merges units
+  // [u0, u1) of 8 columns of its half.  Each head row's (m, l) of the G
+  // pairs become weights l_q 2^(m_q - M) / L in shared memory (the tile ring
+  // is dead by now), and all 320 threads combine (row, unit) items, 16 loads
+  // in flight each.
+  // With pair clusters, no CTA waits for another cluster: each CTA counts
+  // itself in on its half's counter once its partial is written, and the
+  // last of the G CTAs of a half merges all 32 units of that half (and
+  // resets the counter for the next call).  A launch therefore never depends
+  // on CTAs outside its own clusters being resident.
   uint32_t* cnt = a.tickets + ((int64_t)blockIdx.z * gridDim.y + b) * 2;
-  if (tid == 0 && !a.cluster_all) {
-    __threadfence();
-    atomicAdd(cnt, 1u);
-    spin_until_geq(cnt, (uint32_t)(2 * G), a.st, abort_p, 31);
+  __shared__ int merge_here;
+  if (tid == 0) {
+    int last = 1;
+    if (!a.cluster_all) {
+      __threadfence();   // this CTA's partial (ordered before by the CTA barrier) before its count
+      last = atomicAdd(cnt + half, 1u) == (uint32_t)(G - 1);
+      if (last) {
+        __threadfence();   // the other CTAs' partials, released by their counts, after ours
+        cnt[half] = 0u;
+      }
+    }
+    merge_here = last;
   }
   __syncthreads();
   if (tid == 0) stamp3(2);
-  if (tid == 0 && !use_tma) trace(a.st, tr, 13, tr0);   // debug: every partial of the sequence written
-  if (!*abort_p) {
+  if (tid == 0 && !use_tma) trace(a.st, tr, 13, tr0);   // debug: every partial of the half written
+  if (!*abort_p && merge_here) {
     const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
                        (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
     float* wsm = reinterpret_cast<float*>(gbase + kOffE);   // [kMaxPairs][128] weights
@@ -1126,12 +1138,14 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
       for (int q = 0; q < kMaxPairs; ++q) wsm[q * 128 + h] = lq[q] * inv;
-      if (blockIdx.x == 0 && a.lse && h < a.H)
+      // one CTA of half 0 writes the lse
+      const bool lse_here = a.cluster_all ? blockIdx.x == 0 : half == 0;
+      if (lse_here && a.lse && h < a.H)
         a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
     __nv_bfloat16* out = a.out + (int64_t)b * a.H * 512 + half * 256;
-    const int u0 = pair * 32 / G, u1 = (pair + 1) * 32 / G;
+    const int u0 = a.cluster_all ? pair * 32 / G : 0, u1 = a.cluster_all ? (pair + 1) * 32 / G : 32;
     const float2* rtab = (half == 1 && a.rope_pos && a.rope_out)
                              ? reinterpret_cast<const float2*>(gbase + kOffRope) : nullptr;
     if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
@@ -1139,13 +1153,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
     if (tid == 0 && !use_tma) trace(a.st, tr, 4, tr0);   // debug: merge done
   }
-  // the last CTA of the sequence to leave resets the counters for the next call
   __syncthreads();
   if (tid == 0) stamp3(3);
-  if (tid == 0 && !a.cluster_all && atomicAdd(cnt + 1, 1u) == (uint32_t)(2 * G - 1)) {
-    cnt[0] = 0u;
-    cnt[1] = 0u;
-  }
 
   tc_fence_before();
   __syncthreads();

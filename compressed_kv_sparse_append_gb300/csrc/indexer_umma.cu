@@ -8,11 +8,13 @@
 // tensor core applies both scales per 16-element block and accumulates in
 // f32, so the FP4 bytes go from HBM to the tensor core untouched.
 //
-// Per CTA: one chunk of C keys of one sequence.
-//   warp 0   TMA producer: 128-key tiles of packed codes (SWIZZLE_64B) and
+// Per CTA: one chunk of C keys of one sequence (for a CSA2 Reindex pass: C
+// entries of the sequence's candidate pool).
+//   warp 0   producer: 128-key tiles of packed codes (SWIZZLE_64B) and
 //            their scale bytes into a kUStages-deep shared-memory ring,
 //            starting as soon as the previous kernel is done (the other
-//            warps quantise the query meanwhile);
+//            warps quantise the query meanwhile) -- streamed by TMA, or,
+//            for a pool, gathered row by row with cp.async;
 //   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, four
 //            buffers, so the MMA runs up to three tiles ahead of the
 //            epilogue) = keys (A, M = 128) x query (B, N = 64), K = 128 in
@@ -24,6 +26,8 @@
 //            chunk's shared-memory histogram.
 // The scores stay in shared memory; the candidate bound and the cross-chunk
 // merge are those of topk_merge.cuh.
+
+#include <cstring>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -83,6 +87,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// cp.async of `bytes` (8 or 16) from global to shared; src_bytes = 0 reads
+// nothing and writes zeros.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued before has landed
+// (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // 16-byte chunk c (0..3) of row r of a 64-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 
@@ -115,7 +135,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (tid == 0) {
     abort_flag = 0;
     for (int s = 0; s < kUStages; ++s) {
-      mbar_init(&bars[BU_FULL + s], 1);
+      // a gathered tile completes with the 32 producer lanes' cp.async
+      // arrivals, a streamed one with one transaction-counted TMA arrival
+      mbar_init(&bars[BU_FULL + s], a.pool ? 32 : 1);
       mbar_init(&bars[BU_EMPTY + s], 1);
       mbar_init(&bars[BU_SFA + s], 128);
     }
@@ -135,14 +157,60 @@ __global__ void __launch_bounds__(kUThreads, 1)
   const int b = blockIdx.y, chunk = blockIdx.x;
   const int ncomp = min(a.n_comp[b], a.n_comp_max);
   const int64_t c0 = (int64_t)chunk * a.chunk;
-  const int n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, (int64_t)ncomp - c0));
+  // Reindex (a.pool): chunk `chunk` of the sequence's candidate list, whose
+  // entries name the keys; otherwise keys c0 .. of the plane
+  const int32_t* pl = a.pool ? a.pool + (int64_t)b * a.pool_len + c0 : nullptr;
+  const int64_t n_avail = a.pool ? (int64_t)a.pool_len - c0 : (int64_t)ncomp - c0;
+  const int n_elem = (int)max((int64_t)0, min((int64_t)a.chunk, n_avail));
   const int T = (n_elem + kUTile - 1) / kUTile;
   const int64_t row0 = (int64_t)b * a.cap + c0;
   volatile int* abort_p = &abort_flag;
   const bool tr = a.trace && b == 0 && chunk == 0;
   const long long tr0 = clock64();
 
-  if (warp == 0) {
+  if (warp == 0 && pl) {
+    // ----------------------------------------------- gathered key rows ----
+    // Lane l gathers keys l, l + 32, l + 64, l + 96 of each tile: the 64
+    // code bytes (four 16-byte copies to their SW64 places) and the 8 scale
+    // bytes of the key's row; an empty or out-of-range entry copies zeros.
+    // The stage completes with every lane's cp.async arrival.
+    const uint8_t* kd = static_cast<const uint8_t*>(a.kdata);
+    const uint8_t* ks = static_cast<const uint8_t*>(a.kscale);
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      const int s = t % kUStages;
+      bool ok = true;
+      if (lane == 0 && t >= kUStages)
+        ok = mbar_wait_cta(&bars[BU_EMPTY + s], ((t / kUStages) + 1) & 1, a.st, abort_p, 11);
+      if (!__shfl_sync(0xffffffffu, (int)ok, 0)) break;
+      int32_t e[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = t * kUTile + lane + 32 * k;
+        e[k] = i < n_elem ? __ldg(pl + i) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = lane + 32 * k;
+        int64_t row = -1;
+        if (e[k] >= ncomp) report(a.st, CKV_ERR_DEVICE_BOUNDS, e[k]);
+        else if (e[k] >= 0) row = plane_row(a.bt, a.page, a.bt_cols, a.cap, b, e[k]);
+        if (row >= ua.row_limit) {   // a page id beyond the plane
+          report(a.st, CKV_ERR_DEVICE_BOUNDS, e[k]);
+          row = -1;
+        }
+        const uint32_t nb = row >= 0 ? 16u : 0u;
+        const int64_t rr = row >= 0 ? row : 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          cp_async16_zfill(base + kOffData + s * kDataBytes + sw64(r, c), kd + rr * 64 + c * 16, nb);
+        cp_async8_zfill(base + kOffScale + s * kScaleBytes + r * 8, ks + rr * 8, nb >> 1);
+      }
+      cp_async_arrive_noinc(&bars[BU_FULL + s]);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");   // nothing in flight past this point
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA ----
     // The key stream does not depend on the query: it starts at once, while
     // the other warps prepare the query.
@@ -291,6 +359,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
           }
           if (!ok) break;
           tc_fence_after();
+          // gathered tiles were written by cp.async (the generic proxy); the
+          // MMA reads them through the async proxy
+          if (pl) fence_proxy_async_smem();
           if (t0 < 8) trace_at(a.st, tr, 32 + t0, tr0);
 #pragma unroll 1
           for (int j = 0; j < nt; ++j) {
@@ -334,9 +405,13 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const int grp = warp >= 10 ? 1 : 0;
       const int m = qd * 32 + lane;                 // key of the tile = TMEM lane
       const uint32_t lb = (uint32_t)(qd * 32) << 16;
-      uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+      uint32_t kmin = 0xFFFFFFFFu, kmax = 0u, n_mine = 0u;
       for (int t = grp; t < T; t += 2) {
         const int d = t % kDBuf;
+        // the key's entry (its candidate-list value for a Reindex), read
+        // before the wait so that its latency hides behind it
+        const int i = t * kUTile + m;
+        const int64_t ent = pl ? (i < n_elem ? (int64_t)__ldg(pl + i) : -1) : c0 + i;
         if (!mbar_wait_cta(&bars[BU_DFULL + d], (t / kDBuf) & 1, a.st, abort_p, 15)) break;
         tc_fence_after();
         if (m == 0 && t < 8) trace_at(a.st, tr, 48 + t, tr0);
@@ -361,21 +436,26 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
         const float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         if (m == 0 && t < 8) trace_at(a.st, tr, 1 + t, tr0);
-        const int i = t * kUTile + m;
         if (i < n_elem) {
-          const uint32_t key = score_key(sc);
+          uint32_t key = 0u;   // an empty or out-of-range entry: no key
+          if (ent >= 0 && ent < ncomp) {
+            key = score_key(sc);
+            atomicAdd(&hist[key_bin(key)], 1u);
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
+            ++n_mine;
+            if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + ent] = sc;
+          }
           keys[i] = key;
-          atomicAdd(&hist[key_bin(key)], 1u);
-          kmin = min(kmin, key);
-          kmax = max(kmax, key);
-          if (a.dbg) a.dbg[(int64_t)b * a.n_comp_max + c0 + i] = sc;
         }
       }
       kmin = __reduce_min_sync(0xffffffffu, kmin);
       kmax = __reduce_max_sync(0xffffffffu, kmax);
+      n_mine = __reduce_add_sync(0xffffffffu, n_mine);
       if (lane == 0) {
         atomicMin(&msm.kmin, kmin);
         atomicMax(&msm.kmax, kmax);
+        atomicAdd(&msm.n_real, n_mine);
       }
     }
   }
@@ -385,7 +465,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemU);
   }
-  if (tid == 0) msm.n_real = (uint32_t)n_elem;
   if (tid == 0) trace_at(a.st, tr, 9, tr0);
   if (tr && tid == 0) a.st->pad[24] = T;
   __syncthreads();
@@ -395,10 +474,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
 }
 
 bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
-  // FP4 keys, no pool, 64 heads max, scale rows pair up (even cap), the
-  // 2-D maps' row counts fit in int32.
-  return (a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H) && a.pool == nullptr && a.HI <= 64 &&
-         (a.bt ? a.page % kUTile == 0 : (a.cap % 2) == 0) &&
+  // FP4 keys, 64 heads max, the 2-D maps' row counts fit in int32; streamed
+  // tiles (no pool) also need their scale rows to pair up (even cap) and a
+  // page to hold whole tiles.  A Reindex pool gathers its rows one by one.
+  const bool layout_ok = a.pool != nullptr || (a.bt ? a.page % kUTile == 0 : (a.cap % 2) == 0);
+  return (a.fmt == CKV_FMT_FP4 || a.fmt == CKV_FMT_FP4H) && a.HI <= 64 && layout_ok &&
          batch_rows < (int64_t)1 << 31 && a.chunk % kUTile == 0 && tmap_encode_fn() != nullptr;
 }
 
@@ -410,10 +490,14 @@ cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream
   });
   if (e != cudaSuccess) return e;
   CUtensorMap md, ms;
-  if (!encode_tmap_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kdata, 64, (uint64_t)batch_rows, 64, 64,
-                      (uint32_t)kUTile, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kscale, 16, (uint64_t)(batch_rows / 2), 16,
-                      16, (uint32_t)(kUTile / 2), CU_TENSOR_MAP_SWIZZLE_NONE))
+  memset(&md, 0, sizeof(md));
+  memset(&ms, 0, sizeof(ms));
+  // streamed tiles only: a Reindex pool gathers its rows without the maps
+  if (a.pool == nullptr &&
+      (!encode_tmap_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kdata, 64, (uint64_t)batch_rows, 64, 64,
+                       (uint32_t)kUTile, CU_TENSOR_MAP_SWIZZLE_64B) ||
+       !encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kscale, 16, (uint64_t)(batch_rows / 2), 16,
+                       16, (uint32_t)(kUTile / 2), CU_TENSOR_MAP_SWIZZLE_NONE)))
     return cudaErrorInvalidValue;
   UmmaIndexArgs ua;
   ua.a = a;

@@ -37,13 +37,11 @@
  *     offending access and never trap.  ckv_read_device_status() returns
  *     and clears it.  Calls that overlap on the GPU must use distinct
  *     workspaces.  Host-side, the library is thread-safe and reentrant on
- *     distinct workspaces.  On the GPU, an attention launch is sized to have
- *     all its CTAs resident at once.  When a sequence's CTAs span several
- *     clusters (many sequences, long rows), they meet through a bounded spin
- *     in the workspace.  Two such launches that run at the same time (from
- *     different streams) can each hold SMs the other waits for; the wait then
- *     expires and records CKV_ERR_TIMEOUT instead of hanging.  Check the status
- *     when attention calls of several streams may overlap.  One workspace may serve, one after another, the
+ *     distinct workspaces.  On the GPU no kernel waits for CTAs outside its
+ *     own thread-block cluster: where a sequence's attention spans several
+ *     clusters, the last of its CTAs to finish merges their partials (a
+ *     counter in the workspace), so concurrent launches from several streams
+ *     cannot starve one another.  One workspace may serve, one after another, the
  *     ckv_csa_index_topk, ckv_csa_sparse_attn and ckv_hca_attn calls of a
  *     step that share the batch size B (size it for the largest): the state
  *     each keeps between calls (merge tickets, key histograms, merge

@@ -30,6 +30,9 @@ def _seq_rows(B, n_list, W, seed, spikes=False):
     ("fp4", 448, 64, [640, 1], [128, 128]),
     ("bf16", 448, 128, [0, 3], [0, 0]),          # nothing to attend / three rows
     ("bf16", 448, 128, [8192 + 9], [128]),       # many tiles per pair
+    # twelve sequences of 32+ tiles: pair clusters fit more CTA pairs than one
+    # cluster per sequence, and the last CTA of each half merges
+    ("bf16", 448, 16, [2048] * 11 + [2047], [128] * 11 + [3]),
 ])
 def test_hca_matches_oracle(fmt, blk, H, n_list, win_lens):
     b = ckv()
@@ -113,3 +116,4 @@ def test_csa_out_of_range_index_is_flagged():
     o_ref, l_ref = oa.csa_sparse_attention(np32(q[0]), okv[0][0], None, "bf16", np.array([3, -1, 7]),
                                            owin[0][0], None, 4, TAU)
     check_attention(out[0], None, o_ref, l_ref, H)
+

@@ -106,9 +106,9 @@ def test_index_topk_exact_ties_go_to_lower_index():
 
 @pytest.mark.parametrize("HI2", [64, 40])
 def test_index_pool_and_reindex(HI2):
-    """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool; the
-    Reindex pass scores its short chunks two threads per key (heads split at
-    32), so a head count that is not a multiple of 32 is covered too."""
+    """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool: the
+    Reindex gathers the pool's key rows into the block-scaled scorer, and a
+    head count that is not a multiple of 32 is covered too."""
     b = ckv()
     n = 12000
     keys, qi, w, plane = _case(2, [n, n - 999], 64, "fp4", seed=5)
