@@ -173,11 +173,24 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint32_t a, uint32_t parit
   }
 }
 
+__device__ __forceinline__ bool mbar_test_wait_cta(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A phase that has already completed passes on a non-suspending test; only
+// an open one takes the (suspending) bounded wait.
 __device__ __forceinline__ bool mbar_wait_cta(uint64_t* bar, uint32_t parity, DevStatus* st,
                                               volatile int* abort, int where,
                                               uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cta(a, parity)) return true;
+  if (mbar_test_wait_cta(a, parity)) return true;
   return mbar_wait_slow(a, parity, st, abort, where, limit_ns, 1);
 }
 

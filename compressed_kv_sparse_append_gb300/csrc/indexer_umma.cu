@@ -15,10 +15,15 @@
 //            starting as soon as the previous kernel is done (the other
 //            warps quantise the query meanwhile) -- streamed by TMA, or,
 //            for a pool, gathered row by row with cp.async;
-//   warp 1   TMEM owner and MMA issuer: D[128 keys x 64 heads] (f32, four
-//            buffers, so the MMA runs up to three tiles ahead of the
-//            epilogue) = keys (A, M = 128) x query (B, N = 64), K = 128 in
-//            two block-scaled steps;
+//   warps 1 and 14 MMA issuers, of the even and the odd tiles (warp 1 owns
+//            TMEM): D[128 keys x 64 heads] (f32, four buffers, so the MMA
+//            runs up to three tiles ahead of the epilogue) = keys (A,
+//            M = 128) x query (B, N = 64), K = 128 in two block-scaled steps.
+//            A single issuing thread is a serial chain of waits, descriptor
+//            arithmetic and MMA issues (each tcgen05.mma or commit costs it
+//            tens of cycles); two of them, on different SM sub-partitions
+//            and with disjoint stages, accumulators and barriers, keep the
+//            tensor core fed twice as fast;
 //   warps 6-9 move each tile's key scales into TMEM (lane = key), running
 //            ahead of the MMA by up to the ring depth;
 //   warps 2-5 epilogue: read D back (one key per thread), form
@@ -40,9 +45,9 @@ namespace ckv {
 
 namespace {
 
-// warp 0 TMA, warp 1 MMA, warps 2-5 and 10-13 epilogue (even / odd tiles),
-// warps 6-9 scale movers
-constexpr int kUThreads = 448;
+// warp 0 TMA, warps 1 and 14 MMA (even / odd tiles), warps 2-5 and 10-13
+// epilogue (even / odd tiles), warps 6-9 scale movers
+constexpr int kUThreads = 480;
 constexpr int kUStages = 14;
 constexpr int kUTile = 128;
 constexpr uint32_t kDataBytes = kUTile * 64;                 // 8 KB
@@ -64,6 +69,7 @@ constexpr int kNumBarU = 3 * kUStages + 2 * kDBuf;
 constexpr uint32_t kOffSlotU = kOffBar + kNumBarU * 8;
 constexpr uint32_t kSmemU = kOffSlotU + 16 + 1024;
 static_assert(kOffQ % 1024 == 0, "operand tiles 1024-aligned");
+static_assert(kUStages % 2 == 0 && kDBuf % 2 == 0, "each MMA issuer owns alternate stages and accumulators");
 static_assert(kSmemU <= 232448, "fits in shared memory");
 // The merge's shared-memory scratch: ring, keys and histogram (dead by then).
 constexpr int kMergeScratchWords = (int)((kOffHist + kBins * 4) / 4);
@@ -342,41 +348,35 @@ __global__ void __launch_bounds__(kUThreads, 1)
     tc_fence_after();
     if (tid == 32) trace_at(a.st, tr, 0, tr0);
 
-    if (warp == 1) {
+    if (warp == 1 || warp == 14) {
       // ------------------------------------------------------------ MMA ----
-      // Two tiles per iteration: their waits, one fence, four MMAs.
+      // Issuer `par` takes tiles par, par + 2, ...: their stages (kUStages is
+      // even), accumulators and barriers are its own.
       if (lane == 0) {
+        const int par = warp == 1 ? 0 : 1;
+        // descriptors: the stage and K step only move the start address,
+        // whose field (address >> 4, 14 bits) never carries
+        const uint64_t da0 = smem_desc(base + kOffData, 16, 512, 4);
+        const uint64_t db0 = smem_desc(base + kOffQ, 16, 512, 4);
+        const uint64_t db1 = smem_desc(base + kOffQ + 32, 16, 512, 4);
 #pragma unroll 1
-        for (int t0 = 0; t0 < T; t0 += 2) {
-          const int nt = min(2, T - t0);
-          bool ok = true;
-#pragma unroll 1
-          for (int j = 0; j < nt && ok; ++j) {
-            const int t = t0 + j, s = t % kUStages, d = t % kDBuf;
-            ok = mbar_wait_cta(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12);
-            if (ok && t >= kDBuf)
-              ok = mbar_wait_cta(&bars[BU_DEMPTY + d], ((t / kDBuf) + 1) & 1, a.st, abort_p, 13);
-          }
-          if (!ok) break;
+        for (int t = par; t < T; t += 2) {
+          const int s = t % kUStages, d = t % kDBuf;
+          if (!mbar_wait_cta(&bars[BU_SFA + s], (t / kUStages) & 1, a.st, abort_p, 12)) break;
+          if (t >= kDBuf && !mbar_wait_cta(&bars[BU_DEMPTY + d], ((t / kDBuf) + 1) & 1, a.st, abort_p, 13))
+            break;
           tc_fence_after();
           // gathered tiles were written by cp.async (the generic proxy); the
           // MMA reads them through the async proxy
           if (pl) fence_proxy_async_smem();
-          if (t0 < 8) trace_at(a.st, tr, 32 + t0, tr0);
-#pragma unroll 1
-          for (int j = 0; j < nt; ++j) {
-            const int t = t0 + j, s = t % kUStages, d = t % kDBuf;
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-              const uint64_t da = smem_desc(base + kOffData + s * kDataBytes + ks * 32, 16, 512, 4);
-              const uint64_t db = smem_desc(base + kOffQ + ks * 32, 16, 512, 4);
-              umma_nvf4(tmem + kColD + 64 * d, da, db, kIdescNvf4, tmem + kColSFA + 8 * s + 4 * ks,
-                        tmem + kColSFB + 4 * ks, ks > 0);
-            }
-            umma_commit(&bars[BU_DFULL + d]);
-            umma_commit(&bars[BU_EMPTY + s]);
-          }
-          if (t0 < 8) trace_at(a.st, tr, 13 + t0 / 2, tr0);
+          if (t < 8) trace_at(a.st, tr, 32 + t, tr0);
+          const uint64_t da = da0 + ((s * kDataBytes) >> 4);
+          const uint32_t dt = tmem + kColD + 64 * d, sfa = tmem + kColSFA + 8 * s;
+          umma_nvf4(dt, da, db0, kIdescNvf4, sfa, tmem + kColSFB, 0u);
+          umma_nvf4(dt, da + 2, db1, kIdescNvf4, sfa + 4, tmem + kColSFB + 4, 1u);
+          umma_commit(&bars[BU_DFULL + d]);
+          umma_commit(&bars[BU_EMPTY + s]);
+          if (t < 8) trace_at(a.st, tr, (par ? 56 : 13) + t / 2, tr0);
         }
       }
       __syncwarp();
