@@ -245,14 +245,12 @@ __device__ __forceinline__ Tile tile_of(int t, int nt_main, int n_sel, int n_win
   return r;
 }
 
-// Asynchronous global -> shared copies (cp.async): 4-byte MIXED scale
-// words, and the 16-byte chunks of gathered quantised rows.
+// Asynchronous 4-byte global -> shared copies (cp.async) for the MIXED
+// scale words (the 16-byte chunks of gathered quantised rows use cp_async16).
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

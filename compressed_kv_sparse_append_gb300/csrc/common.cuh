@@ -254,8 +254,12 @@ __device__ __forceinline__ void trace_at(DevStatus* st, bool on, int slot, long 
   if (on) trace_at_store(st, slot, t0);
 }
 
-// Asynchronous 4-byte copy global -> shared (cp.async, cached in L1; the
-// caller waits with cp.async.wait_all / wait_group).
+// Asynchronous global -> shared copies (cp.async): 16 bytes through L2
+// only, or 4 bytes cached in L1; the caller waits with cp.async.wait_all /
+// wait_group.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async4_ca(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }

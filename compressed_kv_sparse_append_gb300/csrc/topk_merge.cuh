@@ -34,7 +34,7 @@ template <int NT>
 struct MergeSmem {
   SelectSmem<NT> sel;
   uint32_t cprefix[kMaxChunksPerSeq + 1];   // merge: candidate offsets of the chunks
-  uint32_t sprefix[kMaxChunksPerSeq + 1];   // merge: survivor offsets of the chunks
+  uint32_t sprefix[kMaxChunksPerSeq + 1];   // merge: 4-aligned staging offsets of the chunks
   uint32_t wcnt[NT / 32];                   // per-warp counts of an ordered compaction
   uint32_t sub[256];                        // merge: next 8 key bits within the threshold bin
   int ticket;
@@ -189,7 +189,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   {
     constexpr int kPer = (kMaxChunksPerSeq + NT - 1) / NT;
     const int c0 = min(nch, (int)threadIdx.x * kPer), c1 = min(nch, c0 + kPer);
-    uint32_t cnt[kPer], real = 0, mine = 0;
+    uint32_t cnt[kPer], real = 0, mine = 0, mine4 = 0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       cnt[k] = 0u;
@@ -198,21 +198,29 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
         cnt[k] = v.x;
         real += v.y;
         mine += v.x;
+        mine4 += (v.x + 3u) & ~3u;
       }
     }
-    uint32_t before, rb, tot, rt;
-    block_scan2<NT>(mine, real, before, rb, tot, rt, sm.sel);
+    uint32_t before, before4, tot, tot4, d0, rt;
+    block_scan2<NT>(mine, mine4, before, before4, tot, tot4, sm.sel);
+    block_scan2<NT>(real, 0u, d0, d0, rt, d0, sm.sel);
     n_total = rt;
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
       if (c0 + k < c1) {
         sm.cprefix[c0 + k] = before;
+        sm.sprefix[c0 + k] = before4;
         before += cnt[k];
+        before4 += (cnt[k] + 3u) & ~3u;
       }
-    if (threadIdx.x == 0) sm.cprefix[nch] = tot;
+    if (threadIdx.x == 0) {
+      sm.cprefix[nch] = tot;
+      sm.sprefix[nch] = tot4;
+    }
     __syncthreads();
   }
   const int n_cand = (int)sm.cprefix[nch];
+  const int n_pad = (int)sm.sprefix[nch];   // staged length: chunk lists padded to 4 entries
   const int keff = min(K, (int)n_total);
   // threshold bin and the count above it (every key is a survivor when the
   // sequence has at most K)
@@ -243,12 +251,13 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   trace_at(a.st, tr, 20, t0);
 
   // Every candidate into shared memory, in entry order (chunk c's list at
-  // offset cprefix[c]): one warp per chunk list, 4-byte asynchronous copies,
-  // all of them in flight at once.  Then the keys of the threshold bin are
-  // counted by their next 8 bits.
+  // offset sprefix[c], padded to a multiple of 4 entries whose padding keys
+  // are 0, i.e. no key): one warp per chunk list, 16-byte asynchronous
+  // copies, all of them in flight at once.  Then the keys of the threshold
+  // bin are counted by their next 8 bits.
   constexpr int kWarps = NT / 32;
   const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
-  const int surv_cap = (scratch_words - pool_words - kWarps * 256) / 2;
+  const int surv_cap = ((scratch_words - pool_words - kWarps * 256) / 2) & ~3;
   uint32_t* surv_key = scratch;
   int32_t* surv_ent = reinterpret_cast<int32_t*>(scratch + surv_cap);
   uint32_t* wsub = scratch + 2 * surv_cap;            // [warp][256] private sub-bin counts
@@ -267,24 +276,33 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     sm.bcast[0] = 0u;   // sub-bin search defaults
     sm.bcast[1] = 0u;
   }
-  const bool staged = n_cand <= surv_cap;
+  const bool staged = n_pad <= surv_cap;
   if (staged) {
+    // (the chunk lists start 16-byte aligned in global memory: a.chunk is a
+    // multiple of 4; reading up to 3 slots past a list stays in its chunk)
+    int pad_at = -1, pad_n = 0;   // the padding keys this lane's last copy wrote
 #pragma unroll 1
     for (int c = warp; c < nch; c += kWarps) {
       const int cnt = (int)(sm.cprefix[c + 1] - sm.cprefix[c]);
+      const int groups = (cnt + 3) >> 2;
       const uint32_t* gk = cl.gk + (int64_t)c * a.chunk;
       const int32_t* gi = cl.gi + (int64_t)c * a.chunk;
-      const uint32_t dk = smem_u32(surv_key + sm.cprefix[c]), de = smem_u32(surv_ent + sm.cprefix[c]);
+      const uint32_t dk = smem_u32(surv_key + sm.sprefix[c]), de = smem_u32(surv_ent + sm.sprefix[c]);
 #pragma unroll 1
-      for (int i = lane; i < cnt; i += 32) {
-        cp_async4_ca(dk + 4 * i, gk + i);
-        cp_async4_ca(de + 4 * i, gi + i);
+      for (int g = lane; g < groups; g += 32) {
+        cp_async16(dk + 16 * g, gk + 4 * g);
+        cp_async16(de + 16 * g, gi + 4 * g);
+        if (g == groups - 1 && (cnt & 3)) {
+          pad_at = (int)sm.sprefix[c] + cnt;
+          pad_n = 4 - (cnt & 3);
+        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    for (int k = 0; k < pad_n; ++k) surv_key[pad_at + k] = 0u;   // after this lane's own copy
   }
   __syncthreads();
-  uint32_t n_surv = (uint32_t)n_cand;
+  uint32_t n_surv = (uint32_t)n_pad;
   if (tr) a.st->pad[17] = (int32_t)(clock64() - t0);
   if (hint && staged) {
     // warp-private counters (no contention between warps on the few
@@ -292,12 +310,12 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     // plain shared atomics (match.any aggregation measured far slower)
     uint32_t* ws = wsub + warp * 256;
 #pragma unroll 1
-    for (int base = warp * 32; base < n_cand; base += 4 * NT) {
+    for (int base = warp * 32; base < n_pad; base += 4 * NT) {
       uint32_t d[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int i = base + q * NT + lane;
-        const uint32_t u = i < n_cand ? surv_key[i] : 0u;
+        const uint32_t u = i < n_pad ? surv_key[i] : 0u;
         d[q] = key_bin(u) == tb && u != 0u ? ((u >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
       }
 #pragma unroll
@@ -360,9 +378,11 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     above2 = above + sm.bcast[1];
     prefix = lo_key | (t2 << (kBinShift - 8));
     top_bits = kBinShift - 8;
-    // in-place ordered compaction to the keys >= prefix, kU per thread per
-    // round (a round's reads all happen before its writes, which never reach
-    // past it)
+  }
+  if (staged && (hint || n_pad != n_cand)) {
+    // in-place ordered compaction to the real keys >= prefix (without a
+    // hint prefix is 0: only the padding goes), kU per thread per round (a
+    // round's reads all happen before its writes, which never reach past it)
     constexpr int kU = 8;
     uint32_t kept = 0;
 #pragma unroll 1
