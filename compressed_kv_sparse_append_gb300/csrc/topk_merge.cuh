@@ -279,8 +279,8 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   const bool staged = n_pad <= surv_cap;
   if (staged) {
     // (the chunk lists start 16-byte aligned in global memory: a.chunk is a
-    // multiple of 4; reading up to 3 slots past a list stays in its chunk)
-    int pad_at = -1, pad_n = 0;   // the padding keys this lane's last copy wrote
+    // multiple of 4; reading up to 3 slots past a list stays in its chunk,
+    // and those slots hold whatever an earlier call left there)
 #pragma unroll 1
     for (int c = warp; c < nch; c += kWarps) {
       const int cnt = (int)(sm.cprefix[c + 1] - sm.cprefix[c]);
@@ -292,14 +292,15 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       for (int g = lane; g < groups; g += 32) {
         cp_async16(dk + 16 * g, gk + 4 * g);
         cp_async16(de + 16 * g, gi + 4 * g);
-        if (g == groups - 1 && (cnt & 3)) {
-          pad_at = (int)sm.sprefix[c] + cnt;
-          pad_n = 4 - (cnt & 3);
-        }
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    for (int k = 0; k < pad_n; ++k) surv_key[pad_at + k] = 0u;   // after this lane's own copy
+    __syncthreads();   // every copy has landed
+    // the padding slots of every list become "no key"
+    for (int c = threadIdx.x; c < nch; c += NT) {
+      const int cnt = (int)(sm.cprefix[c + 1] - sm.cprefix[c]);
+      for (int k = cnt; k < ((cnt + 3) & ~3); ++k) surv_key[sm.sprefix[c] + k] = 0u;
+    }
   }
   __syncthreads();
   uint32_t n_surv = (uint32_t)n_pad;

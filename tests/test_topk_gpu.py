@@ -170,3 +170,32 @@ def test_index_all_equal_scores_take_the_lowest_entries(fmt, HI, n, topk, pool_o
         assert np.array_equal(idx, np.arange(topk))
         if pool_out:
             assert np.array_equal(res[1].cpu().numpy()[0], np.arange(pool_out))
+
+
+def test_index_reused_workspace_ignores_earlier_candidates():
+    """One workspace, two Reindex calls over 32 pool chunks of 256 entries.
+    The first (every pool entry valid, scores 1000x larger) leaves large keys
+    in every candidate slot.  In the second, chunk j ends in 1 + j % 3 empty
+    (-1) entries: every chunk's list (all its valid keys: each chunk holds
+    fewer than top-k) has a length that is not a multiple of 4 and ends on
+    the same lane, and 32 lists are more than the merge has warps, so one
+    lane stages the last group of several lists.  The earlier call's keys in
+    the slots past each list must not count."""
+    b = ckv()
+    n = 20000
+    keys, qi, w, plane = _case(1, [n], 64, "fp4", seed=21)
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    P = 32 * 256
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, 64, n, 512, 0) +
+                         b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, 64, n, 512, P))
+    pool1 = torch.arange(P, dtype=torch.int32, device="cuda").view(1, P)
+    b.csa_index_topk(plane, n_comp, n, qi, w * 1000.0, 512, pool=pool1, ws=ws)
+    pool2 = (torch.arange(P, dtype=torch.int32) * 2 + 1).view(32, 256)
+    for j in range(32):
+        pool2[j, 256 - (1 + j % 3):] = -1
+    pool2 = pool2.reshape(1, P).cuda()
+    idx = b.csa_index_topk(plane, n_comp, n, qi, w, 512, pool=pool2, ws=ws)
+    assert b.read_device_status(ws) == 0
+    sc, eps = _oracle_scores(keys[0], qi[0], w[0], "fp4")
+    cand = pool2.cpu().numpy()[0]
+    assert check_topk(idx.cpu().numpy()[0], sc, eps, 512, candidates=cand, where="reused workspace") == 0
