@@ -35,11 +35,11 @@ METRIC = "decode attn layer-steps/s at 128k/1M ctx; achieved HBM GB/s vs ~8 TB/s
 UNIT = "layer-steps/s"
 ALL_SOURCES = ["append.cu", "indexer.cu", "indexer_umma.cu", "attention.cu", "api.cu",
                "common.cuh", "select.cuh", "topk_merge.cuh", "indexer.cuh", "attention.cuh",
-               "tmap.cuh", "rope.cuh", "hadamard.cuh"]
+               "tmap.cuh", "hadamard.cuh"]
 # The sources that decide each library call's kernels and their DRAM traffic
 # (the kernel code, the headers it includes, the host code that sizes the
 # launch).  Keyed by the call's tag in a step's call list.
-_ATTN = ["attention.cu", "attention.cuh", "common.cuh", "tmap.cuh", "rope.cuh", "api.cu"]
+_ATTN = ["attention.cu", "attention.cuh", "common.cuh", "tmap.cuh", "api.cu"]
 KERNEL_SOURCES = {
     "csa_index_topk": ["indexer_umma.cu", "indexer.cu", "topk_merge.cuh", "select.cuh",
                        "indexer.cuh", "common.cuh", "tmap.cuh", "hadamard.cuh", "api.cu"],
