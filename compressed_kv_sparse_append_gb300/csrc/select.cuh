@@ -11,8 +11,9 @@
 //
 // This code runs once per CTA (the chunk's candidates) or once per sequence
 // (the merge), so it executes with a cold instruction cache: it takes its keys
-// from a run-time source, its loops are not unrolled, and each kernel calls it
-// from one place, so that little code has to be fetched.
+// from a run-time source and its loops handle one element per iteration, so
+// that little code has to be fetched (unrolling them for more loads in flight
+// made the merge slower: its time is mostly barriers and code fetch).
 #pragma once
 
 #include "common.cuh"
@@ -123,16 +124,12 @@ __device__ __forceinline__ void block_radix_threshold(const SelSrc src, int n, i
   const uint32_t mask0 = top0 >= 32 ? 0u : (0xFFFFFFFFu << top0);
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll 1
-  for (int i0 = threadIdx.x; i0 < n; i0 += 4 * NT) {
-    uint32_t u[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) u[q] = i0 + q * NT < n ? src.k(i0 + q * NT) : 0u;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (i0 + q * NT < n && ((u[q] ^ prefix0) & mask0) == 0u) {
-        lo = min(lo, u[q]);
-        hi = max(hi, u[q]);
-      }
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t u = src.k(i);
+    if (((u ^ prefix0) & mask0) == 0u) {
+      lo = min(lo, u);
+      hi = max(hi, u);
+    }
   }
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
@@ -173,16 +170,12 @@ __device__ __forceinline__ void block_radix_threshold(const SelSrc src, int n, i
     const int width = top < 8 ? top : 8, shift = top - width;
     const uint32_t mask = top == 32 ? 0u : (0xFFFFFFFFu << top);   // settled bits
     const uint32_t dmask = (1u << width) - 1u;
-    // four independent elements per thread per iteration (plain shared
-    // atomics: warp-aggregating them with match.any measured far slower)
+    // plain shared atomics (warp-aggregating them with match.any measured
+    // far slower)
 #pragma unroll 1
-    for (int i0 = threadIdx.x; i0 < n; i0 += 4 * NT) {
-      uint32_t u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = i0 + q * NT < n ? src.k(i0 + q * NT) : 0u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (i0 + q * NT < n && ((u[q] ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u[q] >> shift) & dmask], 1u);
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const uint32_t u = src.k(i);
+      if (((u ^ prefix) & mask) == 0) atomicAdd(&sm.hist[(u >> shift) & dmask], 1u);
     }
     __syncthreads();
     if (warp == 0) {
@@ -244,15 +237,10 @@ __device__ __forceinline__ int select_ordered(const SelSrc src, int n, int K, ui
   uint32_t gt = 0, eq = 0;
   if (!all) {
 #pragma unroll 1
-    for (int i = i0; i < i1; i += 4) {
-      uint32_t u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = i + q < i1 ? src.k(i + q) : 0u;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        gt += (i + q < i1) && u[q] > T;
-        eq += (i + q < i1) && u[q] == T;
-      }
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t u = src.k(i);
+      gt += u > T;
+      eq += u == T;
     }
   } else {
     gt = (uint32_t)(i1 - i0);

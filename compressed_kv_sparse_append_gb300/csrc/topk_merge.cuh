@@ -311,17 +311,9 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     // plain shared atomics (match.any aggregation measured far slower)
     uint32_t* ws = wsub + warp * 256;
 #pragma unroll 1
-    for (int base = warp * 32; base < n_pad; base += 4 * NT) {
-      uint32_t d[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = base + q * NT + lane;
-        const uint32_t u = i < n_pad ? surv_key[i] : 0u;
-        d[q] = key_bin(u) == tb && u != 0u ? ((u >> (kBinShift - 8)) & 255u) : 0xFFFFFFFFu;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (d[q] != 0xFFFFFFFFu) atomicAdd(&ws[d[q]], 1u);
+    for (int i = threadIdx.x; i < n_pad; i += NT) {
+      const uint32_t u = surv_key[i];
+      if (key_bin(u) == tb && u != 0u) atomicAdd(&ws[(u >> (kBinShift - 8)) & 255u], 1u);
     }
     __syncthreads();
     for (int v = threadIdx.x; v < 256; v += NT) {
