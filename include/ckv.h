@@ -257,7 +257,10 @@ ckv_status ckv_read_static_status(void *stream);
  *   kv, win  [host] main-KV and window planes of the same format (dim 512).
  *   win_len  [B] int32: valid window slots [0, win_len[b]) (<= win->cap).
  *   idx      [B][topk] int32 entries of kv (-1 = none; >= kv->cap is skipped
- *            and records CKV_ERR_DEVICE_BOUNDS).
+ *            and records CKV_ERR_DEVICE_BOUNDS).  The call has no n_comp: an
+ *            entry below kv->cap is attended as whatever its slot holds, so
+ *            callers pass entries that have been written (the output of
+ *            ckv_csa_index_topk only names entries below its n_comp).
  *   q_bf16   [B][H][512] bf16, H <= 128.
  *   out_bf16 [B][H][512] bf16; lse NULL or [B][H] f32 (natural log; -inf when
  *            there is no row to attend, with o = 0). */
