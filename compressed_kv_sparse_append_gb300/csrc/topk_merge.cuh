@@ -163,6 +163,11 @@ __device__ void emit_outputs(const IndexArgs& a, int b, SelSrc src, int n, int n
   for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
 }
 
+// Staged candidate sets up to this size go straight to one exact select:
+// below it the select's fixed cost is lower than the threshold-bin search,
+// the sub-bin count and the compaction it would save.
+constexpr int kDirectSelectMax = 4096;
+
 // Merge of the sequence's candidates, run by its last CTA.  `scratch`
 // (scratch_words 32-bit words of shared memory, dead otherwise) holds the
 // survivors and, for a CSA2 Full layer, the pool.
@@ -222,10 +227,16 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   const int n_cand = (int)sm.cprefix[nch];
   const int n_pad = (int)sm.sprefix[nch];   // staged length: chunk lists padded to 4 entries
   const int keff = min(K, (int)n_total);
+  constexpr int kWarps = NT / 32;
+  const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
+  const int surv_cap = ((scratch_words - pool_words - kWarps * 256) / 2) & ~3;
+  // A small staged set needs no threshold bin: the select runs on all of it
+  // (its K never exceeds the real keys, so the padding, key 0, is never taken).
+  const bool direct = n_pad <= kDirectSelectMax && n_pad <= surv_cap;
   // threshold bin and the count above it (every key is a survivor when the
   // sequence has at most K)
   uint32_t tb = 0, above = 0;
-  if (keff > 0 && (int)n_total > K) {
+  if (!direct && keff > 0 && (int)n_total > K) {
     bool done = false;
     if (own_bound > 0 && top <= (int)own_bound + NT) {
       uint32_t before, d0, tot, d1;
@@ -255,9 +266,6 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   // are 0, i.e. no key): one warp per chunk list, 16-byte asynchronous
   // copies, all of them in flight at once.  Then the keys of the threshold
   // bin are counted by their next 8 bits.
-  constexpr int kWarps = NT / 32;
-  const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
-  const int surv_cap = ((scratch_words - pool_words - kWarps * 256) / 2) & ~3;
   uint32_t* surv_key = scratch;
   int32_t* surv_ent = reinterpret_cast<int32_t*>(scratch + surv_cap);
   uint32_t* wsub = scratch + 2 * surv_cap;            // [warp][256] private sub-bin counts
@@ -270,7 +278,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   cl.n_chunks = nch;
   cl.stride = a.chunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool hint = (int)n_total > K && keff > 0;
+  const bool hint = !direct && (int)n_total > K && keff > 0;
   for (int i = threadIdx.x; i < kWarps * 256; i += NT) wsub[i] = 0u;
   if (threadIdx.x == 0) {
     sm.bcast[0] = 0u;   // sub-bin search defaults
@@ -372,7 +380,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     prefix = lo_key | (t2 << (kBinShift - 8));
     top_bits = kBinShift - 8;
   }
-  if (staged && (hint || n_pad != n_cand)) {
+  if (staged && !direct && (hint || n_pad != n_cand)) {
     // in-place ordered compaction to the real keys >= prefix (without a
     // hint prefix is 0: only the padding goes), kU per thread per round (a
     // round's reads all happen before its writes, which never reach past it)
