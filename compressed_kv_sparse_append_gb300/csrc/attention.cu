@@ -298,10 +298,14 @@ struct Raw {
 };
 
 // Dequantise a loaded chunk to bf16 and store it at row `r` of the swizzled
-// tile (an empty row stores zeros: its raw bytes and scale are zero).
+// tile (an empty row stores zeros: its raw bytes and scale are zero).  Out of
+// line, the chunk passed in registers: the producers' unrolled chunk loop
+// then holds one copy of the conversion, which matters when the kernel starts
+// with its code evicted from the instruction caches (in a decode step the
+// index kernel runs just before): 2 us less per step at 128 k and 1 M.
 template <int FMT>
-__device__ __forceinline__ void store_chunk(const AttnArgs& a, uint32_t tile, int r, int q,
-                                            const Raw& raw, int half) {
+__device__ __noinline__ void store_chunk(const AttnArgs& a, uint32_t tile, int r, int q,
+                                        const Raw raw, int half) {
   if constexpr (FMT == CKV_FMT_BF16) {
     const int d0 = q * 8;
     st_shared_v4(sw128(tile + (d0 >> 6) * 8192, r, (d0 & 63) >> 3), raw.v);
