@@ -486,21 +486,21 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   auto send_scores = [&](int k, int hq) {
     const uint32_t tS = tmem + kColS + 64 * (k & 1) + ((uint32_t)(hq & ~31) << 16);
     const uint32_t xrow_peer = mapa(base + kOffX + (k % kXBufs) * kXBytes + hq * 128, peer);
-#pragma unroll
+#pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t sr[32];
       tmem_ld32(tS + 32 * hh, sr);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 4 * hh; c < 4 * hh + 4; ++c) {
+      for (int i = 0; i < 4; ++i) {
         uint32_t w4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = 8 * (c - 4 * hh) + 2 * u;
+          const int j = 8 * i + 2 * u;
           __half2 hv = __floats2half2_rn(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1]));
           w4[u] = *reinterpret_cast<uint32_t*>(&hv);
         }
-        st_cluster_u4(xrow_peer + ((c ^ (hq & 7)) << 4), make_uint4(w4[0], w4[1], w4[2], w4[3]));
+        st_cluster_u4(xrow_peer + (((4 * hh + i) ^ (hq & 7)) << 4), make_uint4(w4[0], w4[1], w4[2], w4[3]));
       }
     }
   };
