@@ -36,6 +36,7 @@ struct MergeSmem {
   uint32_t cprefix[kMaxChunksPerSeq + 1];   // merge: candidate offsets of the chunks
   uint32_t sprefix[kMaxChunksPerSeq + 1];   // merge: 4-aligned staging offsets of the chunks
   uint32_t wcnt[NT / 32];                   // per-warp counts of an ordered compaction
+  uint32_t wcnt2[NT / 32];                  // second per-warp counts (keys equal to the threshold)
   uint32_t sub[256];                        // merge: next 8 key bits within the threshold bin
   int ticket;
   uint32_t n_real;                          // real keys of this chunk
@@ -163,10 +164,84 @@ __device__ void emit_outputs(const IndexArgs& a, int b, SelSrc src, int n, int n
   for (int i = kk + threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
 }
 
-// Staged candidate sets up to this size go straight to one exact select:
-// below it the select's fixed cost is lower than the threshold-bin search,
-// the sub-bin count and the compaction it would save.
+// Writes, in array order, every element of key[0, n) above T and the first
+// `need` equal to T (the top-K once T and need are those of its K-th largest
+// key): output position = (keys > T before it) + min(keys == T before it,
+// need).  Rounds of NT x 8 elements, each lane's eight in flight; one ballot
+// pair per 32 elements and one barrier per round.  Block-wide.
+template <int NT>
+__device__ __forceinline__ void emit_ordered(const uint32_t* key, const int32_t* ent, int n, uint32_t T,
+                                             uint32_t need, int32_t* out, MergeSmem<NT>& sm) {
+  constexpr int kU = 8, kWarps = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t g_run = 0, e_run = 0;   // keys > T and == T in earlier rounds
+#pragma unroll 1
+  for (int base = 0; base < n; base += NT * kU) {
+    const int wbase = base + warp * 32 * kU;
+    uint32_t bg[kU], be[kU], cg = 0, ce = 0;
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int v = wbase + k * 32 + lane;
+      const uint32_t u = v < n ? key[v] : 0u;
+      bg[k] = __ballot_sync(0xffffffffu, u > T);
+      be[k] = __ballot_sync(0xffffffffu, u == T && u != 0u);
+      cg += __popc(bg[k]);
+      ce += __popc(be[k]);
+    }
+    if (lane == 0) {
+      sm.wcnt[warp] = cg;
+      sm.wcnt2[warp] = ce;
+    }
+    __syncthreads();
+    // every warp scans the warps' counts: its exclusive prefix and the totals
+    const uint32_t xg = lane < kWarps ? sm.wcnt[lane] : 0u, xe = lane < kWarps ? sm.wcnt2[lane] : 0u;
+    uint32_t ig = xg, ie = xe;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, ig, o), ye = __shfl_up_sync(0xffffffffu, ie, o);
+      if (lane >= o) {
+        ig += yg;
+        ie += ye;
+      }
+    }
+    uint32_t g = g_run + __shfl_sync(0xffffffffu, ig - xg, warp);
+    uint32_t e = e_run + __shfl_sync(0xffffffffu, ie - xe, warp);
+    g_run += __shfl_sync(0xffffffffu, ig, kWarps - 1);
+    e_run += __shfl_sync(0xffffffffu, ie, kWarps - 1);
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int v = wbase + k * 32 + lane;
+      const uint32_t gb = g + __popc(bg[k] & lt), eb = e + __popc(be[k] & lt);
+      if ((bg[k] >> lane) & 1u) out[gb + min(eb, need)] = ent[v];
+      else if (((be[k] >> lane) & 1u) && eb < need) out[gb + eb] = ent[v];
+      g += __popc(bg[k]);
+      e += __popc(be[k]);
+    }
+    __syncthreads();   // wcnt is written again by the next round
+  }
+}
+
+// Staged candidate sets of a pool-building call up to this size go straight
+// to one exact select (the pool and then the top-k of the pool).
 constexpr int kDirectSelectMax = 4096;
+
+// Leaves the sequence's histogram (bins in use: below seq[1] = top, from
+// kBins - seq[2] up) and its state words zero for the next call.  Block-wide.
+template <int NT>
+__device__ __forceinline__ void clear_sequence_state(uint32_t* gh, uint32_t* seq, int top) {
+  const int bot = kBins - (int)__ldcg(seq + 2);
+  if (top > 0) {
+    const int z0 = bot & ~3, z1 = (top + 3) & ~3;
+    for (int v = z0 / 4 + (int)threadIdx.x; v < z1 / 4; v += NT)
+      reinterpret_cast<uint4*>(gh)[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (threadIdx.x == 0) {
+    seq[1] = 0u;
+    seq[2] = 0u;
+    seq[0] = 0u;
+  }
+}
 
 // Merge of the sequence's candidates, run by its last CTA.  `scratch`
 // (scratch_words 32-bit words of shared memory, dead otherwise) holds the
@@ -230,9 +305,11 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   constexpr int kWarps = NT / 32;
   const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
   const int surv_cap = ((scratch_words - pool_words - kWarps * 256) / 2) & ~3;
-  // A small staged set needs no threshold bin: the select runs on all of it
-  // (its K never exceeds the real keys, so the padding, key 0, is never taken).
-  const bool direct = n_pad <= kDirectSelectMax && n_pad <= surv_cap;
+  // A small staged set of a pool-building call needs no threshold bin: the
+  // select runs on all of it (its K never exceeds the real keys, so the
+  // padding, key 0, is never taken).  Other staged sets take the threshold
+  // bin and its sub-bin, whose keys decide the threshold on their own.
+  const bool direct = a.pool_out > 0 && n_pad <= kDirectSelectMax && n_pad <= surv_cap;
   // threshold bin and the count above it (every key is a survivor when the
   // sequence has at most K)
   uint32_t tb = 0, above = 0;
@@ -380,6 +457,102 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     prefix = lo_key | (t2 << (kBinShift - 8));
     top_bits = kBinShift - 8;
   }
+  if (hint && staged && a.pool_out == 0) {
+    // The keys of the sub-bin holding the keff-th largest (with their staged
+    // positions) into a list in the dead sub-bin counters; the threshold T
+    // and the count `need` of keys equal to T to keep are found on the list
+    // alone (every key above the sub-bin is kept), then one ordered pass over
+    // the staged candidates writes the output.
+    constexpr int kListMax = 2 * NT;   // 2 x kListMax words fit in wsub
+    constexpr int kRankMax = 64;
+    uint32_t* lkey = wsub;
+    uint32_t* lpos = wsub + kListMax;
+    if (threadIdx.x == 0) sm.bcast[2] = 0u;
+    __syncthreads();
+    const uint32_t hmask = ~((1u << top_bits) - 1u);
+    {
+      // eight keys per lane in flight, one counter update per warp and round
+      constexpr int kU = 8;
+      const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+      for (int w0 = warp * 32 * kU; w0 < n_pad; w0 += NT * kU) {
+        uint32_t u[kU], bal[kU], c = 0;
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = w0 + k * 32 + lane;
+          u[k] = i < n_pad ? surv_key[i] : 0u;
+          bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && (u[k] & hmask) == prefix);
+          c += __popc(bal[k]);
+        }
+        if (c == 0u) continue;   // warp-uniform
+        uint32_t at = 0u;
+        if (lane == 0) at = atomicAdd(&sm.bcast[2], c);
+        at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const uint32_t x = at + __popc(bal[k] & lt);
+          if (((bal[k] >> lane) & 1u) && x < (uint32_t)kListMax) {
+            lkey[x] = u[k];
+            lpos[x] = (uint32_t)(w0 + k * 32 + lane);
+          }
+          at += __popc(bal[k]);
+        }
+      }
+    }
+    __syncthreads();
+    const int m = (int)sm.bcast[2];
+    if (m <= kListMax) {
+      const uint32_t need2 = (uint32_t)keff - above2;   // in [1, m] by the sub-bin search
+      uint32_t T = 0, need = 0;
+      if (m <= kRankMax) {
+        // rank of each list key: larger keys first, equal keys by position;
+        // the key of rank need2 - 1 is T (m^2 comparisons: short lists only)
+        if ((int)threadIdx.x < m) {
+          const uint32_t u = lkey[threadIdx.x], ps = lpos[threadIdx.x];
+          uint32_t r = 0, gt = 0;
+          auto rank_one = [&](uint32_t uj, uint32_t pj) {
+            gt += uj > u;
+            r += uj > u || (uj == u && pj < ps);
+          };
+          // four list entries per 16-byte load (the list starts 16-byte
+          // aligned), several loads in flight
+          const int m4 = m & ~3;
+#pragma unroll 4
+          for (int j = 0; j < m4; j += 4) {
+            const uint4 kq = *reinterpret_cast<const uint4*>(lkey + j);
+            const uint4 pq = *reinterpret_cast<const uint4*>(lpos + j);
+            rank_one(kq.x, pq.x);
+            rank_one(kq.y, pq.y);
+            rank_one(kq.z, pq.z);
+            rank_one(kq.w, pq.w);
+          }
+#pragma unroll 1
+          for (int j = m4; j < m; ++j) rank_one(lkey[j], lpos[j]);
+          if (r == need2 - 1u) {
+            sm.bcast[0] = u;
+            sm.bcast[1] = need2 - gt;
+          }
+        }
+        __syncthreads();
+        T = sm.bcast[0];
+        need = sm.bcast[1];
+        __syncthreads();
+      } else {
+        SelSrc ls{};
+        ls.key = lkey;
+        block_radix_threshold<NT>(ls, m, (int)need2, sm.sel, T, need, prefix, top_bits);
+      }
+      trace_at(a.st, tr, 19, t0);
+      if (tr) a.st->pad[31] = m;
+      int32_t* oi = a.out_idx + (int64_t)b * a.topk;
+      emit_ordered<NT>(surv_key, surv_ent, n_pad, T, need, oi, sm);
+#pragma unroll 1
+      for (int i = keff + (int)threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
+      trace_at(a.st, tr, 22, t0);
+      clear_sequence_state<NT>(gh, seq, top);
+      return;
+    }
+  }
   if (staged && !direct && (hint || n_pad != n_cand)) {
     // in-place ordered compaction to the real keys >= prefix (without a
     // hint prefix is 0: only the padding goes), kU per thread per round (a
@@ -440,18 +613,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
                      hint ? kBinShift : 32, hint ? (int)above : 0);
   }
   trace_at(a.st, tr, 22, t0);
-  // leave the sequence's histogram and state zero for the next call
-  const int bot = kBins - (int)__ldcg(seq + 2);
-  if (top > 0) {
-    const int z0 = bot & ~3, z1 = (top + 3) & ~3;
-    for (int v = z0 / 4 + (int)threadIdx.x; v < z1 / 4; v += NT)
-      reinterpret_cast<uint4*>(gh)[v] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (threadIdx.x == 0) {
-    seq[1] = 0u;
-    seq[2] = 0u;
-    seq[0] = 0u;
-  }
+  clear_sequence_state<NT>(gh, seq, top);
 }
 
 // After scoring: `keys[0, n_elem)` hold this chunk's keys (0 = no entry),
