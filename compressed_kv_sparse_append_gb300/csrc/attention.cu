@@ -144,68 +144,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 constexpr int64_t kPart16 = 2 * kPartFloats / 4;   // 16-byte stride between pairs' partials
 
-// Combines the G partials of one half over units [u0, u1) of 8 columns x 128
-// head rows with the weights in `wsm`; each pass keeps 16 / GMAX items x G
-// loads of 16 bytes in flight per thread.
-//
-// rtab (null: none): (cos, sin) of the 32 rope pairs; the units holding the
-// last 64 latent dims (units 24..31 of half 1) are turned by the opposite
-// angle before they are stored (the output's RoPE at position -i).
-template <int GMAX>
-__device__ __noinline__ void merge_items(const uint4* pq0, const float* wsm, int G, int H,
-                                            __nv_bfloat16* out, int tid, int u0, int u1,
-                                            const float2* rtab) {
-  constexpr int kItems = 16 / GMAX;
-  const int n_items = (u1 - u0) * H;   // only the H real head rows
-#pragma unroll 1
-  for (int k0 = tid; k0 < n_items; k0 += kItems * kThreadsAttn) {
-    uint4 v[kItems][GMAX];
-#pragma unroll
-    for (int t = 0; t < kItems; ++t) {
-      const int k = k0 + t * kThreadsAttn, uu = u0 + k / H, hh = k - (uu - u0) * H;
-#pragma unroll
-      for (int q = 0; q < GMAX; ++q)
-        v[t][q] = (k < n_items && q < G) ? __ldcg(pq0 + q * kPart16 + uu * 128 + hh)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int t = 0; t < kItems; ++t) {
-      const int k = k0 + t * kThreadsAttn, uu = u0 + k / H, hh = k - (uu - u0) * H;
-      if (k >= n_items) continue;
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-      for (int q = 0; q < GMAX; ++q) {
-        if (q < G) {
-          const float wq = wsm[q * 128 + hh];
-          const uint32_t w[4] = {v[t][q].x, v[t][q].y, v[t][q].z, v[t][q].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-            acc[2 * e] += wq * f.x;
-            acc[2 * e + 1] += wq * f.y;
-          }
-        }
-      }
-      if (rtab && uu >= 24) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 cs = rtab[4 * (uu - 24) + e];
-          const float re = acc[2 * e], im = acc[2 * e + 1];
-          acc[2 * e] = re * cs.x + im * cs.y;
-          acc[2 * e + 1] = im * cs.x - re * cs.y;
-        }
-      }
-      uint4 o;
-      o.x = pack_bf16(acc[0], acc[1]);
-      o.y = pack_bf16(acc[2], acc[3]);
-      o.z = pack_bf16(acc[4], acc[5]);
-      o.w = pack_bf16(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(out + (int64_t)hh * 512 + 8 * uu) = o;
-    }
-  }
-}
-
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -371,6 +309,131 @@ __device__ __forceinline__ int chunk_row(int j, int half) {
   else if constexpr (FMT == CKV_FMT_MIXED) return half == 0 ? (j >> 4) : j / 20;
   else return j >> 3;
 }
+
+}  // namespace
+
+namespace {
+
+// Combines the G partials of one half over units [u0, u1) of 8 columns x H
+// head rows into `out`, staged through shared memory at `stage` (room for
+// kMergeStagePieces 16-byte pieces): per pass, every piece of P items x G
+// partials is copied by cp.async, all in flight at once, while warps 6..9
+// turn each row's (m, l) of the G pairs into the weights l_q 2^(m_q - M) / L
+// (`wsm`, 2 x kMaxPairs x 128 floats; the first pass only) and, when lse is
+// not null, write its log-sum-exp; then each thread forms its items from
+// shared memory, one partial at a time.  Out of line and rolled over the partials: the merge
+// runs once per call, usually with its code cold in the instruction caches.
+//
+// rtab (null: none): (cos, sin) of the 32 rope pairs; the units holding the
+// last 64 latent dims (units 24..31 of half 1) are turned by the opposite
+// angle before they are stored (the output's RoPE at position -i).
+constexpr uint32_t kMergeWBytes = 2 * kMaxPairs * 128 * 4;
+constexpr int kMergeStagePieces = (int)((kStages * kEBytes - kMergeWBytes) / 16);
+
+__device__ __noinline__ void merge_partials(const uint4* pq0, float* wsm, uint32_t stage, int G, int H,
+                                            __nv_bfloat16* out, float* lse, int tid, int u0, int u1,
+                                            const float2* rtab) {
+  const int n_items = (u1 - u0) * H;   // only the H real head rows
+  const int P = kMergeStagePieces / G;
+  const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll 1
+  for (int p0 = 0; p0 < n_items; p0 += P) {
+    const int np = min(P, n_items - p0);
+    // item k of the pass is row hh of unit uu: (uu, hh) advance with k
+    const int kf = p0 + tid, uf = u0 + kf / H, hf = kf - (uf - u0) * H;
+    auto step = [&](int& uu, int& hh) {
+      hh += kThreadsAttn;
+#pragma unroll 1
+      while (hh >= H) {
+        hh -= H;
+        ++uu;
+      }
+    };
+    int uu = uf, hh = hf;
+#pragma unroll 1
+    for (int k = tid; k < np; k += kThreadsAttn, step(uu, hh)) {
+      const uint4* src = pq0 + uu * 128 + hh;
+#pragma unroll 1
+      for (int q = 0; q < G; ++q) cp_async16(stage + (uint32_t)(q * P + k) * 16u, src + q * kPart16);
+    }
+    cp_async_commit();
+    if (p0 == 0 && warp >= 6) {
+      const int h = (warp & 3) * 32 + lane;
+      float M = -INFINITY;
+      float2 ml[kMaxPairs];   // every pair's (m, l) load in flight at once
+#pragma unroll
+      for (int q = 0; q < kMaxPairs; ++q)
+        ml[q] = q < G ? __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart16 + 32 * 128) + h)
+                      : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int q = 0; q < kMaxPairs; ++q) {
+        wsm[q * 128 + h] = ml[q].x;   // m_q (the weight from the next loop on)
+        wsm[(kMaxPairs + q) * 128 + h] = ml[q].y;
+        M = fmaxf(M, ml[q].x);
+      }
+      float L = 0.f;
+#pragma unroll 1
+      for (int q = 0; q < G; ++q) {
+        const float mq = wsm[q * 128 + h], lq0 = wsm[(kMaxPairs + q) * 128 + h];
+        const float lq = mq == -INFINITY ? 0.f : lq0 * exp2f(mq - M);
+        wsm[q * 128 + h] = lq;
+        L += lq;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+      for (int q = 0; q < G; ++q) wsm[q * 128 + h] *= inv;
+      if (lse && h < H) lse[h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    uu = uf;
+    hh = hf;
+#pragma unroll 1
+    for (int k = tid; k < np; k += kThreadsAttn, step(uu, hh)) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      // two partials per step: their loads in flight together
+#pragma unroll 1
+      for (int q = 0; q < G; q += 2) {
+        const bool two = q + 1 < G;
+        const float w0 = wsm[q * 128 + hh], w1 = two ? wsm[(q + 1) * 128 + hh] : 0.f;
+        const uint4 v0 = ld_shared_u4(stage + (uint32_t)(q * P + k) * 16u);
+        const uint4 v1 = two ? ld_shared_u4(stage + (uint32_t)((q + 1) * P + k) * 16u) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t x0[4] = {v0.x, v0.y, v0.z, v0.w}, x1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x0[e]));
+          acc[2 * e] += w0 * f.x;
+          acc[2 * e + 1] += w0 * f.y;
+        }
+        if (two) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x1[e]));
+            acc[2 * e] += w1 * f.x;
+            acc[2 * e + 1] += w1 * f.y;
+          }
+        }
+      }
+      if (rtab && uu >= 24) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 cs = rtab[4 * (uu - 24) + e];
+          const float re = acc[2 * e], im = acc[2 * e + 1];
+          acc[2 * e] = re * cs.x + im * cs.y;
+          acc[2 * e + 1] = im * cs.x - re * cs.y;
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16(acc[0], acc[1]);
+      o.y = pack_bf16(acc[2], acc[3]);
+      o.z = pack_bf16(acc[4], acc[5]);
+      o.w = pack_bf16(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + (int64_t)hh * 512 + 8 * uu) = o;
+    }
+    __syncthreads();   // the staging area is written again by the next pass
+  }
+}
+
 
 }  // namespace
 
@@ -1086,10 +1149,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   // ------------------------------------ merge of the G partials of half c ----
   // With a sequence-wide cluster every partial of the sequence is written
   // once the cluster barrier above is through, and pair `pair` merges units
-  // [u0, u1) of 8 columns of its half.  Each head row's (m, l) of the G
-  // pairs become weights l_q 2^(m_q - M) / L in shared memory (the tile ring
-  // is dead by now), and all 320 threads combine (row, unit) items, 16 loads
-  // in flight each.
+  // [u0, u1) of 8 columns of its half (merge_partials).
   // With pair clusters, no CTA waits for another cluster: each CTA counts
   // itself in on its half's counter once its partial is written, and the
   // last of the G CTAs of a half merges all 32 units of that half (and
@@ -1115,44 +1175,17 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   if (!*abort_p && merge_here) {
     const uint4* pq0 = reinterpret_cast<const uint4*>(a.part) +
                        (((int64_t)blockIdx.z * gridDim.y + b) * (2 * G) + half) * (kPartFloats / 4);
-    float* wsm = reinterpret_cast<float*>(gbase + kOffE);   // [kMaxPairs][128] weights
-    if (warp >= 6) {
-      const int h = (warp & 3) * 32 + lane;
-      float mq[kMaxPairs], lq[kMaxPairs];
-      float M = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < kMaxPairs; ++q) {
-        mq[q] = -INFINITY;
-        lq[q] = 0.f;
-        if (q < G) {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(pq0 + q * kPart16 + 32 * 128) + h);
-          mq[q] = v.x;
-          lq[q] = v.y;
-          M = fmaxf(M, v.x);
-        }
-      }
-      float L = 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxPairs; ++q) {
-        lq[q] = (q >= G || mq[q] == -INFINITY) ? 0.f : lq[q] * exp2f(mq[q] - M);
-        L += lq[q];
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxPairs; ++q) wsm[q * 128 + h] = lq[q] * inv;
-      // one CTA of half 0 writes the lse
-      const bool lse_here = a.cluster_all ? blockIdx.x == 0 : half == 0;
-      if (lse_here && a.lse && h < a.H)
-        a.lse[(int64_t)b * a.H + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    }
-    __syncthreads();
+    // the tile ring is dead by now: weights, then the staged pieces
+    float* wsm = reinterpret_cast<float*>(gbase + kOffE);
+    const uint32_t stage = base + kOffE + kMergeWBytes;
+    // one CTA of half 0 writes the lse
+    const bool lse_here = a.cluster_all ? blockIdx.x == 0 : half == 0;
+    float* lse = lse_here && a.lse ? a.lse + (int64_t)b * a.H : nullptr;
     __nv_bfloat16* out = a.out + (int64_t)b * a.H * 512 + half * 256;
     const int u0 = a.cluster_all ? pair * 32 / G : 0, u1 = a.cluster_all ? (pair + 1) * 32 / G : 32;
     const float2* rtab = (half == 1 && a.rope_pos && a.rope_out)
                              ? reinterpret_cast<const float2*>(gbase + kOffRope) : nullptr;
-    if (G <= 2) merge_items<2>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
-    else if (G <= 4) merge_items<4>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
-    else merge_items<8>(pq0, wsm, G, a.H, out, tid, u0, u1, rtab);
+    merge_partials(pq0, wsm, stage, G, a.H, out, lse, tid, u0, u1, rtab);
     if (tid == 0 && !use_tma) trace(a.st, tr, 4, tr0);   // debug: merge done
   }
   __syncthreads();
