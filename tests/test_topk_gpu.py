@@ -104,6 +104,40 @@ def test_index_topk_exact_ties_go_to_lower_index():
     assert np.array_equal(idx, _gpu_selection_of(d, n, 512))
 
 
+@pytest.mark.parametrize("fmt,HI,n_hi,group", [
+    ("fp4", 64, 490, 40),     # the merge ranks a short boundary list directly
+    ("fp4", 64, 200, 600),    # ... and radix-selects a longer one
+    ("bf16", 8, 200, 600),    # the CUDA-core scorer's merge
+])
+def test_index_boundary_tie_group(fmt, HI, n_hi, group):
+    """Three key vectors, each repeated: n_hi copies score highest, `group`
+    copies tie exactly on the top-512 boundary, the rest score lowest.  The
+    selection is the n_hi plus the group's lowest entries, whatever chunk
+    each copy sits in."""
+    b = ckv()
+    n, k = 3000, 512
+    assert n_hi < k < n_hi + group
+    base = wl.rms_rows((3, 128), 91, "cuda")
+    qi = wl.rms_rows((1, HI, 128), 92, "cuda")
+    w = wl.head_weights((1, HI), 93, "cuda")
+    sc3, _ = _oracle_scores(base, qi[0], w[0], fmt)
+    hi, mid, lo = np.argsort(-sc3)
+    assert sc3[hi] > sc3[mid] > sc3[lo]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(94)).numpy()
+    which = np.full(n, lo)
+    which[perm[:n_hi]] = hi
+    which[perm[n_hi:n_hi + group]] = mid
+    keys = base[torch.as_tensor(which, device="cuda")]
+    plane = gpu_plane(fmt, 128, [keys], n)
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, HI, n, k, 0))
+    want = np.sort(np.concatenate([perm[:n_hi], np.sort(perm[n_hi:n_hi + group])[:k - n_hi]]))
+    for _ in range(2):    # the second call checks that the workspace was left clean
+        idx = b.csa_index_topk(plane, n_comp, n, qi, w, k, ws=ws).cpu().numpy()[0]
+        assert b.read_device_status(ws) == 0
+        assert np.array_equal(idx, want)
+
+
 @pytest.mark.parametrize("HI2", [64, 40])
 def test_index_pool_and_reindex(HI2):
     """CSA2 Full (pool of 2048 + top-512) then Reindex over that pool: the
