@@ -396,14 +396,18 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     // plain shared atomics (match.any aggregation measured far slower)
     uint32_t* ws = wsub + warp * 256;
 #pragma unroll 1
-    for (int i = threadIdx.x; i < n_pad; i += NT) {
-      const uint32_t u = surv_key[i];
-      if (key_bin(u) == tb && u != 0u) atomicAdd(&ws[(u >> (kBinShift - 8)) & 255u], 1u);
+    for (int i0 = threadIdx.x; i0 < n_pad; i0 += 4 * NT) {
+      uint32_t u[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) u[k] = i0 + k * NT < n_pad ? surv_key[i0 + k * NT] : 0u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (key_bin(u[k]) == tb && u[k] != 0u) atomicAdd(&ws[(u[k] >> (kBinShift - 8)) & 255u], 1u);
     }
     __syncthreads();
     for (int v = threadIdx.x; v < 256; v += NT) {
       uint32_t t = 0;
-#pragma unroll 1
+#pragma unroll
       for (int w = 0; w < kWarps; ++w) t += wsub[w * 256 + v];
       sm.sub[v] = t;
     }
