@@ -236,6 +236,7 @@ __device__ __forceinline__ void clear_sequence_state(uint32_t* gh, uint32_t* seq
     for (int v = z0 / 4 + (int)threadIdx.x; v < z1 / 4; v += NT)
       reinterpret_cast<uint4*>(gh)[v] = make_uint4(0u, 0u, 0u, 0u);
   }
+  __syncthreads();   // every thread has read seq[2] before it is cleared
   if (threadIdx.x == 0) {
     seq[1] = 0u;
     seq[2] = 0u;
