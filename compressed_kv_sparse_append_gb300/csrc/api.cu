@@ -508,6 +508,132 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
                            lse, nullptr, ws, ws_bytes, stream);
 }
 
+// A side stream and two events per host thread and device, made on first
+// use: the group call's Reindex passes overlap its first attention launch.
+struct SideResources {
+  cudaStream_t s = nullptr;
+  cudaEvent_t full = nullptr, re = nullptr;
+};
+cudaError_t side_resources(SideResources*& out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kOnceDevices) return cudaErrorInvalidDevice;
+  static thread_local SideResources tl[kOnceDevices];
+  SideResources& r = tl[dev];
+  if (!r.s) {
+    cudaStream_t s = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (b) cudaEventDestroy(b);
+      if (a) cudaEventDestroy(a);
+      if (s) cudaStreamDestroy(s);
+      return e;
+    }
+    r.s = s;
+    r.full = a;
+    r.re = b;
+  }
+  out = &r;
+  return cudaSuccess;
+}
+
+// The group's passes with the Reindex passes on the side stream: caller's
+// stream: Full index (layer 0), then one attention launch of up to
+// kLayersPerLaunch layers whose indices come from the Full pass; side stream
+// (after the Full pass): the Reindex passes in layer order; caller's stream
+// (after those): the remaining layers' attention, in launches of at most
+// kLayersPerLaunch split evenly.  root[l]: the layer whose index pass layer l
+// uses.  Everything the call enqueues is ordered before the caller's stream's
+// next work.
+ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const int32_t* n_comp,
+                                 int n_comp_max, const int32_t* win_len, int B, int H, int HI,
+                                 int topk, float sm_scale, int pool_len, int32_t* idxbuf,
+                                 int32_t* pool_buf, uint8_t* idx_region, uint8_t* attn_region,
+                                 DevStatus* dst, cudaStream_t st) {
+  const int L = g->n_layers;
+  SideResources* side = nullptr;
+  ckv_status s = cuda_status(side_resources(side));
+  if (s) return s;
+  int32_t* own[CKV_CSA2_MAX_LAYERS];
+  for (int l = 0; l < L; ++l) own[l] = g->idx_out[l] ? g->idx_out[l] : idxbuf + (size_t)l * B * topk;
+  // Full pass (layer 0) and the copies of the indices that reuse it
+  s = run_index(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[0], g->w[0], HI, topk, nullptr, 0,
+                own[0], pool_buf, pool_len, nullptr, dst, idx_region, st);
+  if (s) return s;
+  s = cuda_status(cudaEventRecord(side->full, st));
+  if (s) return s;
+  // Reindex passes on the side stream
+  s = cuda_status(cudaStreamWaitEvent(side->s, side->full, 0));
+  if (s) return s;
+  for (int l = 1; l < L; ++l)
+    if (g->role[l] == CKV_CSA2_REINDEX) {
+      s = run_index(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[l], g->w[l], HI, topk, pool_buf,
+                    pool_len, own[l], nullptr, 0, nullptr, dst, idx_region, side->s);
+      if (s) return s;
+    }
+  s = cuda_status(cudaEventRecord(side->re, side->s));
+  if (s) return s;
+  // launch order: the first kLayersPerLaunch Full-derived layers, then the rest
+  int order[CKV_CSA2_MAX_LAYERS], n_first = 0, n = 0;
+  for (int l = 0; l < L && n_first < kLayersPerLaunch; ++l)
+    if (g->role[root[l]] == CKV_CSA2_FULL) order[n++] = l, ++n_first;
+  for (int l = 0; l < L; ++l) {
+    bool placed = false;
+    for (int j = 0; j < n_first; ++j) placed |= order[j] == l;
+    if (!placed) order[n++] = l;
+  }
+  AttnArgs la[CKV_CSA2_MAX_LAYERS];
+  bool waited = false;
+  for (int j0 = 0, gi = 0; j0 < L; ++gi) {
+    // the first launch: the Full-derived layers; then the rest, evenly
+    int n_g;
+    if (gi == 0 && n_first > 0) {
+      n_g = n_first;
+    } else {
+      const int left = L - j0, n_launch = (left + kLayersPerLaunch - 1) / kLayersPerLaunch;
+      n_g = left / n_launch;
+    }
+    bool needs_re = false;
+    for (int j = j0; j < j0 + n_g; ++j) needs_re |= g->role[root[order[j]]] == CKV_CSA2_REINDEX;
+    if (needs_re && !waited) {
+      s = cuda_status(cudaStreamWaitEvent(st, side->re, 0));
+      if (s) return s;
+      waited = true;
+    }
+    int rows_max = 0;
+    for (int j = j0; j < j0 + n_g; ++j) {
+      const int r = topk + (int)g->win[g->kv_src[order[j]]].cap;
+      rows_max = rows_max > r ? rows_max : r;
+    }
+    const PairChoice pc = choose_pairs(B * n_g, rows_max);
+    for (int j = j0; j < j0 + n_g; ++j) {
+      const int l = order[j], k = g->kv_src[l];
+      la[j] = attn_args(&g->kv[k], &g->win[k], win_len, g->q[l], H, sm_scale, g->out[l], g->lse[l], dst);
+      set_rope(la[j], &g->rope);   // checked before any launch
+      la[j].idx = own[root[l]];
+      la[j].topk = topk;
+      la[j].G = pc.G;
+      la[j].cluster_all = pc.cluster_all;
+      attn_set_ws(la[j], attn_region, B, CKV_CSA2_MAX_LAYERS, j0);
+      if (g->role[l] == CKV_CSA2_REUSE && g->idx_out[l]) {
+        s = cuda_status(cudaMemcpyAsync(g->idx_out[l], own[root[l]], (size_t)B * topk * 4,
+                                        cudaMemcpyDeviceToDevice, st));
+        if (s) return s;
+      }
+    }
+    s = cuda_status(launch_attention_layers(la + j0, n_g, B, st));
+    if (s) return s;
+    j0 += n_g;
+  }
+  // every side-stream pass is done before the caller's stream goes on
+  if (!waited) s = cuda_status(cudaStreamWaitEvent(st, side->re, 0));
+  return s;
+}
+
 ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
                                  int32_t n_comp_max, const int32_t* win_len, int32_t B,
                                  int32_t H, int32_t HI, int32_t topk, float sm_scale,
@@ -582,6 +708,23 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   if (n_append > 0) {
     s = cuda_status(launch_append(*append_dst, append_src_bf16, append_slot, n_append, dst, st));
     if (s) return s;
+  }
+  // Layers whose indices come from a Reindex pass (directly or by reuse)
+  // wait for it; the others need only the Full pass of layer 0.  With one
+  // Full layer and at least one Reindex layer, the Reindex passes run on a
+  // side stream while the first attention launch (Full-derived layers only)
+  // runs on the caller's stream.
+  {
+    int root[CKV_CSA2_MAX_LAYERS];
+    bool one_full = true, any_re = false;
+    for (int l = 0; l < L; ++l) {
+      root[l] = g->role[l] == CKV_CSA2_REUSE ? root[g->idx_src[l]] : l;
+      if (l > 0 && g->role[l] == CKV_CSA2_FULL) one_full = false;
+      any_re |= g->role[l] == CKV_CSA2_REINDEX;
+    }
+    if (one_full && any_re && L >= 2)
+      return csa2_group_overlapped(g, root, n_comp, n_comp_max, win_len, B, H, HI, topk, sm_scale,
+                                   pool_len, idxbuf, pool_buf, idx_region, attn_region, dst, st);
   }
   const int32_t* layer_idx[CKV_CSA2_MAX_LAYERS];
   for (int l = 0; l < L; ++l) {

@@ -18,7 +18,9 @@
  *   - Pointers are DEVICE pointers unless marked [host].  The caller owns
  *     every buffer; the library allocates no device memory and keeps no
  *     state between calls (apart from the per-device launch attributes it
- *     sets once).
+ *     sets once, and the side stream and two events that
+ *     ckv_csa2_group_decode creates on its first call in each host thread
+ *     and device).
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and return after enqueueing.  The
  *     kernels are launched with programmatic stream serialisation: one may
@@ -330,9 +332,17 @@ ckv_status ckv_hca_attn_rope(const ckv_plane *kv, const int32_t *n_comp,
  * Every layer then attends (as ckv_csa_sparse_attn) to the main KV and
  * window of layer kv_src[l].  Before the layers run, the call appends
  * n_append rows to `append_dst` (as ckv_kv_append_quant).  The layers'
- * attention runs in launches of at most four layers each (six layers: two
- * launches of three), so that every launch's parameter block stays within
- * the classic 4 KB.  The call refuses to be captured into a CUDA graph: on
+ * attention runs in launches of at most four layers each, so that every
+ * launch's parameter block stays within the classic 4 KB.  With one FULL
+ * layer (layer 0) and at least one REINDEX layer, the REINDEX passes run on
+ * a side stream of the library's own (one per host thread and device, made
+ * on first use) while the first attention launch -- up to four layers whose
+ * indices come from the FULL pass -- runs on `stream`; the launches after it
+ * wait for the side stream, so everything the call enqueues is ordered
+ * before the next work on `stream` (six layers FULL, REINDEX, 4 x REUSE of
+ * layer 0: launches of four and two).  Otherwise the passes run in layer
+ * order on `stream` (six layers: two launches of three).  The call refuses
+ * to be captured into a CUDA graph: on
  * a capturing stream it returns CKV_ERR_UNSUPPORTED and enqueues nothing
  * (replaying a captured group call faulted on GB300, cause not found; eager
  * calls are not affected). */
