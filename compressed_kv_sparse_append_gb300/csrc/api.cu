@@ -544,11 +544,11 @@ cudaError_t side_resources(SideResources*& out) {
 // The group's passes with the Reindex passes on the side stream: caller's
 // stream: Full index (layer 0), then one attention launch of up to
 // kLayersPerLaunch layers whose indices come from the Full pass; side stream
-// (after the Full pass): the Reindex passes in layer order; caller's stream
-// (after those): the remaining layers' attention, in launches of at most
-// kLayersPerLaunch split evenly.  root[l]: the layer whose index pass layer l
-// uses.  Everything the call enqueues is ordered before the caller's stream's
-// next work.
+// (after the Full pass): the Reindex passes in layer order, then the
+// remaining layers' attention, in launches of at most kLayersPerLaunch split
+// evenly, beside the caller's stream's launch.  root[l]: the layer whose
+// index pass layer l uses.  The caller's stream finally waits for the side
+// stream, so everything the call enqueues is ordered before its next work.
 ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const int32_t* n_comp,
                                  int n_comp_max, const int32_t* win_len, int B, int H, int HI,
                                  int topk, float sm_scale, int pool_len, int32_t* idxbuf,
@@ -575,8 +575,6 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
                     pool_len, own[l], nullptr, 0, nullptr, dst, idx_region, side->s);
       if (s) return s;
     }
-  s = cuda_status(cudaEventRecord(side->re, side->s));
-  if (s) return s;
   // launch order: the first kLayersPerLaunch Full-derived layers, then the rest
   int order[CKV_CSA2_MAX_LAYERS], n_first = 0, n = 0;
   for (int l = 0; l < L && n_first < kLayersPerLaunch; ++l)
@@ -587,7 +585,6 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
     if (!placed) order[n++] = l;
   }
   AttnArgs la[CKV_CSA2_MAX_LAYERS];
-  bool waited = false;
   for (int j0 = 0, gi = 0; j0 < L; ++gi) {
     // the first launch: the Full-derived layers; then the rest, evenly
     int n_g;
@@ -597,13 +594,9 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
       const int left = L - j0, n_launch = (left + kLayersPerLaunch - 1) / kLayersPerLaunch;
       n_g = left / n_launch;
     }
-    bool needs_re = false;
-    for (int j = j0; j < j0 + n_g; ++j) needs_re |= g->role[root[order[j]]] == CKV_CSA2_REINDEX;
-    if (needs_re && !waited) {
-      s = cuda_status(cudaStreamWaitEvent(st, side->re, 0));
-      if (s) return s;
-      waited = true;
-    }
+    // the first launch on the caller's stream, beside the Reindex passes;
+    // the later ones after those passes on the side stream
+    const cudaStream_t ls = gi == 0 ? st : side->s;
     int rows_max = 0;
     for (int j = j0; j < j0 + n_g; ++j) {
       const int r = topk + (int)g->win[g->kv_src[order[j]]].cap;
@@ -621,17 +614,18 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
       attn_set_ws(la[j], attn_region, B, CKV_CSA2_MAX_LAYERS, j0);
       if (g->role[l] == CKV_CSA2_REUSE && g->idx_out[l]) {
         s = cuda_status(cudaMemcpyAsync(g->idx_out[l], own[root[l]], (size_t)B * topk * 4,
-                                        cudaMemcpyDeviceToDevice, st));
+                                        cudaMemcpyDeviceToDevice, ls));
         if (s) return s;
       }
     }
-    s = cuda_status(launch_attention_layers(la + j0, n_g, B, st));
+    s = cuda_status(launch_attention_layers(la + j0, n_g, B, ls));
     if (s) return s;
     j0 += n_g;
   }
-  // every side-stream pass is done before the caller's stream goes on
-  if (!waited) s = cuda_status(cudaStreamWaitEvent(st, side->re, 0));
-  return s;
+  // everything on the side stream is done before the caller's stream goes on
+  s = cuda_status(cudaEventRecord(side->re, side->s));
+  if (s) return s;
+  return cuda_status(cudaStreamWaitEvent(st, side->re, 0));
 }
 
 ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,

@@ -336,12 +336,13 @@ ckv_status ckv_hca_attn_rope(const ckv_plane *kv, const int32_t *n_comp,
  * launch's parameter block stays within the classic 4 KB.  With one FULL
  * layer (layer 0) and at least one REINDEX layer, the REINDEX passes run on
  * a side stream of the library's own (one per host thread and device, made
- * on first use) while the first attention launch -- up to four layers whose
- * indices come from the FULL pass -- runs on `stream`; the launches after it
- * wait for the side stream, so everything the call enqueues is ordered
- * before the next work on `stream` (six layers FULL, REINDEX, 4 x REUSE of
- * layer 0: launches of four and two).  Otherwise the passes run in layer
- * order on `stream` (six layers: two launches of three).  The call refuses
+ * on first use), followed there by the attention of the layers that need
+ * them, while the first attention launch -- up to four layers whose indices
+ * come from the FULL pass -- runs on `stream`; `stream` finally waits for
+ * the side stream, so everything the call enqueues is ordered before the
+ * next work on `stream` (six layers FULL, REINDEX, 4 x REUSE of layer 0:
+ * launches of four and two).  Otherwise the passes run in layer order on
+ * `stream` (six layers: two launches of three).  The call refuses
  * to be captured into a CUDA graph: on
  * a capturing stream it returns CKV_ERR_UNSUPPORTED and enqueues nothing
  * (replaying a captured group call faulted on GB300, cause not found; eager
