@@ -16,8 +16,11 @@ pytestmark = pytest.mark.gpu
 TAU = 1.0 / math.sqrt(512)
 
 
-# L = 6 runs its attention as two launches of three layers, 8 as 4 + 4,
-# 5 as 3 + 2, 3 as one launch.
+# Every wiring here has a Reindex layer, so the Reindex pass runs on the
+# library's side stream beside a first attention launch of the layers whose
+# indices come from the Full pass: the bench wiring (Reuse of layer 0) as
+# launches of four and L - 4 layers, the pages wiring (Reuse of the previous
+# layer) as layer 0 alone and then the rest in launches of at most four.
 @pytest.mark.parametrize("pool_len,wiring,L", [(256, "bench", 6), (64, "pages", 6),
                                                 (64, "degenerate", 6), (64, "pages", 8),
                                                 (64, "pages", 5), (64, "pages", 3)])
