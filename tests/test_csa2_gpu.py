@@ -23,7 +23,8 @@ TAU = 1.0 / math.sqrt(512)
 # layer) as layer 0 alone and then the rest in launches of at most four.
 @pytest.mark.parametrize("pool_len,wiring,L", [(256, "bench", 6), (64, "pages", 6),
                                                 (64, "degenerate", 6), (64, "pages", 8),
-                                                (64, "pages", 5), (64, "pages", 3)])
+                                                (64, "pages", 5), (64, "pages", 3),
+                                                (256, "no_reindex", 5)])
 def test_csa2_group_matches_oracle(pool_len, wiring, L):
     b = ckv()
     B, n, H, HI, topk, W = 2, 2500, 64, 64, 64, 128
@@ -43,7 +44,10 @@ def test_csa2_group_matches_oracle(pool_len, wiring, L):
     lse = [torch.empty((B, H), device="cuda") for _ in range(L)]
     idx_out = [torch.empty((B, topk), dtype=torch.int32, device="cuda") for _ in range(L)]
     roles = [oc.FULL, oc.REINDEX] + [oc.REUSE] * (L - 2)
-    if wiring == "bench":
+    if wiring == "no_reindex":   # every layer in layer order on the caller's stream
+        roles = [oc.FULL] + [oc.REUSE] * (L - 1)
+        kv_src, idx_src = list(range(L)), [0] * L
+    elif wiring == "bench":
         kv_src, idx_src = [0, 0] + list(range(2, L)), [0] * L
     else:   # the pages' reading: previous layer's indices, one shared KV
         kv_src, idx_src = [0] * L, [0, 0] + list(range(1, L - 1))
@@ -80,12 +84,14 @@ def test_csa2_group_matches_oracle(pool_len, wiring, L):
         e0 = score_eps(qv0, wss[0], kvals)
         gi = [idx_out[l][s].cpu().numpy() for l in range(L)]
         assert check_topk(gi[0], s0, e0, topk, where="full") == 0
-        qv1 = oi.indexer_query(qis[1], True)
-        s1 = oi.index_scores(qv1, wss[1], kvals)
-        e1 = score_eps(qv1, wss[1], kvals)
-        assert check_topk(gi[1], s1, e1, topk, candidates=pool_ref, where="reindex") == 0
-        for l in range(2, L):
-            assert np.array_equal(gi[l], gi[idx_src[l]])
+        if roles[1] == oc.REINDEX:
+            qv1 = oi.indexer_query(qis[1], True)
+            s1 = oi.index_scores(qv1, wss[1], kvals)
+            e1 = score_eps(qv1, wss[1], kvals)
+            assert check_topk(gi[1], s1, e1, topk, candidates=pool_ref, where="reindex") == 0
+        for l in range(1, L):
+            if roles[l] == oc.REUSE:
+                assert np.array_equal(gi[l], gi[idx_src[l]])
         if wiring == "degenerate":
             assert set(gi[1]) == set(gi[0])
         for l in range(L):
