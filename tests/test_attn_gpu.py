@@ -87,6 +87,30 @@ def test_csa_matches_oracle(fmt, blk, H, topk):
         check_attention(out[s], lse[s], o_ref, l_ref, H, where="csa seq %d" % s)
 
 
+@pytest.mark.parametrize("fmt", ["mixed", "fp4"])
+def test_csa_with_nothing_to_attend(fmt):
+    """Every selected index -1: sequence 0 attends its window only, sequence
+    1 (window length 0) attends nothing: zero output and lse -inf."""
+    b = ckv()
+    B, W, n, H, topk = 2, 128, 600, 64, 512
+    kv, win = _seq_rows(B, [n] * B, W, seed=41)
+    kvp, wp = gpu_plane(fmt, 512, kv, n), gpu_plane(fmt, 512, win, W)
+    q = torch.stack([wl.rms_rows((H, 512), 43 + s, "cuda") for s in range(B)])
+    idx = torch.full((B, topk), -1, dtype=torch.int32)
+    win_lens = [W, 0]
+    lse = torch.empty((B, H), device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_SPARSE_ATTN, B))
+    out = b.csa_sparse_attn(kvp, wp, torch.tensor(win_lens, dtype=torch.int32, device="cuda"),
+                            idx.cuda(), q, TAU, lse=lse, ws=ws)
+    assert b.read_device_status(ws) == 0
+    okv, owin = oracle_plane(fmt, kv), oracle_plane(fmt, win)
+    o_ref, l_ref = oa.csa_sparse_attention(np32(q[0]), okv[0][0], okv[0][1], fmt, idx[0].numpy(),
+                                           owin[0][0], owin[0][1], W, TAU)
+    check_attention(out[0], lse[0], o_ref, l_ref, H, where="window only")
+    assert out[1].float().abs().max().item() == 0.0
+    assert bool(torch.isneginf(lse[1]).all())
+
+
 def test_csa_with_every_entry_equals_hca_on_gpu():
     b = ckv()
     n, W, H = 700, 128, 128

@@ -49,6 +49,7 @@ def _gpu_selection_of(dbg_row, n, k):
     ("bf16", 4, [1024], 512),                      # the tiny BF16 workload shape
     ("fp4", 64, [3000, 1500, 700], 512),           # ragged, one sequence below... above k
     ("fp4", 64, [300, 9000], 512),                 # n_comp < k: -1 padding
+    ("fp4", 64, [0, 5000, 1], 512),                # a sequence with no entries, one with one
     ("fp4", 16, [20000], 1024),                    # several chunks, k = 1024
     ("bf16", 8, [5000, 17], 64),
     ("bf16", 16, [2000], 256),                     # CUDA-core scorer sized for 16 heads
