@@ -274,8 +274,8 @@ void attn_set_ws_single(AttnArgs& a, uint8_t* region, int B) {
 // sequence merges after a hardware-scheduled cluster barrier.  Pair clusters
 // fit more pairs on the GPU; their sequence's partials are merged by the
 // last CTA of each half to finish (a counter in the workspace, no waiting),
-// and they are taken when they allow a larger G.  Neither needs more than
-// the launch's clusters resident at once.
+// and they are taken when they leave the busiest pair fewer tiles.  Neither
+// needs more than the launch's clusters resident at once.
 struct PairChoice {
   int G;
   int cluster_all;
@@ -289,7 +289,11 @@ PairChoice choose_pairs(int n_seq, int n_rows_max) {
     if (fit > 0 && n_seq <= fit) g_all = G;
     if (fit2 > 0 && n_seq * G <= fit2) g_pair = G;
   }
-  return g_pair > g_all ? PairChoice{g_pair, 0} : PairChoice{g_all, 1};
+  // fewer tiles for the busiest pair wins; on a tie the sequence-wide
+  // clusters, whose merge every CTA shares (with pair clusters one CTA per
+  // half merges all G partials)
+  const int t_all = (tiles + g_all - 1) / g_all, t_pair = (tiles + g_pair - 1) / g_pair;
+  return t_pair < t_all ? PairChoice{g_pair, 0} : PairChoice{g_all, 1};
 }
 
 ckv_status check_attn_common(const ckv_plane* kv, const ckv_plane* win, const int32_t* win_len,
