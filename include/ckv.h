@@ -230,8 +230,8 @@ ckv_status ckv_csa_index_topk(const ckv_plane *idx_keys, const int32_t *n_comp,
  *   Returns CKV_ERR_WORKSPACE when the call needs more scratch than
  *   CKV_STATIC_SCRATCH_BYTES (see ckv_workspace_bytes(CKV_OP_INDEX_TOPK, ...)).
  *   The first call on a device looks the array up (cudaGetSymbolAddress)
- *   with that device current: make that first call before any stream
- *   capture.  Every call first clears the scratch's counters on `stream`.
+ *   with that device current.  Every call first clears the scratch's
+ *   counters on `stream`.
  *   All calls share the one array, which keeps the last call's contents:
  *   calls that overlap on the GPU (different streams) race and must be
  *   serialised by the caller.  Device-side range errors (a pool entry at or
