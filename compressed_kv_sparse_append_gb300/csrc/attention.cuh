@@ -50,8 +50,8 @@ struct AttnArgs {
 
 constexpr int kMaxPairs = 8;      // CTA pairs per sequence
 // Layers per launch: the kernel's whole parameter block (two tensor maps and
-// the batch) stays within 4 KB, the classic limit, so a launch captured into
-// a CUDA graph carries it whole; more layers take more launches.
+// the batch) stays within 4 KB, the classic kernel-parameter limit; more
+// layers take more launches.
 constexpr int kLayersPerLaunch = 4;
 constexpr int kArgsTag = 0x434B5641;
 struct AttnBatch {
