@@ -17,7 +17,8 @@
 //      candidates in bins >= T are exactly the sequence's keys there (every
 //      chunk's bound is <= T); all candidates are staged in shared memory in
 //      entry order, the keys of bin T are counted by their next 8 bits, and
-//      an exact radix select restricted to that sub-bin picks the top K.
+//      an exact select restricted to that sub-bin picks the top K (a CSA2
+//      Full layer does this twice: for its pool, then for its top-k).
 // Equal keys go to the earliest, i.e. lowest, entries.  When more survivors
 // reach the merge than its shared memory holds (a huge exact tie at the
 // boundary), the select runs on the candidate lists in global memory.
@@ -128,15 +129,14 @@ __device__ uint32_t chunk_bound(const uint32_t* gh, const uint32_t* lh, int top,
 // Final outputs from an ordered source of n elements (n_real real keys in
 // the sequence).  Hint (prefix0, top0, above): the K-th largest key has
 // prefix0's top (32 - top0) bits and `above` keys lie above all such keys
-// (top0 = 32: none).  A CSA2 Full layer keeps its pool (key and entry in
-// shared memory) and then takes its top-k from the pool: two selections run
-// through one call site.
+// (top0 = 32: none).  With `pooled`, a CSA2 Full layer's pool is written
+// first (key and entry also kept in shared memory) and the top-k is then
+// taken from the pool: two selections run through one call site.
 template <int NT>
 __device__ void emit_outputs(const IndexArgs& a, int b, SelSrc src, int n, int n_real,
                              uint32_t* pool_key, int32_t* pool_ent, MergeSmem<NT>& sm,
-                             uint32_t prefix0, int top0, int above) {
+                             uint32_t prefix0, int top0, int above, bool pooled) {
   int32_t* oi = a.out_idx + (int64_t)b * a.topk;
-  const bool pooled = a.pool_out > 0;
   int kk = min(a.topk, n_real);
   int K = pooled ? min(a.pool_out, n_real) : kk;
 #pragma unroll 1
@@ -222,10 +222,6 @@ __device__ __forceinline__ void emit_ordered(const uint32_t* key, const int32_t*
   }
 }
 
-// Staged candidate sets of a pool-building call up to this size go straight
-// to one exact select (the pool and then the top-k of the pool).
-constexpr int kDirectSelectMax = 4096;
-
 // Leaves the sequence's histogram (bins in use: below seq[1] = top, from
 // kBins - seq[2] up) and its state words zero for the next call.  Block-wide.
 template <int NT>
@@ -306,15 +302,18 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   constexpr int kWarps = NT / 32;
   const int pool_words = a.pool_out > 0 ? 2 * kMaxPool : 0;
   const int surv_cap = ((scratch_words - pool_words - kWarps * 256) / 2) & ~3;
-  // A small staged set of a pool-building call needs no threshold bin: the
-  // select runs on all of it (its K never exceeds the real keys, so the
-  // padding, key 0, is never taken).  Other staged sets take the threshold
-  // bin and its sub-bin, whose keys decide the threshold on their own.
-  const bool direct = a.pool_out > 0 && n_pad <= kDirectSelectMax && n_pad <= surv_cap;
-  // threshold bin and the count above it (every key is a survivor when the
-  // sequence has at most K)
-  uint32_t tb = 0, above = 0;
-  if (!direct && keff > 0 && (int)n_total > K) {
+  const bool pooled = a.pool_out > 0;
+  // Every key is a survivor when the sequence has at most K.  Otherwise the
+  // K-th largest key is located by its bin in the complete sequence
+  // histogram (the threshold bin), then by the next 8 bits of the
+  // candidates in that bin (the sub-bin); an exact select among the keys of
+  // that sub-bin alone decides it.
+  const bool hint = keff > 0 && (int)n_total > K;
+  // Threshold bin of the kk-th largest key and the count of keys in the bins
+  // above it: from the window read with the counts when that window reaches
+  // the top bin in use (this CTA's bound is a lower bound on the threshold
+  // bin of any kk <= K), else by a scan from the top.
+  auto threshold_bin = [&](uint32_t kk, uint32_t& tb_, uint32_t& above_) {
     bool done = false;
     if (own_bound > 0 && top <= (int)own_bound + NT) {
       uint32_t before, d0, tot, d1;
@@ -322,28 +321,26 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       if (threadIdx.x == 0) sm.bcast[0] = 0xFFFFFFFFu;
       __syncthreads();
       const uint32_t hi_cnt = tot - before - wv;   // keys in window bins above this one
-      if (wv > 0 && hi_cnt < (uint32_t)keff && hi_cnt + wv >= (uint32_t)keff) {
+      if (wv > 0 && hi_cnt < kk && hi_cnt + wv >= kk) {
         sm.bcast[0] = (uint32_t)wbin;
         sm.bcast[1] = hi_cnt;
       }
       __syncthreads();
       if (sm.bcast[0] != 0xFFFFFFFFu) {
-        tb = sm.bcast[0];
-        above = sm.bcast[1];
+        tb_ = sm.bcast[0];
+        above_ = sm.bcast[1];
         done = true;
       }
       __syncthreads();
     }
-    if (!done) tb = hist_bin_from_top<NT>(gh, top, (uint32_t)keff, sm, above);
-  }
-  const uint32_t lo_key = tb << kBinShift;
-  trace_at(a.st, tr, 20, t0);
+    if (!done) tb_ = hist_bin_from_top<NT>(gh, top, kk, sm, above_);
+    __syncthreads();   // every thread has read bcast before it is written again
+  };
 
   // Every candidate into shared memory, in entry order (chunk c's list at
   // offset sprefix[c], padded to a multiple of 4 entries whose padding keys
   // are 0, i.e. no key): one warp per chunk list, 16-byte asynchronous
-  // copies, all of them in flight at once.  Then the keys of the threshold
-  // bin are counted by their next 8 bits.
+  // copies, all of them in flight while the threshold bin is found.
   uint32_t* surv_key = scratch;
   int32_t* surv_ent = reinterpret_cast<int32_t*>(scratch + surv_cap);
   uint32_t* wsub = scratch + 2 * surv_cap;            // [warp][256] private sub-bin counts
@@ -356,12 +353,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   cl.n_chunks = nch;
   cl.stride = a.chunk;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool hint = !direct && (int)n_total > K && keff > 0;
   for (int i = threadIdx.x; i < kWarps * 256; i += NT) wsub[i] = 0u;
-  if (threadIdx.x == 0) {
-    sm.bcast[0] = 0u;   // sub-bin search defaults
-    sm.bcast[1] = 0u;
-  }
   const bool staged = n_pad <= surv_cap;
   if (staged) {
     // (the chunk lists start 16-byte aligned in global memory: a.chunk is a
@@ -380,6 +372,12 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
         cp_async16(de + 16 * g, gi + 4 * g);
       }
     }
+  }
+  uint32_t tb = 0, above = 0;
+  if (hint) threshold_bin((uint32_t)keff, tb, above);
+  const uint32_t lo_key = tb << kBinShift;
+  trace_at(a.st, tr, 20, t0);
+  if (staged) {
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();   // every copy has landed
     // the padding slots of every list become "no key"
@@ -391,30 +389,6 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
   __syncthreads();
   uint32_t n_surv = (uint32_t)n_pad;
   if (tr) a.st->pad[17] = (int32_t)(clock64() - t0);
-  if (hint && staged) {
-    // warp-private counters (no contention between warps on the few
-    // sub-bins that exact ties crowd), four independent elements per lane,
-    // plain shared atomics (match.any aggregation measured far slower)
-    uint32_t* ws = wsub + warp * 256;
-#pragma unroll 1
-    for (int i0 = threadIdx.x; i0 < n_pad; i0 += 4 * NT) {
-      uint32_t u[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) u[k] = i0 + k * NT < n_pad ? surv_key[i0 + k * NT] : 0u;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (key_bin(u[k]) == tb && u[k] != 0u) atomicAdd(&ws[(u[k] >> (kBinShift - 8)) & 255u], 1u);
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < 256; v += NT) {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) t += wsub[w * 256 + v];
-      sm.sub[v] = t;
-    }
-    __syncthreads();
-  }
-  trace_at(a.st, tr, 21, t0);
   if (tr) {
     a.st->pad[23] = (int32_t)n_surv;
     a.st->pad[25] = n_cand;
@@ -422,92 +396,132 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     a.st->pad[27] = (int32_t)above;
     a.st->pad[28] = (int32_t)n_total;
   }
-  // The sub-bin of the threshold bin that holds the keff-th largest key: the
-  // candidates below it are dropped (in order, in place), and the exact
-  // select resolves only the keys of that sub-bin.
+  bool pool_left = pooled;   // the pool is still to be written
   uint32_t prefix = lo_key, above2 = above;
   int top_bits = kBinShift;
   if (hint && staged) {
-    const uint32_t need = (uint32_t)keff - above;
-    if (warp == 0) {
-      // lane l holds sub-bins 255 - 8l .. 248 - 8l (descending)
-      uint32_t c8[8], t8 = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c8[j] = sm.sub[255 - 8 * lane - j];
-        t8 += c8[j];
-      }
-      uint32_t incl = t8;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t before = incl - t8;
-      if (before < need && incl >= need) {
-        uint32_t cum = before;
-        for (int j = 0; j < 8; ++j) {
-          if (cum + c8[j] >= need) {
-            sm.bcast[0] = (uint32_t)(255 - 8 * lane - j);
-            sm.bcast[1] = cum;
-            break;
-          }
-          cum += c8[j];
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t t2 = sm.bcast[0] & 255u;
-    above2 = above + sm.bcast[1];
-    prefix = lo_key | (t2 << (kBinShift - 8));
-    top_bits = kBinShift - 8;
-  }
-  if (hint && staged && a.pool_out == 0) {
-    // The keys of the sub-bin holding the keff-th largest (with their staged
-    // positions) into a list in the dead sub-bin counters; the threshold T
-    // and the count `need` of keys equal to T to keep are found on the list
-    // alone (every key above the sub-bin is kept), then one ordered pass over
-    // the staged candidates writes the output.
+    // One job per output: the top-K (for a pool-building call, the pool,
+    // then the top-k of the pool, which is the top-k of the sequence).  Per
+    // job: the keys of the threshold bin counted by their next 8 bits, the
+    // sub-bin holding the job's K-th largest, its keys (with their staged
+    // positions) gathered into a list in the dead sub-bin counters, the
+    // threshold T and the count `need` of keys equal to T to keep found on
+    // the list alone (every key above the sub-bin is kept), then one ordered
+    // pass over the staged candidates writes the output.
     constexpr int kListMax = 2 * NT;   // 2 x kListMax words fit in wsub
     constexpr int kRankMax = 64;
     uint32_t* lkey = wsub;
     uint32_t* lpos = wsub + kListMax;
-    if (threadIdx.x == 0) sm.bcast[2] = 0u;
-    __syncthreads();
-    const uint32_t hmask = ~((1u << top_bits) - 1u);
-    {
-      // eight keys per lane in flight, one counter update per warp and round
-      constexpr int kU = 8;
-      const uint32_t lt = (1u << lane) - 1u;
+    int32_t* oi = a.out_idx + (int64_t)b * a.topk;
 #pragma unroll 1
-      for (int w0 = warp * 32 * kU; w0 < n_pad; w0 += NT * kU) {
-        uint32_t u[kU], bal[kU], c = 0;
+    for (int job = 0;; ++job) {
+      const uint32_t kj = job == 0 ? (uint32_t)keff : (uint32_t)min(a.topk, keff);
+      if (job > 0) {
+        threshold_bin(kj, tb, above);
+        for (int i = threadIdx.x; i < kWarps * 256; i += NT) wsub[i] = 0u;   // the list's words
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) {
+        sm.bcast[0] = 0u;   // sub-bin search defaults
+        sm.bcast[1] = 0u;
+      }
+      {
+        // warp-private counters (no contention between warps on the few
+        // sub-bins that exact ties crowd), four independent elements per
+        // lane, plain shared atomics (match.any aggregation measured far
+        // slower)
+        uint32_t* ws = wsub + warp * 256;
+#pragma unroll 1
+        for (int i0 = threadIdx.x; i0 < n_pad; i0 += 4 * NT) {
+          uint32_t u[4];
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = w0 + k * 32 + lane;
-          u[k] = i < n_pad ? surv_key[i] : 0u;
-          bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && (u[k] & hmask) == prefix);
-          c += __popc(bal[k]);
+          for (int k = 0; k < 4; ++k) u[k] = i0 + k * NT < n_pad ? surv_key[i0 + k * NT] : 0u;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (key_bin(u[k]) == tb && u[k] != 0u) atomicAdd(&ws[(u[k] >> (kBinShift - 8)) & 255u], 1u);
         }
-        if (c == 0u) continue;   // warp-uniform
-        uint32_t at = 0u;
-        if (lane == 0) at = atomicAdd(&sm.bcast[2], c);
-        at = __shfl_sync(0xffffffffu, at, 0);
+        __syncthreads();
+        for (int v = threadIdx.x; v < 256; v += NT) {
+          uint32_t t = 0;
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const uint32_t x = at + __popc(bal[k] & lt);
-          if (((bal[k] >> lane) & 1u) && x < (uint32_t)kListMax) {
-            lkey[x] = u[k];
-            lpos[x] = (uint32_t)(w0 + k * 32 + lane);
+          for (int w = 0; w < kWarps; ++w) t += wsub[w * 256 + v];
+          sm.sub[v] = t;
+        }
+        __syncthreads();
+      }
+      trace_at(a.st, tr, 21, t0);
+      {
+        // the sub-bin of the threshold bin that holds the kj-th largest key
+        const uint32_t need = kj - above;
+        if (warp == 0) {
+          // lane l holds sub-bins 255 - 8l .. 248 - 8l (descending)
+          uint32_t c8[8], t8 = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            c8[j] = sm.sub[255 - 8 * lane - j];
+            t8 += c8[j];
           }
-          at += __popc(bal[k]);
+          uint32_t incl = t8;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const uint32_t before = incl - t8;
+          if (before < need && incl >= need) {
+            uint32_t cum = before;
+            for (int j = 0; j < 8; ++j) {
+              if (cum + c8[j] >= need) {
+                sm.bcast[0] = (uint32_t)(255 - 8 * lane - j);
+                sm.bcast[1] = cum;
+                break;
+              }
+              cum += c8[j];
+            }
+          }
+        }
+        __syncthreads();
+        const uint32_t t2 = sm.bcast[0] & 255u;
+        above2 = above + sm.bcast[1];
+        prefix = (tb << kBinShift) | (t2 << (kBinShift - 8));
+        top_bits = kBinShift - 8;
+      }
+      if (threadIdx.x == 0) sm.bcast[2] = 0u;
+      __syncthreads();
+      const uint32_t hmask = ~((1u << top_bits) - 1u);
+      {
+        // eight keys per lane in flight, one counter update per warp and round
+        constexpr int kU = 8;
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+        for (int w0 = warp * 32 * kU; w0 < n_pad; w0 += NT * kU) {
+          uint32_t u[kU], bal[kU], c = 0;
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const int i = w0 + k * 32 + lane;
+            u[k] = i < n_pad ? surv_key[i] : 0u;
+            bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && (u[k] & hmask) == prefix);
+            c += __popc(bal[k]);
+          }
+          if (c == 0u) continue;   // warp-uniform
+          uint32_t at = 0u;
+          if (lane == 0) at = atomicAdd(&sm.bcast[2], c);
+          at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+          for (int k = 0; k < kU; ++k) {
+            const uint32_t x = at + __popc(bal[k] & lt);
+            if (((bal[k] >> lane) & 1u) && x < (uint32_t)kListMax) {
+              lkey[x] = u[k];
+              lpos[x] = (uint32_t)(w0 + k * 32 + lane);
+            }
+            at += __popc(bal[k]);
+          }
         }
       }
-    }
-    __syncthreads();
-    const int m = (int)sm.bcast[2];
-    if (m <= kListMax) {
-      const uint32_t need2 = (uint32_t)keff - above2;   // in [1, m] by the sub-bin search
+      __syncthreads();
+      const int m = (int)sm.bcast[2];
+      if (m > kListMax) break;   // a crowded sub-bin: the compaction below
+      const uint32_t need2 = kj - above2;   // in [1, m] by the sub-bin search
       uint32_t T = 0, need = 0;
       if (m <= kRankMax) {
         // rank of each list key: larger keys first, equal keys by position;
@@ -549,16 +563,21 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       }
       trace_at(a.st, tr, 19, t0);
       if (tr) a.st->pad[31] = m;
-      int32_t* oi = a.out_idx + (int64_t)b * a.topk;
-      emit_ordered<NT>(surv_key, surv_ent, n_pad, T, need, oi, sm);
+      int32_t* out = pool_left ? a.out_pool + (int64_t)b * a.pool_out : oi;
+      const int len = pool_left ? a.pool_out : a.topk;
+      emit_ordered<NT>(surv_key, surv_ent, n_pad, T, need, out, sm);
 #pragma unroll 1
-      for (int i = keff + (int)threadIdx.x; i < a.topk; i += NT) oi[i] = -1;
+      for (int i = (int)kj + (int)threadIdx.x; i < len; i += NT) out[i] = -1;
+      if (pool_left) {
+        pool_left = false;
+        continue;
+      }
       trace_at(a.st, tr, 22, t0);
       clear_sequence_state<NT>(gh, seq, top);
       return;
     }
   }
-  if (staged && !direct && (hint || n_pad != n_cand)) {
+  if (staged && (hint || n_pad != n_cand)) {
     // in-place ordered compaction to the real keys >= prefix (without a
     // hint prefix is 0: only the padding goes), kU per thread per round (a
     // round's reads all happen before its writes, which never reach past it)
@@ -611,11 +630,11 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     ss.key = surv_key;
     ss.ent = surv_ent;
     emit_outputs<NT>(a, b, ss, (int)n_surv, (int)n_total, pool_key, pool_ent, sm, prefix,
-                     hint ? top_bits : 32, hint ? (int)above2 : 0);
+                     hint ? top_bits : 32, hint ? (int)above2 : 0, pool_left);
   } else {
     // a crowded threshold bin: select on the candidate lists in global memory
     emit_outputs<NT>(a, b, cl, n_cand, (int)n_total, pool_key, pool_ent, sm, lo_key,
-                     hint ? kBinShift : 32, hint ? (int)above : 0);
+                     hint ? kBinShift : 32, hint ? (int)above : 0, pool_left);
   }
   trace_at(a.st, tr, 22, t0);
   clear_sequence_state<NT>(gh, seq, top);

@@ -168,6 +168,40 @@ def test_index_pool_and_reindex(HI2):
         assert set(idx2[s]) <= set(pool[s])
 
 
+@pytest.mark.parametrize("n_hi,group", [
+    (200, 1200),     # pool boundary among distinct keys, top-512 boundary in a long tie
+    (1500, 1200),    # pool boundary in a long tie (top-512 inside the n_hi copies)
+])
+def test_index_pool_with_crowded_boundary(n_hi, group):
+    """CSA2 Full layer (pool of 2048 + top-512) on keys where a boundary falls
+    in a run of identical keys longer than the merge's boundary list: n_hi
+    copies of the best-scoring key, `group` copies of the second best, the
+    rest distinct.  Both outputs must equal the oracle's (ties to the lower
+    entries), with the workspace left clean for a second call."""
+    b = ckv()
+    n, k, P = 12000, 512, 2048
+    base = wl.rms_rows((n, 128), 95, "cuda")
+    qi = wl.rms_rows((1, 64, 128), 96, "cuda")
+    w = wl.head_weights((1, 64), 97, "cuda")
+    sc0, _ = _oracle_scores(base, qi[0], w[0], "fp4")
+    best, second = np.argsort(-sc0)[:2]
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(98)).numpy()
+    which = np.arange(n)
+    which[perm[:n_hi]] = best
+    which[perm[n_hi:n_hi + group]] = second
+    keys = base[torch.as_tensor(which, device="cuda")]
+    sc, eps = _oracle_scores(keys, qi[0], w[0], "fp4")
+    plane = gpu_plane("fp4", 128, [keys], n)
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, 64, n, k, P))
+    for _ in range(2):
+        idx, pool = b.csa_index_topk(plane, n_comp, n, qi, w, k, pool_out=P, ws=ws)
+        assert b.read_device_status(ws) == 0
+        idx, pool = idx.cpu().numpy()[0], pool.cpu().numpy()[0]
+        assert check_topk(pool, sc, eps, P, where="pool") == 0
+        assert check_topk(idx, sc, eps, k, where="top-k") == 0
+
+
 def test_index_out_of_range_pool_entry_is_flagged():
     b = ckv()
     keys, qi, w, plane = _case(1, [100], 8, "fp4", seed=9)
