@@ -513,7 +513,7 @@ ckv_status ckv_hca_attn(const ckv_plane* kv, const int32_t* n_comp, int32_t n_co
 }
 
 // A side stream and two events per host thread and device, made on first
-// use: the group call's Reindex passes overlap its first attention launch.
+// use: the group call's first attention launch overlaps its Reindex passes.
 struct SideResources {
   cudaStream_t s = nullptr;
   cudaEvent_t full = nullptr, re = nullptr;
@@ -545,14 +545,15 @@ cudaError_t side_resources(SideResources*& out) {
   return cudaSuccess;
 }
 
-// The group's passes with the Reindex passes on the side stream: caller's
-// stream: Full index (layer 0), then one attention launch of up to
-// kLayersPerLaunch layers whose indices come from the Full pass; side stream
-// (after the Full pass): the Reindex passes in layer order, then the
-// remaining layers' attention, in launches of at most kLayersPerLaunch split
-// evenly, beside the caller's stream's launch.  root[l]: the layer whose
-// index pass layer l uses.  The caller's stream finally waits for the side
-// stream, so everything the call enqueues is ordered before its next work.
+// The group's passes with one attention launch on the side stream: caller's
+// stream: Full index (layer 0), the Reindex passes in layer order (the first
+// of them launched beside the Full pass's tail by programmatic dependent
+// launch), then the remaining layers' attention in launches of at most
+// kLayersPerLaunch split evenly; side stream (after the Full pass): one
+// attention launch of up to kLayersPerLaunch layers whose indices come from
+// the Full pass, beside the Reindex passes.  root[l]: the layer whose index
+// pass layer l uses.  The caller's stream finally waits for the side stream,
+// so everything the call enqueues is ordered before its next work.
 ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const int32_t* n_comp,
                                  int n_comp_max, const int32_t* win_len, int B, int H, int HI,
                                  int topk, float sm_scale, int pool_len, int32_t* idxbuf,
@@ -570,13 +571,14 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
   if (s) return s;
   s = cuda_status(cudaEventRecord(side->full, st));
   if (s) return s;
-  // Reindex passes on the side stream
+  // Reindex passes on the caller's stream, the first attention launch on
+  // the side stream once the Full pass is done
   s = cuda_status(cudaStreamWaitEvent(side->s, side->full, 0));
   if (s) return s;
   for (int l = 1; l < L; ++l)
     if (g->role[l] == CKV_CSA2_REINDEX) {
       s = run_index(&g->idx_keys, n_comp, B, n_comp_max, g->q_idx[l], g->w[l], HI, topk, pool_buf,
-                    pool_len, own[l], nullptr, 0, nullptr, dst, idx_region, side->s);
+                    pool_len, own[l], nullptr, 0, nullptr, dst, idx_region, st);
       if (s) return s;
     }
   // launch order: the first kLayersPerLaunch Full-derived layers, then the rest
@@ -598,9 +600,9 @@ ckv_status csa2_group_overlapped(const ckv_csa2_group* g, const int* root, const
       const int left = L - j0, n_launch = (left + kLayersPerLaunch - 1) / kLayersPerLaunch;
       n_g = left / n_launch;
     }
-    // the first launch on the caller's stream, beside the Reindex passes;
-    // the later ones after those passes on the side stream
-    const cudaStream_t ls = gi == 0 ? st : side->s;
+    // the first launch on the side stream, beside the Reindex passes; the
+    // later ones after those passes on the caller's stream
+    const cudaStream_t ls = gi == 0 ? side->s : st;
     int rows_max = 0;
     for (int j = j0; j < j0 + n_g; ++j) {
       const int r = topk + (int)g->win[g->kv_src[order[j]]].cap;
@@ -709,9 +711,9 @@ ckv_status ckv_csa2_group_decode(const ckv_csa2_group* g, const int32_t* n_comp,
   }
   // Layers whose indices come from a Reindex pass (directly or by reuse)
   // wait for it; the others need only the Full pass of layer 0.  With one
-  // Full layer and at least one Reindex layer, the Reindex passes run on a
-  // side stream while the first attention launch (Full-derived layers only)
-  // runs on the caller's stream.
+  // Full layer and at least one Reindex layer, the first attention launch
+  // (Full-derived layers only) runs on a side stream beside the Reindex
+  // passes on the caller's stream.
   {
     int root[CKV_CSA2_MAX_LAYERS];
     bool one_full = true, any_re = false;

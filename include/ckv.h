@@ -334,14 +334,14 @@ ckv_status ckv_hca_attn_rope(const ckv_plane *kv, const int32_t *n_comp,
  * n_append rows to `append_dst` (as ckv_kv_append_quant).  The layers'
  * attention runs in launches of at most four layers each, so that every
  * launch's parameter block stays within the classic 4 KB.  With one FULL
- * layer (layer 0) and at least one REINDEX layer, the REINDEX passes run on
- * a side stream of the library's own (one per host thread and device, made
- * on first use), followed there by the attention of the layers that need
- * them, while the first attention launch -- up to four layers whose indices
- * come from the FULL pass -- runs on `stream`; `stream` finally waits for
- * the side stream, so everything the call enqueues is ordered before the
- * next work on `stream` (six layers FULL, REINDEX, 4 x REUSE of layer 0:
- * launches of four and two).  Otherwise the passes run in layer order on
+ * layer (layer 0) and at least one REINDEX layer, the first attention
+ * launch -- up to four layers whose indices come from the FULL pass -- runs
+ * on a side stream of the library's own (one per host thread and device,
+ * made on first use) beside the REINDEX passes, which run on `stream`
+ * followed there by the attention of the remaining layers; `stream` finally
+ * waits for the side stream, so everything the call enqueues is ordered
+ * before the next work on `stream` (six layers FULL, REINDEX, 4 x REUSE of
+ * layer 0: launches of four and two).  Otherwise the passes run in layer order on
  * `stream` (six layers: two launches of three).  The call refuses
  * to be captured into a CUDA graph: on
  * a capturing stream it returns CKV_ERR_UNSUPPORTED and enqueues nothing

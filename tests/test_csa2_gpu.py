@@ -16,8 +16,8 @@ pytestmark = pytest.mark.gpu
 TAU = 1.0 / math.sqrt(512)
 
 
-# Every wiring here has a Reindex layer, so the Reindex pass runs on the
-# library's side stream beside a first attention launch of the layers whose
+# Every wiring here has a Reindex layer, so the Reindex pass runs beside a
+# first attention launch, on the library's side stream, of the layers whose
 # indices come from the Full pass: the bench wiring (Reuse of layer 0) as
 # launches of four and L - 4 layers, the pages wiring (Reuse of the previous
 # layer) as layer 0 alone and then the rest in launches of at most four.
