@@ -64,6 +64,7 @@ constexpr uint32_t kOffQs = kOffQ + 64 * 64;                       // 64 x 8 sca
 constexpr uint32_t kOffW = kOffQs + 64 * 8;                        // 64 f32
 constexpr uint32_t kOffMerge = kOffW + 64 * 4;
 constexpr uint32_t kOffBar = (kOffMerge + sizeof(MergeSmem<kUThreads>) + 7) & ~7u;
+constexpr int kLongSequenceEntries = 131072;   // above: the kernel instance with the bitmap output
 constexpr int kDBuf = 4;          // TMEM accumulators: the MMA runs up to 3 tiles ahead
 constexpr int kNumBarU = 3 * kUStages + 2 * kDBuf;
 constexpr uint32_t kOffSlotU = kOffBar + kNumBarU * 8;
@@ -119,6 +120,7 @@ struct UmmaIndexArgs {
   int64_t row_limit;  // B * cap (rows of the key plane)
 };
 
+template <bool BM>
 __global__ void __launch_bounds__(kUThreads, 1)
     index_topk_umma_kernel(const __grid_constant__ CUtensorMap map_data,
                            const __grid_constant__ CUtensorMap map_scale, UmmaIndexArgs ua) {
@@ -469,8 +471,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (tr && tid == 0) a.st->pad[24] = T;
   __syncthreads();
   // The merge's survivors use the pipeline ring, dead by then.
-  chunk_select_and_merge<kUThreads>(a, b, chunk, n_elem, c0, keys, hist, reinterpret_cast<uint32_t*>(g),
-                                    kMergeScratchWords, msm);
+  chunk_select_and_merge<kUThreads, BM>(a, b, chunk, n_elem, c0, keys, hist,
+                                        reinterpret_cast<uint32_t*>(g), kMergeScratchWords, msm);
 }
 
 bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
@@ -485,8 +487,12 @@ bool index_umma_supported(const IndexArgs& a, int64_t batch_rows) {
 cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream_t stream) {
   static DeviceOnce once;
   const cudaError_t e = once_per_device(once, [](int) {
-    return cudaFuncSetAttribute(index_topk_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemU);
+    cudaError_t r = cudaFuncSetAttribute(index_topk_umma_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemU);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(index_topk_umma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemU);
+    return r;
   });
   if (e != cudaSuccess) return e;
   CUtensorMap md, ms;
@@ -510,7 +516,11 @@ cudaError_t launch_index_umma(const IndexArgs& a, int64_t batch_rows, cudaStream
   cudaLaunchAttribute at[1] = {pdl_attribute()};
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, index_topk_umma_kernel, md, ms, ua);
+  // Long sequences stage more candidates than one ordered pass of the merge
+  // takes at once: their instance writes the output from bitmaps.
+  const bool long_seq = a.n_comp_max > kLongSequenceEntries;
+  return cudaLaunchKernelEx(&cfg, long_seq ? index_topk_umma_kernel<true> : index_topk_umma_kernel<false>,
+                            md, ms, ua);
 }
 
 }  // namespace ckv

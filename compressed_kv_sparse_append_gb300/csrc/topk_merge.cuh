@@ -222,6 +222,53 @@ __device__ __forceinline__ void emit_ordered(const uint32_t* key, const int32_t*
   }
 }
 
+// The staged candidates whose top bits equal `prefix` (under hmask) into
+// the list (key, staged position; list slots past 2 x NT are dropped, the
+// count in sm.bcast[2] still counts them); with BM, every bitmap word of
+// bmA covered (32 consecutive candidates, from a warp's ballot) marks the
+// keys above that prefix and the same word of bmE is cleared.  Eight keys
+// per lane in flight, one counter update per warp and round.  Block-wide;
+// sm.bcast[2] must be 0 on entry (barrier after).
+template <int NT, bool BM>
+__device__ __forceinline__ void gather_sub_bin(const uint32_t* surv_key, int n_pad, uint32_t hmask,
+                                               uint32_t prefix, uint32_t* lkey, uint32_t* lpos,
+                                               uint32_t* bmA, uint32_t* bmE, MergeSmem<NT>& sm) {
+  constexpr int kU = 8, kListMax = 2 * NT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int w0 = warp * 32 * kU; w0 < n_pad; w0 += NT * kU) {
+    uint32_t u[kU], bal[kU], c = 0;
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int i = w0 + k * 32 + lane;
+      u[k] = i < n_pad ? surv_key[i] : 0u;
+      bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && (u[k] & hmask) == prefix);
+      if (BM) {
+        const uint32_t ba = __ballot_sync(0xffffffffu, (u[k] & hmask) > prefix);
+        if (lane == 0) {
+          bmA[(w0 >> 5) + k] = ba;
+          bmE[(w0 >> 5) + k] = 0u;
+        }
+      }
+      c += __popc(bal[k]);
+    }
+    if (c == 0u) continue;   // warp-uniform
+    uint32_t at = 0u;
+    if (lane == 0) at = atomicAdd(&sm.bcast[2], c);
+    at = __shfl_sync(0xffffffffu, at, 0);
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const uint32_t x = at + __popc(bal[k] & lt);
+      if (((bal[k] >> lane) & 1u) && x < (uint32_t)kListMax) {
+        lkey[x] = u[k];
+        lpos[x] = (uint32_t)(w0 + k * 32 + lane);
+      }
+      at += __popc(bal[k]);
+    }
+  }
+}
+
 // Leaves the sequence's histogram (bins in use: below seq[1] = top, from
 // kBins - seq[2] up) and its state words zero for the next call.  Block-wide.
 template <int NT>
@@ -242,8 +289,10 @@ __device__ __forceinline__ void clear_sequence_state(uint32_t* gh, uint32_t* seq
 
 // Merge of the sequence's candidates, run by its last CTA.  `scratch`
 // (scratch_words 32-bit words of shared memory, dead otherwise) holds the
-// survivors and, for a CSA2 Full layer, the pool.
-template <int NT>
+// survivors and, for a CSA2 Full layer, the pool.  BM: the kernel instance
+// for long sequences, whose merge writes the output of a large staged set
+// from bitmaps (the code stays out of the other instance).
+template <int NT, bool BM>
 __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uint32_t* scratch,
                                int scratch_words, uint32_t own_bound) {
   const bool tr = a.trace && b == 0 && threadIdx.x == 0;
@@ -404,10 +453,10 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     // then the top-k of the pool, which is the top-k of the sequence).  Per
     // job: the keys of the threshold bin counted by their next 8 bits, the
     // sub-bin holding the job's K-th largest, its keys (with their staged
-    // positions) gathered into a list in the dead sub-bin counters, the
-    // threshold T and the count `need` of keys equal to T to keep found on
-    // the list alone (every key above the sub-bin is kept), then one ordered
-    // pass over the staged candidates writes the output.
+    // positions) gathered into a list in the dead sub-bin counters while the
+    // keys above it are marked in a bitmap, the threshold T and the count
+    // `need` of keys equal to T to keep found on the list alone (every key
+    // above the sub-bin is kept), then the output written from the bitmaps.
     constexpr int kListMax = 2 * NT;   // 2 x kListMax words fit in wsub
     constexpr int kRankMax = 64;
     uint32_t* lkey = wsub;
@@ -489,35 +538,19 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       if (threadIdx.x == 0) sm.bcast[2] = 0u;
       __syncthreads();
       const uint32_t hmask = ~((1u << top_bits) - 1u);
-      {
-        // eight keys per lane in flight, one counter update per warp and round
-        constexpr int kU = 8;
-        const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll 1
-        for (int w0 = warp * 32 * kU; w0 < n_pad; w0 += NT * kU) {
-          uint32_t u[kU], bal[kU], c = 0;
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const int i = w0 + k * 32 + lane;
-            u[k] = i < n_pad ? surv_key[i] : 0u;
-            bal[k] = __ballot_sync(0xffffffffu, u[k] != 0u && (u[k] & hmask) == prefix);
-            c += __popc(bal[k]);
-          }
-          if (c == 0u) continue;   // warp-uniform
-          uint32_t at = 0u;
-          if (lane == 0) at = atomicAdd(&sm.bcast[2], c);
-          at = __shfl_sync(0xffffffffu, at, 0);
-#pragma unroll
-          for (int k = 0; k < kU; ++k) {
-            const uint32_t x = at + __popc(bal[k] & lt);
-            if (((bal[k] >> lane) & 1u) && x < (uint32_t)kListMax) {
-              lkey[x] = u[k];
-              lpos[x] = (uint32_t)(w0 + k * 32 + lane);
-            }
-            at += __popc(bal[k]);
-          }
-        }
-      }
+      // More staged candidates than one ordered pass takes in a round: one
+      // bit per staged candidate, in words after the list, where bmA marks
+      // the keys above the sub-bin (and later the list's keys above T) and
+      // bmE the list's keys equal to T, and the output is written from the
+      // bitmaps.  The gather below writes every word of bmA and bmE it
+      // covers (up to kU words past the staged length).
+      constexpr int kU = 8;
+      const int n_words = (n_pad + 31) >> 5;
+      uint32_t* bmA = lpos + kListMax;
+      uint32_t* bmE = bmA + n_words + kU;
+      const bool use_bm = BM && n_pad > NT * kU && 2 * kListMax + 2 * (n_words + kU) <= kWarps * 256;
+      if (use_bm) gather_sub_bin<NT, true>(surv_key, n_pad, hmask, prefix, lkey, lpos, bmA, bmE, sm);
+      else gather_sub_bin<NT, false>(surv_key, n_pad, hmask, prefix, lkey, lpos, bmA, bmE, sm);
       __syncthreads();
       const int m = (int)sm.bcast[2];
       if (m > kListMax) break;   // a crowded sub-bin: the compaction below
@@ -565,7 +598,53 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       if (tr) a.st->pad[31] = m;
       int32_t* out = pool_left ? a.out_pool + (int64_t)b * a.pool_out : oi;
       const int len = pool_left ? a.pool_out : a.topk;
-      emit_ordered<NT>(surv_key, surv_ent, n_pad, T, need, out, sm);
+      if (!use_bm) {
+        emit_ordered<NT>(surv_key, surv_ent, n_pad, T, need, out, sm);
+      } else {
+        // the list's keys above T and equal to T into the bitmaps
+#pragma unroll 1
+        for (int i = threadIdx.x; i < m; i += NT) {
+          const uint32_t u = lkey[i], ps = lpos[i];
+          if (u > T) atomicOr(&bmA[ps >> 5], 1u << (ps & 31u));
+          else if (u == T) atomicOr(&bmE[ps >> 5], 1u << (ps & 31u));
+        }
+        __syncthreads();
+        // Output position of a kept candidate = keys above T before it +
+        // min(keys equal to T before it, need), counted on the bitmaps:
+        // each thread a contiguous run of words, one scan of their counts.
+        const int per = (n_words + NT - 1) / NT;
+        const int wlo = min(n_words, (int)threadIdx.x * per), whi = min(n_words, wlo + per);
+        uint32_t ca = 0, ce = 0;
+#pragma unroll 1
+        for (int w = wlo; w < whi; ++w) {
+          ca += __popc(bmA[w]);
+          ce += __popc(bmE[w]);
+        }
+        uint32_t pa, pe, ta, te;
+        block_scan2<NT>(ca, ce, pa, pe, ta, te, sm.sel);
+#pragma unroll 1
+        for (int w = wlo; w < whi; ++w) {
+          const uint32_t wa = bmA[w], we = bmE[w];
+          uint32_t x = wa | we;
+          while (x) {
+            const int bit = __ffs(x) - 1;
+            x &= x - 1u;
+            const uint32_t lo = (1u << bit) - 1u;
+            const uint32_t na = pa + __popc(wa & lo), ne = pe + __popc(we & lo);
+            const int32_t ent = surv_ent[w * 32 + bit];
+            // (positions stay below kj by the choice of T and need; the
+            // test keeps a write inside the output row regardless)
+            if ((wa >> bit) & 1u) {
+              const uint32_t at = na + min(ne, need);
+              if (at < kj) out[at] = ent;
+            } else if (ne < need && na + ne < kj) {
+              out[na + ne] = ent;
+            }
+          }
+          pa += __popc(wa);
+          pe += __popc(we);
+        }
+      }
 #pragma unroll 1
       for (int i = (int)kj + (int)threadIdx.x; i < len; i += NT) out[i] = -1;
       if (pool_left) {
@@ -646,7 +725,7 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
 // the chunk's candidates and takes the ticket; the last CTA merges.
 // `scratch` (scratch_words words of shared memory, dead after this chunk's
 // candidates are written; may alias `keys` and `hist`) serves the merge.
-template <int NT>
+template <int NT, bool BM = false>
 __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int n_elem,
                                        int64_t first_entry, const uint32_t* keys, const uint32_t* hist,
                                        uint32_t* scratch, int scratch_words, MergeSmem<NT>& sm) {
@@ -757,7 +836,7 @@ __device__ void chunk_select_and_merge(const IndexArgs& a, int b, int chunk, int
   __syncthreads();
   if (sm.ticket != a.n_chunks - 1) return;
   __threadfence();
-  merge_and_emit<NT>(a, b, sm, scratch, scratch_words, bound);
+  merge_and_emit<NT, BM>(a, b, sm, scratch, scratch_words, bound);
 }
 
 }  // namespace ckv

@@ -51,6 +51,7 @@ def _gpu_selection_of(dbg_row, n, k):
     ("fp4", 64, [300, 9000], 512),                 # n_comp < k: -1 padding
     ("fp4", 64, [0, 5000, 1], 512),                # a sequence with no entries, one with one
     ("fp4", 16, [20000], 1024),                    # several chunks, k = 1024
+    ("fp4", 64, [140000, 133000], 512),            # the long-sequence kernel instance
     ("bf16", 8, [5000, 17], 64),
     ("bf16", 16, [2000], 256),                     # CUDA-core scorer sized for 16 heads
     ("bf16", 32, [1500, 900], 128),                # ... for 32 heads
@@ -103,6 +104,29 @@ def test_index_topk_exact_ties_go_to_lower_index():
     assert (sc == boundary).sum() > 1, "the test must put an exact tie on the boundary"
     assert np.array_equal(idx, oi.topk_set(sc, 512))
     assert np.array_equal(idx, _gpu_selection_of(d, n, 512))
+
+
+def test_index_long_sequence_exact_ties():
+    """The long-sequence kernel instance (more than 131 072 entries) on keys
+    whose ranks 481-544 are copied onto 5 % of the other entries: thousands
+    of staged candidates, exact ties across the top-512 boundary."""
+    b = ckv()
+    n = 140000
+    keys, qi, w, plane = _case(1, [n], 64, "fp4", seed=81)
+    sc, _ = _oracle_scores(keys[0], qi[0], w[0], "fp4")
+    order = np.lexsort((np.arange(n), -sc))
+    k2 = wl.inject_ties(keys[0], order, seed=4, frac=0.05, donor_lo=480, donor_hi=544)
+    plane = gpu_plane("fp4", 128, [k2], n)
+    sc, eps = _oracle_scores(k2, qi[0], w[0], "fp4")
+    n_comp = torch.tensor([n], dtype=torch.int32, device="cuda")
+    dbg = torch.zeros((1, n), device="cuda")
+    ws = b.new_workspace(b.workspace_bytes(b.OP_INDEX_TOPK, 1, 0, 64, n, 512, 0))
+    for _ in range(2):    # the second call checks that the workspace was left clean
+        idx = b.csa_index_topk(plane, n_comp, n, qi, w, 512, dbg_scores=dbg, ws=ws).cpu().numpy()[0]
+        assert b.read_device_status(ws) == 0
+        d = dbg.cpu().numpy()[0]
+        assert np.array_equal(idx, _gpu_selection_of(d, n, 512))
+        assert check_topk(idx, sc, eps, 512, where="long ties") == 0
 
 
 @pytest.mark.parametrize("fmt,HI,n_hi,group", [
