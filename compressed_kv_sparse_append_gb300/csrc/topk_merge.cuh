@@ -453,10 +453,11 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
     // then the top-k of the pool, which is the top-k of the sequence).  Per
     // job: the keys of the threshold bin counted by their next 8 bits, the
     // sub-bin holding the job's K-th largest, its keys (with their staged
-    // positions) gathered into a list in the dead sub-bin counters while the
-    // keys above it are marked in a bitmap, the threshold T and the count
-    // `need` of keys equal to T to keep found on the list alone (every key
-    // above the sub-bin is kept), then the output written from the bitmaps.
+    // positions) gathered into a list in the dead sub-bin counters, the
+    // threshold T and the count `need` of keys equal to T to keep found on
+    // the list alone (every key above the sub-bin is kept), then the output
+    // written by one ordered pass over the staged candidates or, in the
+    // long-sequence instance with many staged, from bitmaps.
     constexpr int kListMax = 2 * NT;   // 2 x kListMax words fit in wsub
     constexpr int kRankMax = 64;
     uint32_t* lkey = wsub;
@@ -538,12 +539,13 @@ __device__ void merge_and_emit(const IndexArgs& a, int b, MergeSmem<NT>& sm, uin
       if (threadIdx.x == 0) sm.bcast[2] = 0u;
       __syncthreads();
       const uint32_t hmask = ~((1u << top_bits) - 1u);
-      // More staged candidates than one ordered pass takes in a round: one
-      // bit per staged candidate, in words after the list, where bmA marks
-      // the keys above the sub-bin (and later the list's keys above T) and
-      // bmE the list's keys equal to T, and the output is written from the
-      // bitmaps.  The gather below writes every word of bmA and bmE it
-      // covers (up to kU words past the staged length).
+      // Long-sequence instance, more staged candidates than one ordered pass
+      // takes in a round: one bit per staged candidate, in words after the
+      // list, where bmA marks the keys above the sub-bin (and later the
+      // list's keys above T) and bmE the list's keys equal to T, and the
+      // output is written from the bitmaps.  The gather below then writes
+      // every word of bmA and bmE it covers (up to kU words past the staged
+      // length).
       constexpr int kU = 8;
       const int n_words = (n_pad + 31) >> 5;
       uint32_t* bmA = lpos + kListMax;
